@@ -1,0 +1,67 @@
+// Internal interface between the translation units of the MoE library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+struct WsHeader;
+
+// Chunk of tokens handled by one CTA of the top-k/histogram and scatter steps.
+constexpr int kChunkTokens = 64;
+
+// One call's resolved sizes and device pointers.
+struct Ctx {
+  const moe_weights* w;
+  int T, D, E, k, I;
+  int BM;          // rows per block-map entry
+  int max_blocks;  // capacity of the block map
+  int n_chunks;    // ceil(T / kChunkTokens)
+  const uint16_t* x;
+  uint16_t* y;
+  WsHeader* hdr;
+  float* logits;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* count;
+  int32_t* off;
+  int32_t* perm;
+  int32_t* inv;
+  int32_t* chunk;  // [n_chunks][E] per-chunk counts, then per-chunk bases
+  int32_t* blocks;
+  int32_t* n_blocks;
+  uint16_t* h;
+  float* y_acc;
+  cudaStream_t stream;
+};
+
+// Bookkeeping of launches: counts this library's kernels and, when kernel
+// timing is on, records an event after each one.
+void launch_done(const char* name, cudaStream_t s);
+void timing_begin(cudaStream_t s);
+
+// Routing: logits, top-k + weights + per-chunk histogram, scan + block map,
+// scatter. Returns the first CUDA error.
+cudaError_t route(const Ctx& c);
+
+// Combine accumulator: zero before, bf16 cast after the down projection.
+cudaError_t zero_yacc(const Ctx& c);
+cudaError_t cast_y(const Ctx& c);
+
+// Grouped-GEMM path (T above the GEMV threshold).
+cudaError_t gemm_simt(const Ctx& c);
+cudaError_t gemm_tc(const Ctx& c);
+bool gemm_tc_supported(const Ctx& c);
+
+// Decode GEMV path (a few rows).
+cudaError_t gemv(const Ctx& c);
+bool gemv_supported(const Ctx& c);
+
+cudaError_t debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, uint16_t* out,
+                          cudaStream_t s);
+
+}  // namespace moe

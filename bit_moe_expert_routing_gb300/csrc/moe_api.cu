@@ -1,0 +1,349 @@
+// C ABI of the 4-bit MoE layer: argument checks, workspace layout, path
+// selection and launch bookkeeping. Every step of the layer runs in this
+// library's kernels on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kDefaultBlockM = 128;
+
+struct Options {
+  int gemv_max_rows = 4;
+  int force_path = 0;
+  int kernel_timing = 0;
+  int gemm_impl = 0;
+};
+Options g_opt;
+std::mutex g_mu;
+
+thread_local int t_launches = 0;
+
+// Kernel timing: events recorded in stream order; consecutive pairs give
+// each kernel's device time.
+struct Mark {
+  const char* name;  // nullptr = start of a forward
+  cudaEvent_t ev;
+};
+std::vector<Mark> g_marks;
+std::vector<cudaEvent_t> g_free_events;
+
+cudaEvent_t take_event() {
+  if (!g_free_events.empty()) {
+    cudaEvent_t e = g_free_events.back();
+    g_free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+void mark(const char* name, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  cudaEvent_t e = take_event();
+  if (!e) return;
+  cudaEventRecord(e, s);
+  g_marks.push_back({name, e});
+}
+
+size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct Layout {
+  int BM, max_blocks, n_chunks;
+  size_t logits, topk_idx, topk_w, count, off, perm, inv, chunk, blocks, n_blocks, h, y_acc, total;
+};
+
+Layout layout(const moe_weights* w, int T) {
+  Layout L{};
+  const size_t A = size_t(T) * w->k;
+  L.BM = kDefaultBlockM;
+  L.n_chunks = (T + kChunkTokens - 1) / kChunkTokens;
+  L.max_blocks = int(A / L.BM + std::min<size_t>(w->E, A) + (T + L.BM - 1) / L.BM + 1);
+  size_t o = sizeof(WsHeader);
+  auto put = [&](size_t bytes) {
+    const size_t at = o;
+    o = al256(o + bytes);
+    return at;
+  };
+  L.logits = put(size_t(T) * w->E * 4);
+  L.topk_idx = put(A * 4);
+  L.topk_w = put(A * 4);
+  L.count = put(size_t(w->E) * 4);
+  L.off = put(size_t(w->E + 1) * 4);
+  L.perm = put(A * 4);
+  L.inv = put(A * 4);
+  L.chunk = put(size_t(L.n_chunks) * w->E * 4);
+  L.blocks = put(size_t(L.max_blocks) * 3 * 4);
+  L.n_blocks = put(4);
+  L.h = put((A + T) * size_t(w->I) * 2);
+  L.y_acc = put(size_t(T) * w->D * 4);
+  L.total = o;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+moe_status check_qmat(const moe_qmatrix& m) {
+  if (!m.codes || !m.scales || !m.biases) return MOE_ERR_ARG;
+  if (!aligned16(m.codes) || !aligned16(m.scales) || !aligned16(m.biases)) return MOE_ERR_ARG;
+  return MOE_OK;
+}
+
+moe_status check_weights(const moe_weights* w) {
+  if (!w) return MOE_ERR_ARG;
+  if (w->D < 64 || w->D > 16384 || w->D % 64 || w->I < 64 || w->I > 4096 || w->I % 64) return MOE_ERR_SHAPE;
+  if (w->k < 1 || w->k > 32 || w->E < w->k || w->E > 1024) return MOE_ERR_SHAPE;
+  if (!w->router_w || !aligned16(w->router_w)) return MOE_ERR_ARG;
+  const moe_qmatrix* ms[] = {&w->gate, &w->up, &w->down, &w->s_gate, &w->s_up, &w->s_down};
+  for (const moe_qmatrix* m : ms)
+    if (moe_status s = check_qmat(*m)) return s;
+  return MOE_OK;
+}
+
+constexpr int kMaxT = 1 << 20;
+
+moe_status make_ctx(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* ws, size_t ws_bytes,
+                    void* stream, Ctx* c) {
+  if (moe_status s = check_weights(w)) return s;
+  if (T < 0 || T > kMaxT) return MOE_ERR_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return MOE_ERR_WORKSPACE;
+  const Layout L = layout(w, T);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  char* base = static_cast<char*>(ws);
+  c->w = w;
+  c->T = T;
+  c->D = w->D;
+  c->E = w->E;
+  c->k = w->k;
+  c->I = w->I;
+  c->BM = L.BM;
+  c->max_blocks = L.max_blocks;
+  c->n_chunks = L.n_chunks;
+  c->x = x;
+  c->y = y;
+  c->hdr = reinterpret_cast<WsHeader*>(base);
+  c->logits = reinterpret_cast<float*>(base + L.logits);
+  c->topk_idx = reinterpret_cast<int32_t*>(base + L.topk_idx);
+  c->topk_w = reinterpret_cast<float*>(base + L.topk_w);
+  c->count = reinterpret_cast<int32_t*>(base + L.count);
+  c->off = reinterpret_cast<int32_t*>(base + L.off);
+  c->perm = reinterpret_cast<int32_t*>(base + L.perm);
+  c->inv = reinterpret_cast<int32_t*>(base + L.inv);
+  c->chunk = reinterpret_cast<int32_t*>(base + L.chunk);
+  c->blocks = reinterpret_cast<int32_t*>(base + L.blocks);
+  c->n_blocks = reinterpret_cast<int32_t*>(base + L.n_blocks);
+  c->h = reinterpret_cast<uint16_t*>(base + L.h);
+  c->y_acc = reinterpret_cast<float*>(base + L.y_acc);
+  c->stream = static_cast<cudaStream_t>(stream);
+  return MOE_OK;
+}
+
+void fill_view(const Ctx& c, moe_route_view* v) {
+  v->T = c.T;
+  v->block_m = c.BM;
+  v->max_blocks = c.max_blocks;
+  v->logits = c.logits;
+  v->topk_idx = c.topk_idx;
+  v->topk_w = c.topk_w;
+  v->count = c.count;
+  v->off = c.off;
+  v->perm = c.perm;
+  v->inv = c.inv;
+  v->blocks = c.blocks;
+  v->n_blocks = c.n_blocks;
+  v->h = c.h;
+  v->y_acc = c.y_acc;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+void launch_done(const char* name, cudaStream_t s) {
+  ++t_launches;
+  if (g_opt.kernel_timing) mark(name, s);
+}
+
+void timing_begin(cudaStream_t s) {
+  if (g_opt.kernel_timing) mark(nullptr, s);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_weights* w, int T) {
+  if (check_weights(w) != MOE_OK || T < 0 || T > kMaxT) return 0;
+  return layout(w, T).total;
+}
+
+size_t moe_host_staging_size(const moe_weights* w, int T) {
+  if (check_weights(w) != MOE_OK || T < 0 || T > kMaxT) return 0;
+  return 2 * al256(size_t(T) * w->D * 2);
+}
+
+moe_status moe_route(const moe_weights* w, const uint16_t* x, int T, void* workspace, size_t workspace_bytes,
+                     void* stream, moe_route_view* view) {
+  Ctx c;
+  if (moe_status s = make_ctx(w, x, T, nullptr, workspace, workspace_bytes, stream, &c)) return s;
+  if (T > 0 && (!x || !aligned16(x))) return MOE_ERR_ARG;
+  t_launches = 0;
+  if (view) fill_view(c, view);
+  if (T == 0) return MOE_OK;
+  timing_begin(c.stream);
+  return cuda_status(route(c));
+}
+
+moe_status moe_workspace_view(const moe_weights* w, int T, void* workspace, size_t workspace_bytes,
+                              moe_route_view* view) {
+  Ctx c;
+  if (!view) return MOE_ERR_ARG;
+  if (moe_status s = make_ctx(w, nullptr, T, nullptr, workspace, workspace_bytes, nullptr, &c)) return s;
+  fill_view(c, view);
+  return MOE_OK;
+}
+
+moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  Ctx c;
+  if (moe_status s = make_ctx(w, x, T, y, workspace, workspace_bytes, stream, &c)) return s;
+  t_launches = 0;
+  if (T == 0) return MOE_OK;
+  if (!x || !y || !aligned16(x) || !aligned16(y) || x == y) return MOE_ERR_ARG;
+  timing_begin(c.stream);
+  cudaError_t err = route(c);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  int path = g_opt.force_path;
+  if (path == 0) path = (T <= g_opt.gemv_max_rows) ? 1 : 2;
+  if (path == 1 && !gemv_supported(c)) path = 2;
+  if (path == 1) return cuda_status(gemv(c));
+  if (g_opt.gemm_impl == 0 && gemm_tc_supported(c)) return cuda_status(gemm_tc(c));
+  return cuda_status(gemm_simt(c));
+}
+
+moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, int T, uint16_t* y_host,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (check_weights(w) != MOE_OK) return check_weights(w);
+  if (T < 0 || T > kMaxT) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !y_host) return MOE_ERR_ARG;
+  const size_t need = moe_workspace_size(w, T), stage = al256(size_t(T) * w->D * 2);
+  if (!workspace || workspace_bytes < need + 2 * stage) return MOE_ERR_WORKSPACE;
+  char* base = static_cast<char*>(workspace);
+  uint16_t* xd = reinterpret_cast<uint16_t*>(base + need);
+  uint16_t* yd = reinterpret_cast<uint16_t*>(base + need + stage);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = size_t(T) * w->D * 2;
+  if (cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+  moe_status st = moe_layer_forward(w, xd, T, yd, workspace, need, stream);
+  if (st != MOE_OK) return st;
+  if (cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_get_device_status(void* workspace, void* stream) {
+  if (!workspace) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  WsHeader h;
+  if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h.status != 0) {
+    const int zero[2] = {0, 0};
+    if (cudaMemcpy(workspace, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return static_cast<moe_status>(h.status);
+}
+
+moe_status moe_set_option(int option, int value) {
+  switch (option) {
+    case MOE_OPT_GEMV_MAX_ROWS:
+      if (value < 0 || value > 8) return MOE_ERR_ARG;
+      g_opt.gemv_max_rows = value;
+      return MOE_OK;
+    case MOE_OPT_FORCE_PATH:
+      if (value < 0 || value > 2) return MOE_ERR_ARG;
+      g_opt.force_path = value;
+      return MOE_OK;
+    case MOE_OPT_KERNEL_TIMING:
+      if (value < 0 || value > 1) return MOE_ERR_ARG;
+      g_opt.kernel_timing = value;
+      return MOE_OK;
+    case MOE_OPT_GEMM_IMPL:
+      if (value < 0 || value > 1) return MOE_ERR_ARG;
+      g_opt.gemm_impl = value;
+      return MOE_OK;
+    default:
+      return MOE_ERR_ARG;
+  }
+}
+
+int moe_get_option(int option) {
+  switch (option) {
+    case MOE_OPT_GEMV_MAX_ROWS: return g_opt.gemv_max_rows;
+    case MOE_OPT_FORCE_PATH: return g_opt.force_path;
+    case MOE_OPT_KERNEL_TIMING: return g_opt.kernel_timing;
+    case MOE_OPT_GEMM_IMPL: return g_opt.gemm_impl;
+    default: return -1;
+  }
+}
+
+moe_status moe_kernel_times(const char** names, float* total_ms, int* launches, int max, int* n) {
+  if (!n || max < 0 || (max > 0 && (!names || !total_ms || !launches))) return MOE_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  *n = 0;
+  if (!g_marks.empty() && cudaEventSynchronize(g_marks.back().ev) != cudaSuccess) return MOE_ERR_CUDA;
+  for (size_t i = 1; i < g_marks.size(); ++i) {
+    if (!g_marks[i].name) continue;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_marks[i - 1].ev, g_marks[i].ev) != cudaSuccess) return MOE_ERR_CUDA;
+    int slot = -1;
+    for (int j = 0; j < *n; ++j)
+      if (std::strcmp(names[j], g_marks[i].name) == 0) slot = j;
+    if (slot < 0) {
+      if (*n >= max) continue;
+      slot = (*n)++;
+      names[slot] = g_marks[i].name;
+      total_ms[slot] = 0.f;
+      launches[slot] = 0;
+    }
+    total_ms[slot] += ms;
+    launches[slot] += 1;
+  }
+  for (const Mark& m : g_marks) g_free_events.push_back(m.ev);
+  g_marks.clear();
+  return MOE_OK;
+}
+
+moe_status moe_debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, uint16_t* out, void* stream) {
+  if (!m || !out || !m->codes || !m->scales || !m->biases) return MOE_ERR_ARG;
+  if (expert < 0 || rows < 1 || K < 64 || K % 64) return MOE_ERR_SHAPE;
+  return cuda_status(debug_dequant(m, expert, rows, K, out, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_last_launch_count(void) { return t_launches; }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

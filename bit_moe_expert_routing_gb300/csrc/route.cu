@@ -1,0 +1,333 @@
+// GPU-resident expert routing: router logits, top-k with renormalised
+// weights, per-expert histogram, exclusive scan, scatter into expert groups
+// and the block map of fixed-size row blocks. All on the caller's stream,
+// with no host synchronisation ("Optimizing on-device inference for Apple
+// Silicon", section "Keep expert routing on the GPU").
+//
+// Router logits use one fixed fp32 evaluation order so that the top-k
+// decision (an integer result) is reproducible by any implementation:
+//   acc[l] = 0, l = 0..31
+//   for c = 0 .. D/32-1:  acc[l] = fma(float(x[t, 32c+l]), W_r[e, 32c+l], acc[l])
+//   for off = 16, 8, 4, 2, 1:  acc[l] = acc[l] + acc[l+off]   (l < off)
+//   logit = acc[0] (+ bias[e])
+// Lane l of a warp owns partial sum l; the tree is a shuffle-down reduction.
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kRouterWarps = 8;
+constexpr int kRouterDChunk = 1024;  // x columns staged in shared memory per pass
+
+// Logits of TT tokens x (kRouterWarps * EPW) experts. Tokens are processed in
+// pairs with the packed fp32 FMA (two independent correctly rounded FMAs).
+template <int TT, int EPW>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+    router_logits_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
+                         const float* __restrict__ bias, int T, int D, int E,
+                         float* __restrict__ logits) {
+  static_assert(TT % 2 == 0, "tokens go in pairs");
+  __shared__ __align__(16) uint16_t xs[TT * kRouterDChunk];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * TT;
+  const int e0 = (blockIdx.y * kRouterWarps + warp) * EPW;
+
+  float2 acc[TT / 2][EPW];
+#pragma unroll
+  for (int i = 0; i < TT / 2; ++i)
+#pragma unroll
+    for (int j = 0; j < EPW; ++j) acc[i][j] = make_float2(0.f, 0.f);
+
+  const float* wrow[EPW];
+#pragma unroll
+  for (int j = 0; j < EPW; ++j) wrow[j] = wr + size_t(min(e0 + j, E - 1)) * D;
+
+  for (int d0 = 0; d0 < D; d0 += kRouterDChunk) {
+    const int dc = min(kRouterDChunk, D - d0);  // a multiple of 64
+    __syncthreads();
+    for (int i = threadIdx.x; i < TT * (dc / 8); i += blockDim.x) {
+      const int t = i / (dc / 8), c8 = i % (dc / 8);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (t0 + t < T) v = *reinterpret_cast<const uint4*>(x + size_t(t0 + t) * D + d0 + c8 * 8);
+      *reinterpret_cast<uint4*>(xs + t * kRouterDChunk + c8 * 8) = v;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int c = 0; c < dc / 32; ++c) {
+      float wv[EPW];
+#pragma unroll
+      for (int j = 0; j < EPW; ++j) wv[j] = __ldg(wrow[j] + d0 + 32 * c + lane);
+#pragma unroll
+      for (int i = 0; i < TT / 2; ++i) {
+        const float2 xv = make_float2(bf16_to_f32(xs[(2 * i) * kRouterDChunk + 32 * c + lane]),
+                                      bf16_to_f32(xs[(2 * i + 1) * kRouterDChunk + 32 * c + lane]));
+#pragma unroll
+        for (int j = 0; j < EPW; ++j) acc[i][j] = __ffma2_rn(xv, make_float2(wv[j], wv[j]), acc[i][j]);
+      }
+    }
+  }
+
+#pragma unroll
+  for (int i = 0; i < TT / 2; ++i)
+#pragma unroll
+    for (int j = 0; j < EPW; ++j) {
+      float a = acc[i][j].x, b = acc[i][j].y;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        a = __fadd_rn(a, __shfl_down_sync(0xffffffffu, a, off));
+        b = __fadd_rn(b, __shfl_down_sync(0xffffffffu, b, off));
+      }
+      const int e = e0 + j, t = t0 + 2 * i;
+      if (lane == 0 && e < E) {
+        const float be = bias ? bias[e] : 0.f;
+        if (t < T) logits[size_t(t) * E + e] = bias ? __fadd_rn(a, be) : a;
+        if (t + 1 < T) logits[size_t(t + 1) * E + e] = bias ? __fadd_rn(b, be) : b;
+      }
+    }
+}
+
+// Top-k of each token (larger logit first, lower expert index on ties),
+// weights softmax-renormalised over the k kept, and this chunk's per-expert
+// assignment counts. One warp per token; lane l holds logits l, l+32, ...
+constexpr int kMaxPerLane = 32;  // E <= 1024
+
+__global__ void __launch_bounds__(256)
+    topk_hist_kernel(const float* __restrict__ logits, int T, int E, int k,
+                     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                     int32_t* __restrict__ chunk_count) {
+  extern __shared__ int hist[];  // [E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int M = (E + 31) / 32;
+  for (int tt = warp; tt < kChunkTokens; tt += blockDim.x / 32) {
+    const int t = blockIdx.x * kChunkTokens + tt;
+    if (t >= T) break;
+    const float* lg = logits + size_t(t) * E;
+    float v[kMaxPerLane];
+    unsigned taken = 0;
+#pragma unroll
+    for (int m = 0; m < kMaxPerLane; ++m) {
+      const int e = lane + 32 * m;
+      v[m] = (m < M && e < E) ? lg[e] : 0.f;
+      if (!(m < M && e < E)) taken |= 1u << m;
+    }
+    float first = 0.f, myv = 0.f;
+    int myi = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int m = 0; m < kMaxPerLane; ++m) {
+        const int e = lane + 32 * m;
+        if (!((taken >> m) & 1u) && (v[m] > bv || (v[m] == bv && e < bi))) {
+          bv = v[m];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (j == 0) first = bv;
+      if (lane == j) {
+        myv = bv;
+        myi = bi;
+      }
+    }
+    const float ex = lane < k ? expf(myv - first) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane < k) {
+      topk_idx[size_t(t) * k + lane] = myi;
+      topk_w[size_t(t) * k + lane] = ex / sum;
+      atomicAdd(&hist[myi], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_count[size_t(blockIdx.x) * E + e] = hist[e];
+}
+
+// Exclusive scan over the threads of one CTA (blockDim.x <= 1024, a multiple of 32).
+__device__ int block_exclusive_scan(int v, int* s_warp, int* s_total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += o;
+  }
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int w = lane < nw ? s_warp[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += o;
+    }
+    if (lane < nw) s_warp[lane] = wi - w;
+    if (lane == nw - 1) *s_total = wi;
+  }
+  __syncthreads();
+  const int r = s_warp[warp] + inc - v;
+  __syncthreads();
+  return r;
+}
+
+// Totals, offsets, per-chunk bases and the block map. One CTA of 1024 threads;
+// thread e owns expert e (E <= 1024).
+__global__ void __launch_bounds__(1024)
+    scan_blocks_kernel(int T, int E, int k, int BM, int n_chunks, int max_blocks,
+                       int32_t* __restrict__ chunk, int32_t* __restrict__ count,
+                       int32_t* __restrict__ off, int32_t* __restrict__ blocks,
+                       int32_t* __restrict__ n_blocks, WsHeader* hdr) {
+  __shared__ int s_warp[32];
+  __shared__ int s_tot_rows, s_tot_blocks;
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < E) {
+    for (int c = 0; c < n_chunks; ++c) {
+      const int v = chunk[size_t(c) * E + e];
+      chunk[size_t(c) * E + e] = total;
+      total += v;
+    }
+  }
+  const int nb = (total + BM - 1) / BM;
+  const int ex_off = block_exclusive_scan(total, s_warp, &s_tot_rows);
+  const int ex_nb = block_exclusive_scan(nb, s_warp, &s_tot_blocks);
+  if (e < E) {
+    count[e] = total;
+    off[e] = ex_off;
+    for (int c = 0; c < n_chunks; ++c) chunk[size_t(c) * E + e] += ex_off;
+    for (int b = 0; b < nb; ++b) {
+      const int idx = ex_nb + b;
+      if (idx < max_blocks) {
+        blocks[3 * idx + 0] = e;
+        blocks[3 * idx + 1] = ex_off + b * BM;
+        blocks[3 * idx + 2] = min(BM, total - b * BM);
+      }
+    }
+  }
+  if (e == 0) off[E] = s_tot_rows;
+  const int routed_blocks = s_tot_blocks;
+  const int shared_blocks = (T + BM - 1) / BM;
+  for (int s = threadIdx.x; s < shared_blocks; s += blockDim.x) {
+    const int idx = routed_blocks + s;
+    if (idx < max_blocks) {
+      blocks[3 * idx + 0] = E;
+      blocks[3 * idx + 1] = T * k + s * BM;
+      blocks[3 * idx + 2] = min(BM, T - s * BM);
+    }
+  }
+  if (threadIdx.x == 0) {
+    const int total_blocks = routed_blocks + shared_blocks;
+    *n_blocks = min(total_blocks, max_blocks);
+    if (total_blocks > max_blocks || s_tot_rows != T * k) report(hdr, MOE_ERR_DEVICE_CHECK, 1);
+  }
+}
+
+// Scatter: position of assignment a = its expert's base for this chunk plus
+// the number of earlier assignments of the chunk to the same expert, so the
+// permutation is unique (ascending a inside every expert segment).
+__global__ void __launch_bounds__(256)
+    scatter_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
+                   const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm,
+                   int32_t* __restrict__ inv, WsHeader* hdr) {
+  extern __shared__ int sm[];
+  int* base = sm;      // [E]
+  int* wh = sm + E;    // [8][E] per-warp counts of the current round
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) base[e] = chunk_base[size_t(blockIdx.x) * E + e];
+  for (int i = threadIdx.x; i < 8 * E; i += blockDim.x) wh[i] = 0;
+  __syncthreads();
+  const int a0 = blockIdx.x * kChunkTokens * k;
+  const int a1 = min(T, (blockIdx.x + 1) * kChunkTokens) * k;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int r0 = a0; r0 < a1; r0 += blockDim.x) {
+    const int a = r0 + threadIdx.x;
+    const bool valid = a < a1;
+    int e = valid ? topk_idx[a] : -1;
+    if (valid && (e < 0 || e >= E)) {
+      report(hdr, MOE_ERR_DEVICE_CHECK, 5);
+      e = 0;
+    }
+    const unsigned act = __ballot_sync(0xffffffffu, valid);
+    unsigned peers = 0;
+    int rank = 0;
+    if (valid) {
+      peers = __match_any_sync(act, e);
+      rank = __popc(peers & lt);
+      if (rank == 0) wh[warp * E + e] = __popc(peers);
+    }
+    __syncthreads();
+    if (valid) {
+      int pos = base[e] + rank;
+      for (int w2 = 0; w2 < warp; ++w2) pos += wh[w2 * E + e];
+      if (pos >= 0 && pos < T * k) {
+        perm[pos] = a;
+        inv[a] = pos;
+      } else {
+        report(hdr, MOE_ERR_DEVICE_CHECK, 4);
+      }
+    }
+    __syncthreads();
+    if (valid && rank == 0) {
+      atomicAdd(&base[e], __popc(peers));
+      wh[warp * E + e] = 0;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t route(const Ctx& c) {
+  const moe_weights* w = c.w;
+  cudaError_t err;
+  if (c.T <= 2) {
+    dim3 grid(c.T > 0 ? (c.T + 1) / 2 : 1, (c.E + kRouterWarps - 1) / kRouterWarps);
+    router_logits_kernel<2, 1><<<grid, kRouterWarps * 32, 0, c.stream>>>(c.x, w->router_w, w->router_bias,
+                                                                          c.T, c.D, c.E, c.logits);
+  } else if (c.T <= 8) {
+    dim3 grid(1, (c.E + kRouterWarps - 1) / kRouterWarps);
+    router_logits_kernel<8, 1><<<grid, kRouterWarps * 32, 0, c.stream>>>(c.x, w->router_w, w->router_bias,
+                                                                          c.T, c.D, c.E, c.logits);
+  } else {
+    dim3 grid((c.T + 15) / 16, (c.E + 8 * kRouterWarps - 1) / (8 * kRouterWarps));
+    router_logits_kernel<16, 8><<<grid, kRouterWarps * 32, 0, c.stream>>>(c.x, w->router_w, w->router_bias,
+                                                                           c.T, c.D, c.E, c.logits);
+  }
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  launch_done("router_logits", c.stream);
+
+  topk_hist_kernel<<<c.n_chunks, 256, c.E * sizeof(int), c.stream>>>(c.logits, c.T, c.E, c.k, c.topk_idx,
+                                                                     c.topk_w, c.chunk);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  launch_done("topk_hist", c.stream);
+
+  scan_blocks_kernel<<<1, 1024, 0, c.stream>>>(c.T, c.E, c.k, c.BM, c.n_chunks, c.max_blocks, c.chunk,
+                                               c.count, c.off, c.blocks, c.n_blocks, c.hdr);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  launch_done("scan_blocks", c.stream);
+
+  scatter_kernel<<<c.n_chunks, 256, 9 * c.E * sizeof(int), c.stream>>>(c.topk_idx, c.T, c.E, c.k, c.chunk,
+                                                                       c.perm, c.inv, c.hdr);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  launch_done("scatter", c.stream);
+  return cudaSuccess;
+}
+
+}  // namespace moe

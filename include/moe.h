@@ -1,0 +1,188 @@
+/* moe.h — C ABI of the GB300 4-bit mixture-of-experts FFN layer.
+ *
+ * The layer (from "Optimizing on-device inference for Apple Silicon",
+ * Perplexity 2026, sections "Qwen creates three workload shapes",
+ * "Dequantise weights during matrix multiplication", "Keep expert routing on
+ * the GPU", "Optimise the single-row weight path" and "Reduce intermediate and
+ * state traffic"):
+ *
+ *   logits[t,e] = x[t,:] . W_r[e,:] (+ bias[e])                     fp32
+ *   top-k experts of each token (larger logit first, lower index on ties),
+ *   weights w[t,j] = softmax over all E, renormalised over the k kept
+ *   h = silu(x . dq(W_gate[e])^T) * (x . dq(W_up[e])^T)               bf16
+ *   y[t] = sum_j w[t,j] * (h . dq(W_down[e_j])^T) + shared expert     bf16
+ *
+ * where dq(W)[n,kk] = scale[n,kk/64] * code[n,kk] + bias[n,kk/64]: 4-bit
+ * codes, one bf16 scale and one bf16 bias per group of 64 weights along each
+ * matrix's input axis.
+ *
+ * Conventions for every entry point:
+ *   - Row-major arrays. bf16 values travel as their uint16_t bit patterns.
+ *   - "device" pointers are CUDA device memory owned by the caller; the
+ *     library never frees or retains them past the call (work is enqueued on
+ *     the caller's stream and may still be running when the call returns).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Nothing throws across the ABI. Argument and shape errors are found on
+ *     the host before anything is enqueued and return MOE_ERR_ARG /
+ *     MOE_ERR_SHAPE / MOE_ERR_WORKSPACE. Launch failures return MOE_ERR_CUDA.
+ *     Errors found by the kernels themselves (bounded waits that gave up,
+ *     index checks) are recorded in a status word inside the workspace and
+ *     reported by moe_get_device_status().
+ *   - Not re-entrant on one workspace: two calls that overlap on the GPU must
+ *     use distinct workspaces. Distinct workspaces and streams are
+ *     independent. Options (moe_set_option) are process-wide.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = 1,            /* null pointer, bad option, negative T */
+  MOE_ERR_SHAPE = 2,          /* D, I not multiples of 64; k, E out of range */
+  MOE_ERR_WORKSPACE = 3,      /* workspace NULL, too small or not 256-byte aligned */
+  MOE_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait gave up */
+  MOE_ERR_DEVICE_CHECK = 6    /* a device-side index/size check failed */
+} moe_status;
+
+/* One packed 4-bit matrix family of n_exp experts, each rows x K:
+ *   codes  [n_exp, rows, K/8] uint32; code j (0..7) of word m is bits
+ *          4j..4j+3 and holds element 8m+j of the row;
+ *   scales [n_exp, rows, K/64] bf16, biases the same: group g of a row covers
+ *          elements 64g..64g+63 (the matrix's input axis).
+ * All three are device pointers, 16-byte aligned. */
+typedef struct {
+  const uint32_t* codes;
+  const uint16_t* scales;
+  const uint16_t* biases;
+} moe_qmatrix;
+
+/* The layer's weights (all device pointers, caller-owned).
+ *   D hidden size, E routed experts, k experts kept per token, I expert
+ *   intermediate size. Requirements: D % 64 == 0, I % 64 == 0 (one quant
+ *   group is 64), 64 <= D <= 16384, 64 <= I <= 4096, 1 <= k <= E <= 1024,
+ *   k <= 32.
+ *   router_w    fp32 [E, D]
+ *   router_bias fp32 [E] or NULL (added to the logits; NULL = no bias)
+ *   gate, up    [E, I, D] (input axis D)      down   [E, D, I] (input axis I)
+ *   s_gate, s_up [1, I, D]  s_down [1, D, I]   the shared expert, weight 1 */
+typedef struct {
+  int D, E, k, I;
+  const float* router_w;
+  const float* router_bias;
+  moe_qmatrix gate, up, down;
+  moe_qmatrix s_gate, s_up, s_down;
+} moe_weights;
+
+/* Device pointers into a workspace after moe_route()/moe_layer_forward(),
+ * for inspection (tests, diagnostics). Valid until the workspace is reused.
+ *   logits    fp32 [T, E]
+ *   topk_idx  int32 [T, k]     topk_w fp32 [T, k]
+ *   count     int32 [E]        off    int32 [E+1] exclusive scan of count
+ *   perm      int32 [T*k]      row p of the permuted order holds assignment
+ *                              a = t*k + j; inside an expert's segment rows
+ *                              are in ascending a
+ *   inv       int32 [T*k]      inv[perm[p]] = p
+ *   blocks    int32 [max_blocks][3] = (group, first row, rows): for each
+ *             expert in ascending order its segment cut into blocks of
+ *             block_m rows, then the shared expert as group E over rows
+ *             T*k .. T*k+T-1 (token t at row T*k+t)
+ *   n_blocks  int32 [1]        number of valid entries of blocks
+ *   h         bf16 [T*k + T, I]  SwiGLU intermediate in the permuted order
+ *                                (the shared expert's rows last)
+ *   y_acc     fp32 [T, D]      the combine accumulator (GEMM path) */
+typedef struct {
+  int T, block_m, max_blocks;
+  float* logits;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* count;
+  int32_t* off;
+  int32_t* perm;
+  int32_t* inv;
+  int32_t* blocks;
+  int32_t* n_blocks;
+  uint16_t* h;
+  float* y_acc;
+} moe_route_view;
+
+/* Options (process-wide). */
+typedef enum {
+  MOE_OPT_GEMV_MAX_ROWS = 1, /* T <= this runs the decode GEMV path (default 4) */
+  MOE_OPT_FORCE_PATH = 2,    /* 0 auto by row count, 1 GEMV, 2 grouped GEMM */
+  MOE_OPT_KERNEL_TIMING = 3, /* 1: record CUDA events around each kernel of
+                                the next forwards (read with moe_kernel_times) */
+  MOE_OPT_GEMM_IMPL = 4      /* 0 tensor-core (tcgen05) grouped GEMM, 1 CUDA-core
+                                grouped GEMM (the comparison baseline) */
+} moe_option;
+
+/* Bytes of workspace one call with T tokens needs (pure host; 0 on bad
+ * arguments). The workspace also holds the device status word. */
+size_t moe_workspace_size(const moe_weights* w, int T);
+
+/* The whole layer on the GPU: routing (logits, top-k, weights, histogram,
+ * scan, scatter, block map), then either the grouped-GEMM path or the decode
+ * GEMV path, then the combine into y. Everything is enqueued on `stream` with
+ * no host synchronisation. x: device bf16 [T, D]; y: device bf16 [T, D]
+ * (may not alias x); workspace: device, >= moe_workspace_size(w, T) bytes,
+ * 256-byte aligned. T = 0 is a no-op returning MOE_OK. */
+moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uint16_t* y,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Same layer with HOST x and y: copies x into the workspace, runs
+ * moe_layer_forward, copies y back and synchronises `stream` before it
+ * returns. Page-locked host buffers make the copies asynchronous DMA. The
+ * workspace must hold moe_workspace_size(w, T) + moe_host_staging_size(w, T). */
+size_t moe_host_staging_size(const moe_weights* w, int T);
+moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, int T,
+                                  uint16_t* y_host, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/* Routing only (the first five steps of the layer), on `stream`, no host
+ * sync; fills `view` with device pointers into the workspace. The tables are
+ * the ones moe_layer_forward builds for the same T (same block_m). */
+moe_status moe_route(const moe_weights* w, const uint16_t* x, int T, void* workspace,
+                     size_t workspace_bytes, void* stream, moe_route_view* view);
+
+/* Device pointers of the workspace arrays for T tokens without running
+ * anything (e.g. to read h after moe_layer_forward). */
+moe_status moe_workspace_view(const moe_weights* w, int T, void* workspace,
+                              size_t workspace_bytes, moe_route_view* view);
+
+/* Synchronises `stream`, then returns (and clears) the device status word of
+ * `workspace`: MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_CHECK. */
+moe_status moe_get_device_status(void* workspace, void* stream);
+
+moe_status moe_set_option(int option, int value);
+int moe_get_option(int option);
+
+/* With MOE_OPT_KERNEL_TIMING on, every forward records a CUDA event on its
+ * stream before its first kernel and after each kernel. This call waits for
+ * the last recorded event, then sums the device time of each kernel name over
+ * all forwards since the previous call: up to `max` entries of (static name
+ * string, total milliseconds, launches); *n gets the entry count. It then
+ * forgets those events. */
+moe_status moe_kernel_times(const char** names, float* total_ms, int* launches, int max, int* n);
+
+/* Dequantises rows x K of expert `expert` of `m` into bf16 [rows, K] on the
+ * device with the conversion the tensor-core GEMM uses (one round to nearest
+ * even of scale*code + bias). A diagnostic of the weight format. */
+moe_status moe_debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, uint16_t* out,
+                             void* stream);
+
+/* Number of this library's kernels the last forward on this thread launched. */
+int moe_last_launch_count(void);
+
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

@@ -1,0 +1,113 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every entry
+point include/moe.h declares, and rejects bad arguments on the host before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_moe_expert_routing_gb300 as moe
+from bit_moe_expert_routing_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return moe.lib()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    syms = declared_symbols()
+    assert "moe_layer_forward" in syms and "moe_route" in syms and len(syms) >= 10
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in moe.SIGNATURES, f"binding lacks {name}"
+
+
+def _weights(D=256, E=16, k=2, I=128, ptr=0x1000):
+    q = moe.moe_qmatrix(ptr, ptr, ptr)
+    return moe.moe_weights(D, E, k, I, ptr, None, q, q, q, q, q, q)
+
+
+def test_workspace_size_and_shape_checks(lib):
+    w = _weights()
+    assert moe.moe_workspace_size(w, 16) > 0
+    assert moe.moe_workspace_size(w, 0) > 0
+    assert moe.moe_workspace_size(w, -1) == 0
+    for bad in (dict(D=100), dict(I=96), dict(k=0), dict(k=17), dict(E=2000, k=2), dict(k=33, E=64)):
+        assert moe.moe_workspace_size(_weights(**bad), 4) == 0, bad
+    # grows with T
+    assert moe.moe_workspace_size(w, 4096) > moe.moe_workspace_size(w, 16)
+
+
+def test_host_side_validation_needs_no_gpu(lib):
+    w = _weights()
+    ws = 0x100000
+    n = moe.moe_workspace_size(w, 4)
+    # workspace too small, misaligned or missing: rejected before any CUDA call
+    assert moe.moe_layer_forward(w, 0x2000, 4, 0x3000, ws, n - 1, None) == moe.MOE_ERR_WORKSPACE
+    assert moe.moe_layer_forward(w, 0x2000, 4, 0x3000, ws + 16, n, None) == moe.MOE_ERR_WORKSPACE
+    assert moe.moe_layer_forward(w, 0x2000, 4, 0x3000, None, n, None) == moe.MOE_ERR_WORKSPACE
+    # bad shapes and pointers
+    assert moe.moe_layer_forward(_weights(D=100), 0x2000, 4, 0x3000, ws, n, None) == moe.MOE_ERR_SHAPE
+    assert moe.moe_layer_forward(w, 0x2000, -1, 0x3000, ws, n, None) == moe.MOE_ERR_ARG
+    assert moe.moe_layer_forward(w, None, 4, 0x3000, ws, n, None) == moe.MOE_ERR_ARG
+    assert moe.moe_layer_forward(w, 0x2000, 4, 0x2000, ws, n, None) == moe.MOE_ERR_ARG  # y aliases x
+    assert moe.moe_layer_forward(w, 0x2001, 4, 0x3000, ws, n, None) == moe.MOE_ERR_ARG  # unaligned x
+    nullw = _weights(ptr=0)
+    assert moe.moe_layer_forward(nullw, 0x2000, 4, 0x3000, ws, n, None) == moe.MOE_ERR_ARG
+    # T = 0 is a no-op
+    assert moe.moe_layer_forward(w, 0x2000, 0, 0x3000, ws, moe.moe_workspace_size(w, 0), None) == moe.MOE_OK
+    assert moe.moe_last_launch_count() == 0
+
+
+def test_workspace_view_layout(lib):
+    w = _weights(D=256, E=16, k=2, I=128)
+    T = 37
+    n = moe.moe_workspace_size(w, T)
+    v = moe.moe_route_view()
+    base = 1 << 30
+    assert moe.moe_workspace_view(w, T, base, n, v) == moe.MOE_OK
+    assert v.T == T and v.block_m == 128
+    ptrs = [v.logits, v.topk_idx, v.topk_w, v.count, v.off, v.perm, v.inv, v.blocks, v.n_blocks, v.h, v.y_acc]
+    assert all(p % 256 == 0 for p in ptrs)
+    assert all(base < p < base + n for p in ptrs)
+    assert ptrs == sorted(ptrs)
+    assert v.y_acc + T * 256 * 4 <= base + n
+    assert v.max_blocks >= (T * 2) // 128 + min(16, T * 2) + 1
+
+
+def test_options(lib):
+    old = moe.moe_get_option(moe.MOE_OPT_GEMV_MAX_ROWS)
+    assert moe.moe_set_option(moe.MOE_OPT_GEMV_MAX_ROWS, 3) == moe.MOE_OK
+    assert moe.moe_get_option(moe.MOE_OPT_GEMV_MAX_ROWS) == 3
+    assert moe.moe_set_option(moe.MOE_OPT_GEMV_MAX_ROWS, 99) == moe.MOE_ERR_ARG
+    assert moe.moe_set_option(moe.MOE_OPT_FORCE_PATH, 3) == moe.MOE_ERR_ARG
+    assert moe.moe_set_option(12345, 0) == moe.MOE_ERR_ARG
+    assert moe.moe_get_option(12345) == -1
+    moe.moe_set_option(moe.MOE_OPT_GEMV_MAX_ROWS, old)
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert moe.moe_status_string(s)
+    assert moe.moe_status_string(999) == "unknown status"
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(moe, "_lib", None)
+    monkeypatch.setattr(moe, "LIB_PATH", "/nonexistent/libmoe.so")
+    with pytest.raises(RuntimeError):
+        moe.lib()

@@ -1,0 +1,295 @@
+"""CUDA path vs the CPU oracle, through the C ABI, on the five workloads and
+edge cases. Routing tables and logits must be bit-exact; the layer output must
+be within the tolerance of gpu_util.check_output."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import bit_moe_expert_routing_gb300 as moe
+from bit_moe_expert_routing_gb300 import build, synth
+from oracle import oracle as O
+
+from gpu_util import WEIGHT_ATOL, bf16_to_np, check_output, config, rne_bf16, x_to_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    moe.lib()
+    yield
+    moe.moe_set_option(moe.MOE_OPT_FORCE_PATH, moe.PATH_AUTO)
+    moe.moe_set_option(moe.MOE_OPT_GEMM_IMPL, moe.GEMM_TENSOR_CORE)
+
+
+_dev_layers = {}
+
+
+def dev_layer(name, layer):
+    key = (name, id(layer))
+    if key not in _dev_layers:
+        _dev_layers[key] = moe.DeviceLayer(layer)
+    return _dev_layers[key]
+
+
+def run_forward(dl, x_bits, path=moe.PATH_AUTO, impl=moe.GEMM_TENSOR_CORE):
+    assert moe.moe_set_option(moe.MOE_OPT_FORCE_PATH, path) == moe.MOE_OK
+    assert moe.moe_set_option(moe.MOE_OPT_GEMM_IMPL, impl) == moe.MOE_OK
+    x = x_to_device(x_bits)
+    ws = dl.workspace(x.shape[0])
+    y = dl.forward(x, workspace=ws)
+    torch.cuda.synchronize()
+    st = moe.moe_get_device_status(ctypes.c_void_p(ws.data_ptr()), None)
+    assert st == moe.MOE_OK, moe.moe_status_string(st)
+    return bf16_to_np(y), ws
+
+
+# --- dequantisation ------------------------------------------------------------------------
+
+def test_debug_dequant_matches_rounded_oracle():
+    layer, _ = config("tiny")
+    dl = dev_layer("tiny", layer)
+    for m, qm, rows, K in ((layer.gate, dl.w.gate, layer.I, layer.D), (layer.down, dl.w.down, layer.D, layer.I)):
+        for e in (0, 3, layer.E - 1):
+            out = torch.empty(rows * K, dtype=torch.int16, device="cuda")
+            assert moe.moe_debug_dequant(qm, e, rows, K, out.data_ptr(), None) == moe.MOE_OK
+            torch.cuda.synchronize()
+            got = synth.bf16_bits_to_f32(out.cpu().numpy().view(np.uint16)).astype(np.float64)
+            want = rne_bf16(O.dequant(m, e, rows, K)).reshape(-1)
+            assert np.array_equal(got, want)
+
+
+def test_debug_dequant_golden_vectors():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "dequant_vectors.txt")
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        name, word, s, b, exact, rne = [p.strip() for p in line.split("|")]
+        codes = torch.tensor([int(word, 16)] * 8, dtype=torch.int64).to(torch.int32).cuda()
+        sc = torch.tensor([int(s, 16)], dtype=torch.int32).to(torch.int16).cuda()
+        bi = torch.tensor([int(b, 16)], dtype=torch.int32).to(torch.int16).cuda()
+        qm = moe.moe_qmatrix(codes.data_ptr(), sc.data_ptr(), bi.data_ptr())
+        out = torch.empty(64, dtype=torch.int16, device="cuda")
+        assert moe.moe_debug_dequant(qm, 0, 1, 64, out.data_ptr(), None) == moe.MOE_OK
+        torch.cuda.synchronize()
+        got = synth.bf16_bits_to_f32(out.cpu().numpy().view(np.uint16))
+        assert np.array_equal(got, np.tile(np.array([float(v) for v in rne.split()], np.float32), 8)), name
+
+
+# --- routing: bit-exact --------------------------------------------------------------------
+
+def check_routing(layer, x_bits, name):
+    dl = dev_layer(name, layer)
+    x = x_to_device(x_bits)
+    T = x.shape[0]
+    ws = dl.workspace(T)
+    v = dl.route(x, ws)
+    torch.cuda.synchronize()
+    ol = O.OracleLayer(layer)
+    logits, idx, w = O.route(ol, x_bits)
+    tb = O.route_tables(idx, layer.E, v.block_m)
+    g = lambda p, shape, dt: moe.ws_tensor(ws, p, shape, dt).cpu().numpy()
+    A = T * layer.k
+    assert np.array_equal(g(v.logits, (T, layer.E), torch.float32).view(np.uint32), logits.view(np.uint32)), \
+        "router logits differ in bits"
+    assert np.array_equal(g(v.topk_idx, (T, layer.k), torch.int32), idx)
+    assert np.abs(g(v.topk_w, (T, layer.k), torch.float32) - w).max() <= WEIGHT_ATOL
+    assert np.array_equal(g(v.count, (layer.E,), torch.int32), tb["count"])
+    assert np.array_equal(g(v.off, (layer.E + 1,), torch.int32), tb["off"])
+    assert np.array_equal(g(v.perm, (A,), torch.int32), tb["perm"])
+    assert np.array_equal(g(v.inv, (A,), torch.int32), tb["inv"])
+    nb = int(g(v.n_blocks, (1,), torch.int32)[0])
+    assert nb == len(tb["blocks"])
+    assert np.array_equal(g(v.blocks, (v.max_blocks, 3), torch.int32)[:nb], tb["blocks"])
+    assert moe.moe_get_device_status(ctypes.c_void_p(ws.data_ptr()), None) == moe.MOE_OK
+    return tb
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill512", "prefill4096_zipf", "sweep"])
+def test_routing_bit_exact(name):
+    layer, x = config(name)
+    tb = check_routing(layer, x, name)
+    if name == "prefill4096_zipf":
+        assert tb["count"].max() > 1000 and (tb["count"] == 0).any()
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 63, 64, 65, 200])
+def test_routing_ragged_token_counts(T):
+    layer = synth.make_layer(31, 256, 16, 4, 128)
+    check_routing(layer, synth.make_x(31, T, 256), f"ragged{T}")
+
+
+def test_routing_ties_go_to_lower_index():
+    layer = synth.make_layer(32, 256, 16, 4, 128)
+    layer.router_w[9] = layer.router_w[3]
+    layer.router_w[12] = layer.router_w[2]
+    layer.router_w[15] = layer.router_w[2]
+    x = synth.make_x(32, 96, 256)
+    check_routing(layer, x, "ties")
+
+
+def test_routing_all_equal_logits():
+    layer = synth.make_layer(33, 128, 8, 8, 64)
+    layer.router_w[:] = 0
+    check_routing(layer, synth.make_x(33, 5, 128), "equal")
+
+
+# --- the layer -----------------------------------------------------------------------------
+
+PATHS = [("gemm_tc", moe.PATH_GEMM, moe.GEMM_TENSOR_CORE), ("gemm_simt", moe.PATH_GEMM, moe.GEMM_CUDA_CORE),
+         ("gemv", moe.PATH_GEMV, moe.GEMM_TENSOR_CORE)]
+
+
+@pytest.mark.parametrize("path", PATHS, ids=[p[0] for p in PATHS])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 16])
+def test_layer_tiny(path, T):
+    layer, x = config("tiny")
+    x = x[:T]
+    _, p, impl = path
+    if p == moe.PATH_GEMV and T > 8:
+        pytest.skip("the GEMV path takes at most 8 rows")
+    y, _ = run_forward(dev_layer("tiny", layer), x, p, impl)
+    check_output(y, O.forward(O.OracleLayer(layer), x), f"tiny T={T} {path[0]}")
+
+
+@pytest.mark.parametrize("path", PATHS, ids=[p[0] for p in PATHS])
+def test_layer_decode(path):
+    layer, x = config("decode")
+    y, _ = run_forward(dev_layer("decode", layer), x, path[1], path[2])
+    check_output(y, O.forward(O.OracleLayer(layer), x), f"decode {path[0]}")
+
+
+@pytest.mark.parametrize("path", PATHS, ids=[p[0] for p in PATHS])
+@pytest.mark.parametrize("T", synth.SWEEP_T)
+def test_layer_crossover_sweep(path, T):
+    layer, x = config("sweep")
+    x = x[:T]
+    y, _ = run_forward(dev_layer("sweep", layer), x, path[1], path[2])
+    check_output(y, O.forward(O.OracleLayer(layer), x), f"sweep T={T} {path[0]}")
+
+
+@pytest.mark.parametrize("impl", [moe.GEMM_TENSOR_CORE, moe.GEMM_CUDA_CORE], ids=["tc", "simt"])
+def test_layer_prefill512_all_tokens(impl):
+    layer, x = config("prefill512")
+    y, _ = run_forward(dev_layer("prefill512", layer), x, moe.PATH_GEMM, impl)
+    check_output(y, O.forward(O.OracleLayer(layer), x), "prefill512")
+
+
+def _sample_tokens(idx, count, T):
+    heavy = int(np.argmax(count))
+    light = int(np.argmin(np.where(count > 0, count, 1 << 30)))
+    on_heavy = np.where((idx == heavy).any(1))[0]
+    on_light = np.where((idx == light).any(1))[0]
+    pick = list(range(8)) + list(range(T - 8, T)) + list(on_heavy[:8]) + list(on_light[:4]) + \
+        list(np.random.default_rng(0).choice(T, 12, replace=False))
+    return np.array(sorted(set(int(t) for t in pick)), dtype=np.int32)
+
+
+@pytest.mark.parametrize("impl", [moe.GEMM_TENSOR_CORE, moe.GEMM_CUDA_CORE], ids=["tc", "simt"])
+def test_layer_prefill4096_zipf_sampled(impl):
+    layer, x = config("prefill4096_zipf")
+    y, _ = run_forward(dev_layer("prefill4096_zipf", layer), x, moe.PATH_GEMM, impl)
+    ol = O.OracleLayer(layer)
+    _, idx, _ = O.route(ol, x)
+    toks = _sample_tokens(idx, np.bincount(idx.reshape(-1), minlength=layer.E), x.shape[0])
+    check_output(y[toks], O.forward(ol, x, tokens=toks), "prefill4096 sampled")
+    assert np.isfinite(y).all()
+
+
+def test_intermediate_h_matches_oracle():
+    layer, x = config("tiny")
+    dl = dev_layer("tiny", layer)
+    ol = O.OracleLayer(layer)
+    for p, impl in ((moe.PATH_GEMM, moe.GEMM_TENSOR_CORE), (moe.PATH_GEMM, moe.GEMM_CUDA_CORE),
+                    (moe.PATH_GEMV, moe.GEMM_TENSOR_CORE)):
+        xx = x[:8]
+        _, ws = run_forward(dl, xx, p, impl)
+        v = dl.view(xx.shape[0], ws)
+        T, k = xx.shape[0], layer.k
+        h = bf16_to_np(moe.ws_tensor(ws, v.h, (T * k + T, layer.I), torch.bfloat16))
+        perm = moe.ws_tensor(ws, v.perm, (T * k,), torch.int32).cpu().numpy()
+        idx = moe.ws_tensor(ws, v.topk_idx, (T, k), torch.int32).cpu().numpy()
+        ref = np.stack([O.expert_h(ol, int(idx[a // k, a % k]), xx[a // k]) for a in perm] +
+                       [O.expert_h(ol, -1, xx[t]) for t in range(T)])
+        check_output(h, ref, f"h path={p} impl={impl}")
+
+
+@pytest.mark.parametrize("shape", [dict(D=128, E=1, k=1, I=64), dict(D=192, E=8, k=8, I=128),
+                                   dict(D=320, E=40, k=3, I=192), dict(D=1024, E=64, k=6, I=256)],
+                         ids=["E1k1", "kE", "odd", "mid"])
+@pytest.mark.parametrize("T", [1, 7, 130])
+def test_layer_shapes(shape, T):
+    layer = synth.make_layer(40, **shape)
+    x = synth.make_x(40, T, shape["D"])
+    dl = moe.DeviceLayer(layer)
+    ref = O.forward(O.OracleLayer(layer), x)
+    for p, impl in ((moe.PATH_GEMM, moe.GEMM_TENSOR_CORE), (moe.PATH_GEMM, moe.GEMM_CUDA_CORE),
+                    (moe.PATH_GEMV, moe.GEMM_TENSOR_CORE)):
+        if p == moe.PATH_GEMV and T > 8:
+            continue
+        y, _ = run_forward(dl, x, p, impl)
+        check_output(y, ref, f"{shape} T={T} path={p} impl={impl}")
+
+
+def test_zero_tokens_is_noop():
+    layer, _ = config("tiny")
+    dl = dev_layer("tiny", layer)
+    ws = dl.workspace(0)
+    r = moe.moe_layer_forward(dl.w, 0, 0, 0, ws.data_ptr(), ws.numel(), None)
+    assert r == moe.MOE_OK and moe.moe_last_launch_count() == 0
+
+
+def test_workspace_too_small_rejected():
+    layer, x = config("tiny")
+    dl = dev_layer("tiny", layer)
+    xd = x_to_device(x)
+    y = torch.empty_like(xd)
+    ws = dl.workspace(x.shape[0])
+    r = moe.moe_layer_forward(dl.w, xd.data_ptr(), x.shape[0], y.data_ptr(), ws.data_ptr(), ws.numel() - 256,
+                              None)
+    assert r == moe.MOE_ERR_WORKSPACE
+
+
+def test_host_buffers_entry_point_matches_device_entry_point():
+    layer, x = config("sweep")
+    x = x[:5]
+    dl = dev_layer("sweep", layer)
+    y_dev, _ = run_forward(dl, x, moe.PATH_AUTO)
+    ws = dl.workspace(5, host_staging=True)
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    r = moe.moe_layer_forward_host(dl.w, xh.data_ptr(), 5, yh.data_ptr(), ws.data_ptr(), ws.numel(), None)
+    assert r == moe.MOE_OK
+    y_host = synth.bf16_bits_to_f32(yh.numpy().view(np.uint16)).astype(np.float64)
+    assert np.array_equal(y_host, y_dev)
+
+
+def test_gemv_path_is_deterministic():
+    layer, x = config("sweep")
+    dl = dev_layer("sweep", layer)
+    a, _ = run_forward(dl, x[:3], moe.PATH_GEMV)
+    b, _ = run_forward(dl, x[:3], moe.PATH_GEMV)
+    assert np.array_equal(a, b)
+
+
+def test_kernel_timing_and_launch_count():
+    layer, x = config("tiny")
+    dl = dev_layer("tiny", layer)
+    moe.moe_kernel_times()
+    assert moe.moe_set_option(moe.MOE_OPT_KERNEL_TIMING, 1) == moe.MOE_OK
+    try:
+        run_forward(dl, x, moe.PATH_GEMM, moe.GEMM_CUDA_CORE)
+        n = moe.moe_last_launch_count()
+        times = moe.moe_kernel_times()
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_KERNEL_TIMING, 0)
+    assert n >= 6
+    assert sum(c for _, c in times.values()) == n
+    assert all(ms >= 0 for ms, _ in times.values())
+    assert "router_logits" in times and "gateup_simt" in times
