@@ -29,6 +29,7 @@ MOE_OPT_GEMV_MAX_ROWS = 1
 MOE_OPT_FORCE_PATH = 2
 MOE_OPT_KERNEL_TIMING = 3
 MOE_OPT_GEMM_IMPL = 4
+MOE_OPT_TEST_WAIT_CYCLES = 5
 
 PATH_AUTO, PATH_GEMV, PATH_GEMM = 0, 1, 2
 GEMM_TENSOR_CORE, GEMM_CUDA_CORE = 0, 1

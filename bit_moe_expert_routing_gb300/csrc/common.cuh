@@ -41,6 +41,9 @@ __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v &
 
 namespace moe {
 
+// Raises a kernel's dynamic shared-memory limit once per device (host side).
+bool ensure_smem_limit(const void* func, int bytes);
+
 // Eight 4-bit codes of one word -> eight bf16 weights s*q + b, each rounded
 // once to nearest even (the tensor-core operand format). out[i] holds
 // elements 2i (low half) and 2i+1 (high half).

@@ -208,14 +208,9 @@ constexpr size_t simt_smem_bytes(int nb) { return sizeof(float) * SBK * (SBM + n
 
 cudaError_t gemm_simt(const Ctx& c) {
   const moe_weights* w = c.w;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(gemm_simt_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         int(simt_smem_bytes(2)));
-    cudaFuncSetAttribute(gemm_simt_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         int(simt_smem_bytes(1)));
-    attr_set = true;
-  }
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(gemm_simt_kernel<true>), int(simt_smem_bytes(2))) ||
+      !ensure_smem_limit(reinterpret_cast<const void*>(gemm_simt_kernel<false>), int(simt_smem_bytes(1))))
+    return cudaErrorInvalidValue;
   SimtArgs a{c.x, c.h, w->gate, w->up, w->s_gate, w->s_up, c.blocks, c.n_blocks, c.perm, c.topk_w,
              c.h, c.y_acc, c.hdr, c.T, c.D, c.E, c.k, c.I};
   cudaError_t err = zero_yacc(c);

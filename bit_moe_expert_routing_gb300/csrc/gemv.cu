@@ -254,10 +254,9 @@ cudaError_t gemv(const Ctx& c) {
   cudaError_t err;
   const int cpl = (c.D / 32 + 31) / 32;
   void (*gk)(GemvArgs) = cpl <= 1 ? gemv_gateup_kernel<1> : cpl <= 2 ? gemv_gateup_kernel<2> : gemv_gateup_kernel<4>;
-  if ((err = cudaFuncSetAttribute(gk, cudaFuncAttributeMaxDynamicSharedMemorySize, int(s1))) != cudaSuccess)
-    return err;
-  if ((err = cudaFuncSetAttribute(gemv_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(s2))) != cudaSuccess)
-    return err;
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(gk), int(s1)) ||
+      !ensure_smem_limit(reinterpret_cast<const void*>(gemv_down_kernel), int(s2)))
+    return cudaErrorInvalidValue;
   const int rows_per_cta = kGemvWarps;
   gk<<<dim3(c.max_blocks, (c.I + rows_per_cta - 1) / rows_per_cta), kGemvWarps * 32, s1,
                        c.stream>>>(a);

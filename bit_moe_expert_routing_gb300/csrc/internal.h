@@ -56,6 +56,7 @@ cudaError_t cast_y(const Ctx& c);
 cudaError_t gemm_simt(const Ctx& c);
 cudaError_t gemm_tc(const Ctx& c);
 bool gemm_tc_supported(const Ctx& c);
+void set_tc_epilogue_wait_limit(long long cycles);  // <= 0: the normal limit
 
 // Decode GEMV path (a few rows).
 cudaError_t gemv(const Ctx& c);

@@ -21,6 +21,7 @@ struct Options {
   int force_path = 0;
   int kernel_timing = 0;
   int gemm_impl = 0;
+  int test_wait_cycles = 0;
 };
 Options g_opt;
 std::mutex g_mu;
@@ -168,6 +169,24 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 
 }  // namespace
 
+bool ensure_smem_limit(const void* func, int bytes) {
+  struct Entry {
+    const void* f;
+    int dev;
+    int bytes;
+  };
+  static std::vector<Entry> done;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  for (const Entry& e : done)
+    if (e.f == func && e.dev == dev && e.bytes >= bytes) return true;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  done.push_back({func, dev, bytes});
+  return true;
+}
+
 void launch_done(const char* name, cudaStream_t s) {
   ++t_launches;
   if (g_opt.kernel_timing) mark(name, s);
@@ -283,6 +302,11 @@ moe_status moe_set_option(int option, int value) {
       if (value < 0 || value > 1) return MOE_ERR_ARG;
       g_opt.gemm_impl = value;
       return MOE_OK;
+    case MOE_OPT_TEST_WAIT_CYCLES:
+      if (value < 0) return MOE_ERR_ARG;
+      g_opt.test_wait_cycles = value;
+      set_tc_epilogue_wait_limit(value);
+      return MOE_OK;
     default:
       return MOE_ERR_ARG;
   }
@@ -294,6 +318,7 @@ int moe_get_option(int option) {
     case MOE_OPT_FORCE_PATH: return g_opt.force_path;
     case MOE_OPT_KERNEL_TIMING: return g_opt.kernel_timing;
     case MOE_OPT_GEMM_IMPL: return g_opt.gemm_impl;
+    case MOE_OPT_TEST_WAIT_CYCLES: return g_opt.test_wait_cycles;
     default: return -1;
   }
 }

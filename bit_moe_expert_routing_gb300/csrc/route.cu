@@ -28,8 +28,14 @@ template <int TT, int EPW>
 __global__ void __launch_bounds__(kRouterWarps * 32)
     router_logits_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
                          const float* __restrict__ bias, int T, int D, int E,
-                         float* __restrict__ logits) {
+                         float* __restrict__ logits, WsHeader* hdr) {
   static_assert(TT % 2 == 0, "tokens go in pairs");
+  // First kernel of every call: start the call's device status afresh. No
+  // other CTA of this kernel reports, so nothing races with the clear.
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    hdr->status = 0;
+    hdr->detail = 0;
+  }
   __shared__ __align__(16) uint16_t xs[TT * kRouterDChunk];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t0 = blockIdx.x * TT;
@@ -300,15 +306,15 @@ cudaError_t route(const Ctx& c) {
   if (c.T <= 2) {
     dim3 grid(c.T > 0 ? (c.T + 1) / 2 : 1, (c.E + kRouterWarps - 1) / kRouterWarps);
     router_logits_kernel<2, 1><<<grid, kRouterWarps * 32, 0, c.stream>>>(c.x, w->router_w, w->router_bias,
-                                                                          c.T, c.D, c.E, c.logits);
+                                                                          c.T, c.D, c.E, c.logits, c.hdr);
   } else if (c.T <= 8) {
     dim3 grid(1, (c.E + kRouterWarps - 1) / kRouterWarps);
     router_logits_kernel<8, 1><<<grid, kRouterWarps * 32, 0, c.stream>>>(c.x, w->router_w, w->router_bias,
-                                                                          c.T, c.D, c.E, c.logits);
+                                                                          c.T, c.D, c.E, c.logits, c.hdr);
   } else {
     dim3 grid((c.T + 15) / 16, (c.E + 8 * kRouterWarps - 1) / (8 * kRouterWarps));
     router_logits_kernel<16, 8><<<grid, kRouterWarps * 32, 0, c.stream>>>(c.x, w->router_w, w->router_bias,
-                                                                           c.T, c.D, c.E, c.logits);
+                                                                           c.T, c.D, c.E, c.logits, c.hdr);
   }
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done("router_logits", c.stream);

@@ -119,8 +119,14 @@ typedef enum {
   MOE_OPT_FORCE_PATH = 2,    /* 0 auto by row count, 1 GEMV, 2 grouped GEMM */
   MOE_OPT_KERNEL_TIMING = 3, /* 1: record CUDA events around each kernel of
                                 the next forwards (read with moe_kernel_times) */
-  MOE_OPT_GEMM_IMPL = 4      /* 0 tensor-core (tcgen05) grouped GEMM, 1 CUDA-core
+  MOE_OPT_GEMM_IMPL = 4,     /* 0 tensor-core (tcgen05) grouped GEMM, 1 CUDA-core
                                 grouped GEMM (the comparison baseline) */
+  MOE_OPT_TEST_WAIT_CYCLES = 5 /* test hook: > 0 makes the tensor-core epilogue
+                                first wait, for at most this many cycles, on a
+                                barrier that nothing arrives on, so the
+                                bounded-wait failure path (status
+                                MOE_ERR_DEVICE_TIMEOUT, drain, clean exit) runs;
+                                0 (the default) turns the hook off */
 } moe_option;
 
 /* Bytes of workspace one call with T tokens needs (pure host; 0 on bad
