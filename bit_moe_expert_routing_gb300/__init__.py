@@ -60,6 +60,7 @@ _W = ctypes.POINTER(moe_weights)
 SIGNATURES = {
     "moe_workspace_size": (_SZ, [_W, _CI]),
     "moe_layer_forward": (_CI, [_W, _VP, _CI, _VP, _VP, _SZ, _VP]),
+    "moe_layer_forward_static": (_CI, [_W, _VP, _CI, _VP, _VP]),
     "moe_host_staging_size": (_SZ, [_W, _CI]),
     "moe_layer_forward_host": (_CI, [_W, _VP, _CI, _VP, _VP, _SZ, _VP]),
     "moe_route": (_CI, [_W, _VP, _CI, _VP, _SZ, _VP, ctypes.POINTER(moe_route_view)]),
@@ -114,6 +115,12 @@ def moe_host_staging_size(w: moe_weights, T: int) -> int:
 
 def moe_layer_forward(w, x_ptr, T, y_ptr, ws_ptr, ws_bytes, stream) -> int:
     return lib().moe_layer_forward(ctypes.byref(w), x_ptr, T, y_ptr, ws_ptr, ws_bytes, stream)
+
+
+def moe_layer_forward_static(w, x_ptr, T, y_ptr, stream) -> int:
+    """The layer with the library's fixed device scratch array as its
+    workspace, for callers that cannot allocate device memory (see include/moe.h)."""
+    return lib().moe_layer_forward_static(ctypes.byref(w), x_ptr, T, y_ptr, stream)
 
 
 def moe_layer_forward_host(w, x_host_ptr, T, y_host_ptr, ws_ptr, ws_bytes, stream) -> int:

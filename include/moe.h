@@ -183,6 +183,31 @@ moe_status moe_kernel_times(const char** names, float* total_ms, int* launches, 
 moe_status moe_debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, uint16_t* out,
                              void* stream);
 
+/* Bytes of the library's fixed device scratch array used by
+ * moe_layer_forward_static(). */
+#define MOE_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* The whole layer, like moe_layer_forward(), but with no workspace argument:
+ * its scratch memory is a fixed 8 MiB device array inside this library, so
+ * the call allocates no device memory at all. (The source pages have no
+ * counterpart; this serves callers that cannot allocate: code running while a
+ * CUDA graph is captured, loops that forbid cudaMalloc after start-up because
+ * it can synchronise the device or fail on fragmentation, and hosts that hand
+ * their plug-ins only input and output buffers.)
+ *   x, y, stream: as for moe_layer_forward(); the caller still owns them.
+ *   Limit: T is accepted only while moe_workspace_size(w, T) <=
+ *   MOE_STATIC_SCRATCH_BYTES (for the D=2048, E=256, k=8, I=512 layer that is
+ *   T <= 451); larger T returns MOE_ERR_WORKSPACE and enqueues nothing.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current), so make that first call before any stream capture.
+ *   Every call on a device shares the one array and leaves its contents
+ *   behind; each call clears what must start at zero itself. Calls whose
+ *   work overlaps on the GPU (unordered streams or host threads) race on the
+ *   array: order them on one stream. The array occupies device memory on
+ *   every GPU that loads the library, until the process exits. */
+moe_status moe_layer_forward_static(const moe_weights* w, const uint16_t* x, int T, uint16_t* y,
+                                    void* stream);
+
 /* Number of this library's kernels the last forward on this thread launched. */
 int moe_last_launch_count(void);
 
