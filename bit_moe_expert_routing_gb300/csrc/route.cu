@@ -95,11 +95,61 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     }
 }
 
-// Top-k of each token (larger logit first, lower expert index on ties),
-// weights softmax-renormalised over the k kept, and this chunk's per-expert
-// assignment counts. One warp per token; lane l holds logits l, l+32, ...
+// Top-k of one token's logits (larger logit first, lower expert index on
+// ties) by one warp; lane l holds logits l, l+32, ... On return lane j < k
+// holds slot j: its expert and its weight, the softmax renormalised over the
+// k kept, exp(l_j - l_max) / sum.
 constexpr int kMaxPerLane = 32;  // E <= 1024
 
+__device__ __forceinline__ void select_topk(const float* __restrict__ lg, int E, int k, int& myi, float& myw) {
+  const int lane = threadIdx.x & 31;
+  const int M = (E + 31) / 32;
+  float v[kMaxPerLane];
+  unsigned taken = 0;
+#pragma unroll
+  for (int m = 0; m < kMaxPerLane; ++m) {
+    const int e = lane + 32 * m;
+    v[m] = (m < M && e < E) ? lg[e] : 0.f;
+    if (!(m < M && e < E)) taken |= 1u << m;
+  }
+  float first = 0.f, myv = 0.f;
+  myi = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int m = 0; m < kMaxPerLane; ++m) {
+      const int e = lane + 32 * m;
+      if (!((taken >> m) & 1u) && (v[m] > bv || (v[m] == bv && e < bi))) {
+        bv = v[m];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (j == 0) first = bv;
+    if (lane == j) {
+      myv = bv;
+      myi = bi;
+    }
+  }
+  const float ex = lane < k ? expf(myv - first) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  myw = ex / sum;
+}
+
+// Top-k and weights of each token of a chunk, and the chunk's per-expert
+// assignment counts. One warp per token.
 __global__ void __launch_bounds__(256)
     topk_hist_kernel(const float* __restrict__ logits, int T, int E, int k,
                      int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
@@ -108,55 +158,15 @@ __global__ void __launch_bounds__(256)
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int M = (E + 31) / 32;
   for (int tt = warp; tt < kChunkTokens; tt += blockDim.x / 32) {
     const int t = blockIdx.x * kChunkTokens + tt;
     if (t >= T) break;
-    const float* lg = logits + size_t(t) * E;
-    float v[kMaxPerLane];
-    unsigned taken = 0;
-#pragma unroll
-    for (int m = 0; m < kMaxPerLane; ++m) {
-      const int e = lane + 32 * m;
-      v[m] = (m < M && e < E) ? lg[e] : 0.f;
-      if (!(m < M && e < E)) taken |= 1u << m;
-    }
-    float first = 0.f, myv = 0.f;
-    int myi = 0;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
-#pragma unroll
-      for (int m = 0; m < kMaxPerLane; ++m) {
-        const int e = lane + 32 * m;
-        if (!((taken >> m) & 1u) && (v[m] > bv || (v[m] == bv && e < bi))) {
-          bv = v[m];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (j == 0) first = bv;
-      if (lane == j) {
-        myv = bv;
-        myi = bi;
-      }
-    }
-    const float ex = lane < k ? expf(myv - first) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    int myi;
+    float myw;
+    select_topk(logits + size_t(t) * E, E, k, myi, myw);
     if (lane < k) {
       topk_idx[size_t(t) * k + lane] = myi;
-      topk_w[size_t(t) * k + lane] = ex / sum;
+      topk_w[size_t(t) * k + lane] = myw;
       atomicAdd(&hist[myi], 1);
     }
   }
@@ -298,16 +308,160 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ---- small token counts (decode): two kernels for the whole routing ----------------------
+
+// Router logits for T <= TT tokens: one warp per expert, every token of the
+// call in the same warp. Each lane first loads kSmallBatch of its W_r values
+// (one DRAM round trip for them all), then runs its fixed-order FMA chain.
+constexpr int kSmallBatch = 32;
+
+template <int TT>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+    router_small_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
+                        const float* __restrict__ bias, int T, int D, int E, float* __restrict__ logits,
+                        WsHeader* hdr) {
+  extern __shared__ uint4 xsm4[];  // x rows [TT][D] bf16, rows >= T zero
+  const uint16_t* xsm = reinterpret_cast<const uint16_t*>(xsm4);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {  // first kernel of the call
+    hdr->status = 0;
+    hdr->detail = 0;
+  }
+  for (int i = threadIdx.x; i < TT * (D / 8); i += blockDim.x) {
+    const int t = i / (D / 8), c8 = i % (D / 8);
+    xsm4[i] = t < T ? *reinterpret_cast<const uint4*>(x + size_t(t) * D + c8 * 8) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = blockIdx.x * kRouterWarps + warp;
+  if (e >= E) return;
+  const float* w = wr + size_t(e) * D;
+  const int nch = D / 32;
+  float acc[TT];
+#pragma unroll
+  for (int t = 0; t < TT; ++t) acc[t] = 0.f;
+  for (int c0 = 0; c0 < nch; c0 += kSmallBatch) {
+    float wv[kSmallBatch];
+#pragma unroll
+    for (int u = 0; u < kSmallBatch; ++u) wv[u] = (c0 + u < nch) ? __ldg(w + (c0 + u) * 32 + lane) : 0.f;
+#pragma unroll
+    for (int u = 0; u < kSmallBatch; ++u) {
+      if (c0 + u < nch) {
+#pragma unroll
+        for (int t = 0; t < TT; ++t) acc[t] = fmaf(bf16_to_f32(xsm[t * D + (c0 + u) * 32 + lane]), wv[u], acc[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TT; ++t) {
+    float a = acc[t];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) a = __fadd_rn(a, __shfl_down_sync(0xffffffffu, a, off));
+    if (lane == 0 && t < T) logits[size_t(t) * E + e] = bias ? __fadd_rn(a, bias[e]) : a;
+  }
+}
+
+// Top-k, weights, histogram, scan, scatter and block map of up to
+// kSmallRouteTokens tokens in one CTA of 1024 threads (thread e owns expert e
+// for the scan; warp t selects token t's experts).
+constexpr int kSmallRouteTokens = 16;
+
+__global__ void __launch_bounds__(1024)
+    route_small_kernel(const float* __restrict__ logits, int T, int E, int k, int BM, int max_blocks,
+                       int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ count,
+                       int32_t* __restrict__ off, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                       int32_t* __restrict__ blocks, int32_t* __restrict__ n_blocks, WsHeader* hdr) {
+  __shared__ int s_idx[kSmallRouteTokens * 32];
+  __shared__ int s_cnt[1024];
+  __shared__ int s_warp[32];
+  __shared__ int s_tot_rows, s_tot_blocks;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int A = T * k;
+  s_cnt[threadIdx.x] = 0;
+  __syncthreads();
+  if (warp < T) {
+    int myi;
+    float myw;
+    select_topk(logits + size_t(warp) * E, E, k, myi, myw);
+    if (lane < k) {
+      topk_idx[warp * k + lane] = myi;
+      topk_w[warp * k + lane] = myw;
+      s_idx[warp * k + lane] = myi;
+      atomicAdd(&s_cnt[myi], 1);
+    }
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int total = e < E ? s_cnt[e] : 0;
+  const int nb = (total + BM - 1) / BM;
+  const int ex_off = block_exclusive_scan(total, s_warp, &s_tot_rows);
+  const int ex_nb = block_exclusive_scan(nb, s_warp, &s_tot_blocks);
+  if (e < E) {
+    count[e] = total;
+    off[e] = ex_off;
+    for (int b = 0; b < nb; ++b) {
+      const int idx = ex_nb + b;
+      if (idx < max_blocks) {
+        blocks[3 * idx + 0] = e;
+        blocks[3 * idx + 1] = ex_off + b * BM;
+        blocks[3 * idx + 2] = min(BM, total - b * BM);
+      }
+    }
+    s_cnt[e] = ex_off;  // now the segment start of expert e
+  }
+  if (e == 0) off[E] = s_tot_rows;
+  const int shared_blocks = (T + BM - 1) / BM;
+  for (int sb = threadIdx.x; sb < shared_blocks; sb += blockDim.x) {
+    const int idx = s_tot_blocks + sb;
+    if (idx < max_blocks) {
+      blocks[3 * idx + 0] = E;
+      blocks[3 * idx + 1] = A + sb * BM;
+      blocks[3 * idx + 2] = min(BM, T - sb * BM);
+    }
+  }
+  if (threadIdx.x == 0) {
+    const int total_blocks = s_tot_blocks + shared_blocks;
+    *n_blocks = min(total_blocks, max_blocks);
+    if (total_blocks > max_blocks || s_tot_rows != A) report(hdr, MOE_ERR_DEVICE_CHECK, 6);
+  }
+  __syncthreads();
+  // scatter: rank of assignment a among earlier assignments to the same expert
+  const int a = threadIdx.x;
+  if (a < A) {
+    const int ea = s_idx[a];
+    int pos = s_cnt[ea];
+    for (int b = 0; b < a; ++b) pos += (s_idx[b] == ea);
+    if (pos >= 0 && pos < A) {
+      perm[pos] = a;
+      inv[a] = pos;
+    } else {
+      report(hdr, MOE_ERR_DEVICE_CHECK, 7);
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t route(const Ctx& c) {
   const moe_weights* w = c.w;
   cudaError_t err;
-  if (c.T <= 2) {
-    dim3 grid(c.T > 0 ? (c.T + 1) / 2 : 1, (c.E + kRouterWarps - 1) / kRouterWarps);
-    router_logits_kernel<2, 1><<<grid, kRouterWarps * 32, 0, c.stream>>>(c.x, w->router_w, w->router_bias,
-                                                                          c.T, c.D, c.E, c.logits, c.hdr);
-  } else if (c.T <= 8) {
+  if (c.T <= kSmallRouteTokens && c.D <= 4096) {
+    const int tt = c.T <= 2 ? 2 : c.T <= 8 ? 8 : 16;
+    void (*rk)(const uint16_t*, const float*, const float*, int, int, int, float*, WsHeader*) =
+        tt == 2 ? router_small_kernel<2> : tt == 8 ? router_small_kernel<8> : router_small_kernel<16>;
+    const size_t smem = size_t(tt) * c.D * 2;
+    if (!ensure_smem_limit(reinterpret_cast<const void*>(rk), int(smem))) return cudaErrorInvalidValue;
+    rk<<<(c.E + kRouterWarps - 1) / kRouterWarps, kRouterWarps * 32, smem, c.stream>>>(
+        c.x, w->router_w, w->router_bias, c.T, c.D, c.E, c.logits, c.hdr);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    launch_done("router_small", c.stream);
+    route_small_kernel<<<1, 1024, 0, c.stream>>>(c.logits, c.T, c.E, c.k, c.BM, c.max_blocks, c.topk_idx,
+                                                 c.topk_w, c.count, c.off, c.perm, c.inv, c.blocks, c.n_blocks,
+                                                 c.hdr);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    launch_done("route_small", c.stream);
+    return cudaSuccess;
+  }
+  if (c.T <= 8) {
     dim3 grid(1, (c.E + kRouterWarps - 1) / kRouterWarps);
     router_logits_kernel<8, 1><<<grid, kRouterWarps * 32, 0, c.stream>>>(c.x, w->router_w, w->router_bias,
                                                                           c.T, c.D, c.E, c.logits, c.hdr);
