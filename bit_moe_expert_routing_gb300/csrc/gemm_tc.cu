@@ -35,19 +35,23 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kStages = 4;
-constexpr int BM = 128;  // token rows per tile
-constexpr int BN = 256;  // weight rows per tile
-constexpr int BK = 64;   // one quantisation group per k-step
-constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
-constexpr uint32_t kBBytes = BN * BK * 2;  // 32 KB
-constexpr uint32_t kCBytes = BN * BK / 2;  // 8 KB of codes
-constexpr uint32_t kTmemCols = 2 * BN;     // two accumulators
-constexpr int kAPipeLag = 2;               // cp.async groups kept in flight
+constexpr int kStages = 4;   // A/B operand ring (MMA side)
+constexpr int kCStages = 4;  // packed-code ring (TMA side)
+constexpr int BM = 128;      // token rows per tile (MMA M)
+constexpr int kTileRows = BM;
+constexpr int BN = 256;      // weight rows per tile (MMA N)
+constexpr int BK = 64;       // one quantisation group per k-step
+constexpr uint32_t kABytes = BM * BK * 2;        // 16 KB
+constexpr uint32_t kBBytes = BN * BK * 2;        // 32 KB
+constexpr uint32_t kCBytes = BN * BK / 2;        // 8 KB of codes
+constexpr uint32_t kTmemCols = 2 * BN;           // two accumulators: tile i+1 runs while tile i drains
+constexpr int kAPipeLag = 3;                     // cp.async groups kept in flight (< kStages)
+static_assert(kAPipeLag < kStages, "the gather may not wait on a stage it has not released");
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpA0 = 2, kNumAWarps = 4, kWarpDq0 = 6, kNumDqWarps = 8,
               kWarpEpi0 = 14, kNumEpiWarps = 4;
@@ -57,61 +61,15 @@ constexpr int kNumThreads = kNumWarps * 32;
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffC = kOffB + kStages * kBBytes;
-constexpr uint32_t kOffBar = kOffC + kStages * kCBytes;
-constexpr uint32_t kNumBars = 5 * kStages + 6;  // full, empty, cfull, cempty, afull [S]; accf, acce [2]; drain; never
+constexpr uint32_t kOffBar = kOffC + kCStages * kCBytes;
+// full, empty, afull [kStages]; cfull, cempty [kCStages]; accf, acce [2]; drain; never
+constexpr uint32_t kNumBars = 3 * kStages + 2 * kCStages + 6;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr size_t kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024
 
-constexpr long long kWaitLimit = 4000000000LL;  // cycles (about 2 s): far beyond any legal wait
 
-// ---- PTX wrappers -------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase of `parity` to complete. Gives up when the CTA's
-// abort flag is set (unless draining) or after `limit` cycles (then sets the
-// flag and reports).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr,
-                                          long long limit = kWaitLimit, bool draining = false) {
-  if (mbar_try(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_try(bar, parity)) return true;
-    if (!draining && *abort_flag) return false;
-    if (clock64() - t0 > limit) {
-      *abort_flag = 1;
-      report(hdr, MOE_ERR_DEVICE_TIMEOUT, 100);
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// ---- PTX wrappers (beyond the shared ones) ---------------------------------------------
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
   asm volatile(
@@ -168,6 +126,12 @@ __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c
                : "memory");
 }
 
+// bf16 number gi (0..7) of a 16-byte vector, without indexing registers.
+__device__ __forceinline__ uint16_t pick_bf16(uint4 v, int gi) {
+  const uint32_t w = (gi & 4) ? ((gi & 2) ? v.w : v.z) : ((gi & 2) ? v.y : v.x);
+  return uint16_t((gi & 1) ? (w >> 16) : (w & 0xFFFFu));
+}
+
 // Byte offset of 16-byte chunk c of row r inside a 1024-aligned SW128 K-major tile.
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return uint32_t((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
@@ -204,13 +168,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
   const uint32_t bar0 = base + kOffBar;
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto cfull = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
-  auto cempty = [&](int s) { return bar0 + 8u * (3 * kStages + s); };
-  auto afull = [&](int s) { return bar0 + 8u * (4 * kStages + s); };  // down: h rows landed
-  auto accf = [&](int b) { return bar0 + 8u * (5 * kStages + b); };
-  auto acce = [&](int b) { return bar0 + 8u * (5 * kStages + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (5 * kStages + 4);
-  const uint32_t never_bar = bar0 + 8u * (5 * kStages + 5);  // test hook: nothing arrives here
+  auto afull = [&](int s) { return bar0 + 8u * (2 * kStages + s); };  // down: h rows landed
+  auto cfull = [&](int s) { return bar0 + 8u * (3 * kStages + s); };
+  auto cempty = [&](int s) { return bar0 + 8u * (3 * kStages + kCStages + s); };
+  constexpr uint32_t kBarAcc = 3 * kStages + 2 * kCStages;
+  auto accf = [&](int b) { return bar0 + 8u * (kBarAcc + b); };
+  auto acce = [&](int b) { return bar0 + 8u * (kBarAcc + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (kBarAcc + 4);
+  const uint32_t never_bar = bar0 + 8u * (kBarAcc + 5);  // test hook: nothing arrives here
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kOffMisc + 4);
 
@@ -225,9 +190,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full(s), GATEUP ? (kNumDqWarps + kNumAWarps) : kNumDqWarps);
       mbar_init(empty(s), 1);
+      mbar_init(afull(s), 1);
+    }
+    for (int s = 0; s < kCStages; ++s) {
       mbar_init(cfull(s), 1);
       mbar_init(cempty(s), kNumDqWarps);
-      mbar_init(afull(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf(b), 1);
@@ -236,7 +203,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
     mbar_init(drain_bar, 1);
     mbar_init(never_bar, 1);
     *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
   }
   if (warp == kWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -263,7 +230,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
     g = a.blocks[3 * b];
     p0 = a.blocks[3 * b + 1];
     R = a.blocks[3 * b + 2];
-    if (g < 0 || g > a.E || R < 1 || R > BM || p0 < 0 || p0 + R > A_rows + a.T) {
+    if (g < 0 || g > a.E || R < 1 || R > kTileRows || p0 < 0 || p0 + R > A_rows + a.T) {
       report(a.hdr, MOE_ERR_DEVICE_CHECK, 11);
       return false;
     }
@@ -284,17 +251,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
         const bool sh = (g == a.E);
         const int ex = sh ? 0 : g;
         for (int ks = 0; ks < KS; ++ks, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1u;
-          if (!(ok = mbar_wait(cempty(s), ph ^ 1u, abort_flag, a.hdr))) break;
-          const uint32_t cdst = base + kOffC + s * kCBytes;
-          mbar_arrive_tx(cfull(s), kCBytes);
+          const int s = it % kStages, cs = it % kCStages;
+          const uint32_t ph = (it / kStages) & 1u, cph = (it / kCStages) & 1u;
+          if (!(ok = mbar_wait(cempty(cs), cph ^ 1u, abort_flag, a.hdr))) break;
+          const uint32_t cdst = base + kOffC + cs * kCBytes;
+          mbar_arrive_tx(cfull(cs), kCBytes);
           if (GATEUP) {
             const int row = ex * a.I + j * 128;
-            tma_load_2d(cdst, sh ? &maps.cs0 : &maps.c0, ks * 8, row, cfull(s));
-            tma_load_2d(cdst + kCBytes / 2, sh ? &maps.cs1 : &maps.c1, ks * 8, row, cfull(s));
+            tma_load_2d(cdst, sh ? &maps.cs0 : &maps.c0, ks * 8, row, cfull(cs));
+            tma_load_2d(cdst + kCBytes / 2, sh ? &maps.cs1 : &maps.c1, ks * 8, row, cfull(cs));
           } else {
-            tma_load_2d(cdst, sh ? &maps.cs0 : &maps.c0, ks * 8, ex * a.D + j * BN, cfull(s));
+            tma_load_2d(cdst, sh ? &maps.cs0 : &maps.c0, ks * 8, ex * a.D + j * BN, cfull(cs));
           }
           c_issued = it + 1;
           if (!GATEUP) {
@@ -306,11 +273,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
         }
       }
       // drain: every load this thread issued lands before the CTA exits
-      for (uint32_t s = 0; s < uint32_t(kStages); ++s) {
+      for (uint32_t s = 0; s < uint32_t(kCStages); ++s) {
         if (s < c_issued) {
-          const uint32_t last = c_issued - 1 - ((c_issued - 1 - s) % kStages);  // last issue to stage s
-          mbar_wait(cfull(s), (last / kStages) & 1u, abort_flag, a.hdr, kWaitLimit, true);
+          const uint32_t last = c_issued - 1 - ((c_issued - 1 - s) % kCStages);  // last issue to stage s
+          mbar_wait(cfull(s), (last / kCStages) & 1u, abort_flag, a.hdr, kWaitLimit, true);
         }
+      }
+      for (uint32_t s = 0; s < uint32_t(kStages); ++s) {
         if (s < a_issued) {
           const uint32_t last = a_issued - 1 - ((a_issued - 1 - s) % kStages);
           mbar_wait(afull(s), (last / kStages) & 1u, abort_flag, a.hdr, kWaitLimit, true);
@@ -324,8 +293,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
       bool ok = true;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
         const int buf = tc & 1;
-        const uint32_t aph = (tc >> 1) & 1u;
-        if (!(ok = mbar_wait(acce(buf), aph ^ 1u, abort_flag, a.hdr))) break;
+        if (!(ok = mbar_wait(acce(buf), ((tc >> 1) & 1u) ^ 1u, abort_flag, a.hdr))) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * BN;
         for (int ks = 0; ks < KS; ++ks, ++it) {
@@ -358,17 +326,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
         *abort_flag = 1;
         break;
       }
-      int t = -1;
-      if (r < R) t = (g == a.E) ? (p0 + r - A_rows) : (a.perm[p0 + r] / a.k);
-      const bool valid = (t >= 0 && t < a.T);
-      const char* src = reinterpret_cast<const char*>(a.x + size_t(valid ? t : 0) * a.D);
+      int t0 = -1;
+      if (r < R) t0 = (g == a.E) ? (p0 + r - A_rows) : (a.perm[p0 + r] / a.k);
+      const bool v0 = (t0 >= 0 && t0 < a.T);
+      const char* src0 = reinterpret_cast<const char*>(a.x + size_t(v0 ? t0 : 0) * a.D);
       for (int ks = 0; ks < KS; ++ks, ++it) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
         if (!(ok = mbar_wait(empty(s), ph ^ 1u, abort_flag, a.hdr))) break;
         const uint32_t dst = base + kOffA + s * kABytes;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) cp_async16(dst + sw128(r, c), src + ks * 128 + c * 16, valid ? 16u : 0u);
+        for (int c = 0; c < 8; ++c) cp_async16(dst + sw128(r, c), src0 + ks * 128 + c * 16, v0 ? 16u : 0u);
         cp_async_commit();
         ++pending;
         if (pending > kAPipeLag) {
@@ -390,6 +358,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
   } else if (warp >= kWarpDq0 && warp < kWarpDq0 + kNumDqWarps) {
     // ---------------- dequantisation: B operand ----------------
     const int r = threadIdx.x - kWarpDq0 * 32;  // weight row 0..255 of the tile
+    const bool vec_sb = (K / 64) % 8 == 0;
     uint32_t it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
@@ -404,26 +373,65 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
       const size_t row = GATEUP ? size_t(ex) * a.I + j * 128 + (r & 127) : size_t(ex) * a.D + j * BN + r;
       const uint16_t* srow = m.scales + row * (K / 64);
       const uint16_t* brow = m.biases + row * (K / 64);
-      uint16_t s_next = srow[0], b_next = brow[0];
-      for (int ks = 0; ks < KS; ++ks, ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1u;
-        const uint16_t sc = s_next, bi = b_next;
-        if (ks + 1 < KS) {
-          s_next = srow[ks + 1];
-          b_next = brow[ks + 1];
+      // scales and biases: windows of 8 groups (16 bytes) fetched one window
+      // ahead when rows hold a multiple of 8 groups; else one group ahead
+      uint4 s_cur = make_uint4(0u, 0u, 0u, 0u), b_cur = s_cur, s_nxt = s_cur, b_nxt = s_cur;
+      uint16_t s_one = 0, b_one = 0;
+      if (vec_sb) {
+        s_cur = *reinterpret_cast<const uint4*>(srow);
+        b_cur = *reinterpret_cast<const uint4*>(brow);
+        if (KS > 8) {
+          s_nxt = *reinterpret_cast<const uint4*>(srow + 8);
+          b_nxt = *reinterpret_cast<const uint4*>(brow + 8);
         }
-        if (!(ok = mbar_wait(cfull(s), ph, abort_flag, a.hdr))) break;
-        const uint4* cw = reinterpret_cast<const uint4*>(gbase + kOffC + s * kCBytes + r * 32);
-        const uint4 w0 = cw[0], w1 = cw[1];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cempty(s));
+      } else {
+        s_one = srow[0];
+        b_one = brow[0];
+      }
+      for (int ks = 0; ks < KS; ++ks, ++it) {
+        const int s = it % kStages, cs = it % kCStages;
+        const uint32_t ph = (it / kStages) & 1u, cph = (it / kCStages) & 1u;
+        uint16_t sc, bi;
+        if (vec_sb) {
+          const int gi = ks & 7;
+          sc = pick_bf16(s_cur, gi);
+          bi = pick_bf16(b_cur, gi);
+          if (gi == 7) {
+            s_cur = s_nxt;
+            b_cur = b_nxt;
+            if (ks + 9 < KS) {
+              s_nxt = *reinterpret_cast<const uint4*>(srow + ks + 9);
+              b_nxt = *reinterpret_cast<const uint4*>(brow + ks + 9);
+            }
+          }
+        } else {
+          sc = s_one;
+          bi = b_one;
+          if (ks + 1 < KS) {
+            s_one = srow[ks + 1];
+            b_one = brow[ks + 1];
+          }
+        }
+        if (!(ok = mbar_wait(cfull(cs), cph, abort_flag, a.hdr))) break;
+        // the two 16-byte halves of the row's codes, read in an order that
+        // spreads a quarter-warp over all banks
+        const uint4* cw = reinterpret_cast<const uint4*>(gbase + kOffC + cs * kCBytes + r * 32);
+        const int h0 = (r >> 2) & 1;
+        const uint4 first = cw[h0], second = cw[h0 ^ 1];
+        const uint4 w0 = h0 ? second : first, w1 = h0 ? first : second;
         const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16(sc), __ushort_as_bfloat16(sc));
         const __nv_bfloat162 b2 = __halves2bfloat162(__ushort_as_bfloat16(bi), __ushort_as_bfloat16(bi));
         const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         uint32_t o[8][4];
 #pragma unroll
         for (int c = 0; c < 8; ++c) dq8_bf16(words[c], s2, b2, o[c]);
+        // The code stage goes back to the TMA (an async-proxy writer) only
+        // after every lane's reads of it have returned: the dequantised values
+        // above depend on them. The proxy fence orders those generic-proxy
+        // reads before the next asynchronous write of the stage.
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cempty(cs));
         if (!(ok = mbar_wait(empty(s), ph ^ 1u, abort_flag, a.hdr))) break;
         uint8_t* bt = gbase + kOffB + s * kBBytes;
 #pragma unroll
@@ -437,7 +445,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kNumEpiWarps) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;
     uint32_t tc = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
@@ -446,60 +453,62 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
         *abort_flag = 1;
         break;
       }
-      const int buf = tc & 1;
-      const uint32_t aph = (tc >> 1) & 1u;
       // test hook: a wait on a barrier nothing arrives on, bounded by the hook's limit
       if (a.epi_wait_limit > 0 && !(ok = mbar_wait(never_bar, 0, abort_flag, a.hdr, a.epi_wait_limit))) break;
-      if (!(ok = mbar_wait(accf(buf), aph, abort_flag, a.hdr))) break;
+      const int buf = tc & 1;
+      if (!(ok = mbar_wait(accf(buf), (tc >> 1) & 1u, abort_flag, a.hdr))) break;
       tc_fence_after();
-      const bool valid = r < R;
-      const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + buf * BN;
-      if (GATEUP) {
-        uint16_t* hrow = a.h + size_t(p0 + (valid ? r : 0)) * a.I + j * 128;
+      {
+        const int r = q * 32 + lane;  // tile row of this thread
+        const bool valid = r < R;
+        const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + buf * BN;
+        if (GATEUP) {
+          uint16_t* hrow = a.h + size_t(p0 + (valid ? r : 0)) * a.I + j * 128;
 #pragma unroll 1
-        for (int cc = 0; cc < 128; cc += 16) {
-          uint32_t gv[16], uv[16];
-          tmem_ld16(tbase + cc, gv);
-          tmem_ld16(tbase + 128 + cc, uv);
-          tmem_wait_ld();
-          uint32_t pk[8];
+          for (int cc = 0; cc < 128; cc += 16) {
+            uint32_t gv[16], uv[16];
+            tmem_ld16(tbase + cc, gv);
+            tmem_ld16(tbase + 128 + cc, uv);
+            tmem_wait_ld();
+            uint32_t pk[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float h0 = silu_mul(__uint_as_float(gv[2 * i]), __uint_as_float(uv[2 * i]));
-            const float h1 = silu_mul(__uint_as_float(gv[2 * i + 1]), __uint_as_float(uv[2 * i + 1]));
-            pk[i] = uint32_t(f32_to_bf16(h0)) | (uint32_t(f32_to_bf16(h1)) << 16);
+            for (int i = 0; i < 8; ++i) {
+              const float h0 = silu_mul(__uint_as_float(gv[2 * i]), __uint_as_float(uv[2 * i]));
+              const float h1 = silu_mul(__uint_as_float(gv[2 * i + 1]), __uint_as_float(uv[2 * i + 1]));
+              pk[i] = uint32_t(f32_to_bf16(h0)) | (uint32_t(f32_to_bf16(h1)) << 16);
+            }
+            if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(hrow + cc);
+              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
           }
+        } else {
+          int t = 0;
+          float wgt = 0.f;
           if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(hrow + cc);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            const int p = p0 + r;
+            if (g == a.E) {
+              t = p - A_rows;
+              wgt = 1.f;
+            } else {
+              const int asg = a.perm[p];
+              t = asg / a.k;
+              wgt = a.topk_w[asg];
+            }
           }
-        }
-      } else {
-        int t = 0;
-        float wgt = 0.f;
-        if (valid) {
-          const int p = p0 + r;
-          if (g == a.E) {
-            t = p - A_rows;
-            wgt = 1.f;
-          } else {
-            const int asg = a.perm[p];
-            t = asg / a.k;
-            wgt = a.topk_w[asg];
-          }
-        }
-        float* yrow = a.y_acc + size_t(t) * a.D + j * BN;
+          float* yrow = a.y_acc + size_t(t) * a.D + j * BN;
 #pragma unroll 1
-        for (int cc = 0; cc < BN; cc += 16) {
-          uint32_t v[16];
-          tmem_ld16(tbase + cc, v);
-          tmem_wait_ld();
-          if (valid) {
+          for (int cc = 0; cc < BN; cc += 16) {
+            uint32_t v[16];
+            tmem_ld16(tbase + cc, v);
+            tmem_wait_ld();
+            if (valid) {
 #pragma unroll
-            for (int i = 0; i < 16; i += 4)
-              red_add_v4(yrow + cc + i, wgt * __uint_as_float(v[i]), wgt * __uint_as_float(v[i + 1]),
-                         wgt * __uint_as_float(v[i + 2]), wgt * __uint_as_float(v[i + 3]));
+              for (int i = 0; i < 16; i += 4)
+                red_add_v4(yrow + cc + i, wgt * __uint_as_float(v[i]), wgt * __uint_as_float(v[i + 1]),
+                           wgt * __uint_as_float(v[i + 2]), wgt * __uint_as_float(v[i + 3]));
+            }
           }
         }
       }
@@ -618,7 +627,7 @@ cudaError_t gemm_tc(const Ctx& c) {
   std::memset(&maps, 0, sizeof(maps));
   ok = make_map(&maps.c0, U32, 4, w->down.codes, uint64_t(c.E) * c.D, c.I / 8, 8, BN, NOSW) &&
        make_map(&maps.cs0, U32, 4, w->s_down.codes, c.D, c.I / 8, 8, BN, NOSW) &&
-       make_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.h, uint64_t(A + c.T), c.I, BK, BM,
+       make_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.h, uint64_t(A + c.T), c.I, BK, kTileRows,
                 CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   const int grid2 = std::max(1, std::min(num_sms(), c.max_blocks * (c.D / BN)));

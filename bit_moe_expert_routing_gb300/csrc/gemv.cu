@@ -4,18 +4,20 @@
 // traffic"; the switch to matrix kernels above a row count follows
 // "Why continuous batching halved LLM throughput on an M2 Mac mini").
 //
-//   gemv_gateup: one warp per (expert block, intermediate row i). Lanes stream
-//     the gate and up rows of i with 128-bit loads (32 codes per load), dot
-//     them with every token row of the block, reduce with shuffles and write
+//   gemv_gateup: a CTA owns 32 consecutive intermediate rows of one expert
+//     block. Their gate and up codes, scales and biases are contiguous in
+//     memory, so one thread fetches all of them into shared memory with six
+//     bulk (TMA) copies on one mbarrier while the CTA stages the block's token
+//     rows. Each warp then dots four rows with every token and writes
 //     h = bf16(silu(g) * u) in the permuted order.
-//   gemv_down: one warp per output column d. For each token it reads row d of
-//     the down matrix of each of its k experts and of the shared expert, dots
-//     it with h, scales by the routing weight and sums, then writes
-//     y = bf16(sum). No atomics: the result is deterministic.
+//   gemv_down: a CTA owns 16 output columns of one token. It bulk-copies the
+//     16 rows of the down matrix of each of the token's k experts and of the
+//     shared expert, stages the token's k+1 h rows, and sums
+//     w_j * (h_j . row) in fp32; y = bf16(sum). No atomics: deterministic.
 //
-// The kernels are bound by weight reads, so each warp issues its weight loads
-// before anything else (the activations are staged while those loads fly),
-// and register use is capped so that four CTAs share an SM.
+// The kernels are bound by weight reads: every byte a CTA needs is in flight
+// at once (bulk copies do not hold registers), and the grids fill the GPU in
+// about one wave.
 //
 // Per group of 64 weights w = s*q + b, so a dot product over a 32-code chunk
 // of one group is s * sum(x*q) + b * sum(x). The codes enter the sum as fp32
@@ -26,17 +28,20 @@
 // Activations live in shared memory chunk-major: for a row of K values with
 // nch = K/32 chunks, float4 number (jq * nch + c) holds values 32c+4jq..32c+4jq+3.
 // Lane l works on chunk c = l + 32m, so the lanes of a warp read consecutive
-// float4s (no bank conflicts).
+// float4s and consecutive 16-byte code chunks (no bank conflicts).
 #include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kMaxGemvRows = 8;
 constexpr int kGemvWarps = 8;
+constexpr int kGateupRows = 32;  // intermediate rows per gate/up CTA
+constexpr int kDownCols = 16;    // output columns per down CTA
 
 // fp32 value 128 + q of the nibble in bits 16..19 of w_shifted.
 __device__ __forceinline__ float q128(uint32_t w_shifted) {
@@ -54,15 +59,16 @@ __device__ __forceinline__ float2 dot8_128(uint32_t w, float4 xa, float4 xb, flo
   return acc;
 }
 
-// s * sum(x*q) + b * sum(x) over one 32-code chunk; sb = (scale, bias) bf16 pair.
+// s * sum(x*q) + b * sum(x) over one 32-code chunk c of a row; xr is the
+// chunk-major activation row, s and b the bf16 scale and bias of the chunk.
 __device__ __forceinline__ float chunk_dot(const uint4 w4, const float4* xr, int nch, int c, float xsum,
-                                           uint32_t sb) {
+                                           uint16_t s, uint16_t b) {
   float2 d = make_float2(0.f, 0.f);
   d = dot8_128(w4.x, xr[0 * nch + c], xr[1 * nch + c], d);
   d = dot8_128(w4.y, xr[2 * nch + c], xr[3 * nch + c], d);
   d = dot8_128(w4.z, xr[4 * nch + c], xr[5 * nch + c], d);
   d = dot8_128(w4.w, xr[6 * nch + c], xr[7 * nch + c], d);
-  return bf16lo(sb) * (d.x + d.y - 128.f * xsum) + bf16hi(sb) * xsum;
+  return bf16_to_f32(s) * (d.x + d.y - 128.f * xsum) + bf16_to_f32(b) * xsum;
 }
 
 struct GemvArgs {
@@ -80,8 +86,7 @@ struct GemvArgs {
   int T, D, E, k, I;
 };
 
-// Stages bf16 row `r` (K values, 16-byte aligned) into chunk-major fp32;
-// called by all threads of the CTA for q8 = thread, thread + blockDim, ...
+// Stages 8 bf16 values (number q8 of a row) into a chunk-major fp32 row.
 __device__ __forceinline__ void stage_bf16x8(float4* rowdst, int nch, int q8, uint4 v) {
   const int c = q8 >> 2, jq = (q8 & 3) * 2;
   rowdst[jq * nch + c] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
@@ -103,18 +108,27 @@ __device__ __forceinline__ void chunk_sums(const float4* xs4, float* xsum, int r
   }
 }
 
-// Shared memory: xs4 [R][8*nch] float4 (chunk-major x rows), xsum [R][nch],
-// then the gate and up results of the CTA's rows. Warp w streams row
-// blockIdx.y * 4 + w/2 of the gate (even w) or up (odd w) matrix; the pair
-// meets in shared memory for h = silu(g) * u. CPL = 32-code chunks per lane
-// (ceil(D/1024)).
-constexpr int kGateupRowsPerCta = kGemvWarps / 2;
+__device__ __forceinline__ size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
-template <int CPL>
-__global__ void __launch_bounds__(kGemvWarps * 32, CPL == 1 ? 4 : 3) gemv_gateup_kernel(GemvArgs a) {
-  extern __shared__ float4 gv_smem[];
-  float4* xs4 = gv_smem;
-  __shared__ float s_gu[kGemvWarps][kMaxGemvRows];
+// Shared-memory layout of a gate/up CTA (D input columns, R token rows).
+struct GateupSmem {
+  size_t codes_g, codes_u, sg, bg, su, bu, xs4, xsum, total;
+  __host__ __device__ GateupSmem(int D, int R) {
+    const size_t cb = size_t(kGateupRows) * D / 2, sbb = size_t(kGateupRows) * (D / 64) * 2;
+    codes_g = 16;  // bytes 0..15: mbarrier and abort flag
+    codes_u = codes_g + cb;
+    sg = codes_u + cb;
+    bg = sg + sbb;
+    su = bg + sbb;
+    bu = su + sbb;
+    xs4 = (bu + sbb + 15) & ~size_t(15);
+    xsum = xs4 + size_t(R) * D * 4;
+    total = xsum + size_t(R) * (D / 32) * 4;
+  }
+};
+
+__global__ void __launch_bounds__(kGemvWarps * 32) gemv_gateup_kernel(GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t gsm[];
   if (blockIdx.x >= *a.n_blocks) return;
   const int g = a.blocks[3 * blockIdx.x], p0 = a.blocks[3 * blockIdx.x + 1], R = a.blocks[3 * blockIdx.x + 2];
   const int A = a.T * a.k;
@@ -122,30 +136,34 @@ __global__ void __launch_bounds__(kGemvWarps * 32, CPL == 1 ? 4 : 3) gemv_gateup
     if (threadIdx.x == 0) report(a.hdr, MOE_ERR_DEVICE_CHECK, 3);
     return;
   }
-  const int D = a.D, I = a.I, nch = D / 32;
-  float* xsum = reinterpret_cast<float*>(xs4 + size_t(R) * 8 * nch);
+  const int D = a.D, I = a.I, nch = D / 32, G = D / 64;
+  const GateupSmem L(D, min(a.T, kMaxGemvRows));
   const bool shared = (g == a.E);
   const int ex = shared ? 0 : g;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const moe_qmatrix m = (warp & 1) ? (shared ? a.s_up : a.up) : (shared ? a.s_gate : a.gate);
-  const int i = blockIdx.y * kGateupRowsPerCta + (warp >> 1);
-  const bool row_ok = i < I;
-  const size_t row = size_t(ex) * I + (row_ok ? i : 0);
+  const moe_qmatrix mg = shared ? a.s_gate : a.gate;
+  const moe_qmatrix mu = shared ? a.s_up : a.up;
+  const int i0 = blockIdx.y * kGateupRows;
+  const int nr = min(kGateupRows, I - i0);
+  const uint32_t bar = smem_u32(gsm);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gsm + 8);
 
-  // this warp's weights first: they do not depend on x
-  uint4 w4[CPL];
-  uint32_t sb[CPL];
-#pragma unroll
-  for (int mm = 0; mm < CPL; ++mm) {
-    const int c = lane + 32 * mm;
-    w4[mm] = make_uint4(0u, 0u, 0u, 0u);
-    sb[mm] = 0u;
-    if (c < nch && row_ok) {
-      w4[mm] = __ldcs(reinterpret_cast<const uint4*>(m.codes + row * (D / 8)) + c);
-      sb[mm] = uint32_t(m.scales[row * (D / 64) + c / 2]) | (uint32_t(m.biases[row * (D / 64) + c / 2]) << 16);
-    }
+  if (threadIdx.x == 0) {  // all of this CTA's weights, in six bulk copies
+    *abort_flag = 0;
+    mbar_init(bar, 1);
+    mbar_init_fence();
+    const uint32_t cb = uint32_t(nr) * D / 2, sbb = uint32_t(nr) * G * 2;
+    const size_t row0 = size_t(ex) * I + i0;
+    mbar_arrive_tx(bar, 2 * cb + 4 * sbb);
+    bulk_g2s(bar + uint32_t(L.codes_g), mg.codes + row0 * (D / 8), cb, bar);
+    bulk_g2s(bar + uint32_t(L.codes_u), mu.codes + row0 * (D / 8), cb, bar);
+    bulk_g2s(bar + uint32_t(L.sg), mg.scales + row0 * G, sbb, bar);
+    bulk_g2s(bar + uint32_t(L.bg), mg.biases + row0 * G, sbb, bar);
+    bulk_g2s(bar + uint32_t(L.su), mu.scales + row0 * G, sbb, bar);
+    bulk_g2s(bar + uint32_t(L.bu), mu.biases + row0 * G, sbb, bar);
   }
 
+  float4* xs4 = reinterpret_cast<float4*>(gsm + L.xs4);
+  float* xsum = reinterpret_cast<float*>(gsm + L.xsum);
   for (int q = threadIdx.x; q < R * (D / 8); q += blockDim.x) {
     const int r = q / (D / 8), q8 = q % (D / 8);
     const int p = p0 + r;
@@ -155,129 +173,137 @@ __global__ void __launch_bounds__(kGemvWarps * 32, CPL == 1 ? 4 : 3) gemv_gateup
   __syncthreads();
   chunk_sums(xs4, xsum, R, nch);
   __syncthreads();
+  if (!mbar_wait(bar, 0, abort_flag, a.hdr, kWaitLimit, true)) return;
 
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint8_t* cg = gsm + L.codes_g;
+  const uint8_t* cu = gsm + L.codes_u;
+  const uint16_t* sg = reinterpret_cast<const uint16_t*>(gsm + L.sg);
+  const uint16_t* bg = reinterpret_cast<const uint16_t*>(gsm + L.bg);
+  const uint16_t* su = reinterpret_cast<const uint16_t*>(gsm + L.su);
+  const uint16_t* bu = reinterpret_cast<const uint16_t*>(gsm + L.bu);
+  for (int rr = warp; rr < nr; rr += kGemvWarps) {
+    const uint4* rg = reinterpret_cast<const uint4*>(cg + size_t(rr) * D / 2);
+    const uint4* ru = reinterpret_cast<const uint4*>(cu + size_t(rr) * D / 2);
 #pragma unroll 1
-  for (int r = 0; r < R; ++r) {
-    const float4* xr = xs4 + size_t(r) * 8 * nch;
-    float v = 0.f;
+    for (int r = 0; r < R; ++r) {
+      const float4* xr = xs4 + size_t(r) * 8 * nch;
+      float gv = 0.f, uv = 0.f;
+      for (int c = lane; c < nch; c += 32) {  // 32-code chunk c lies in group c/2
+        const float sx = xsum[r * nch + c];
+        const int gi = rr * G + c / 2;
+        gv += chunk_dot(rg[c], xr, nch, c, sx, sg[gi], bg[gi]);
+        uv += chunk_dot(ru[c], xr, nch, c, sx, su[gi], bu[gi]);
+      }
 #pragma unroll
-    for (int mm = 0; mm < CPL; ++mm) {
-      const int c = lane + 32 * mm;  // 32-code chunk c lies in group c/2
-      if (c < nch) v += chunk_dot(w4[mm], xr, nch, c, xsum[r * nch + c], sb[mm]);
+      for (int off = 16; off >= 1; off >>= 1) {
+        gv += __shfl_xor_sync(0xffffffffu, gv, off);
+        uv += __shfl_xor_sync(0xffffffffu, uv, off);
+      }
+      if (lane == 0) a.h[size_t(p0 + r) * I + i0 + rr] = f32_to_bf16(silu_mul(gv, uv));
     }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (lane == 0) s_gu[warp][r] = v;
-  }
-  __syncthreads();
-  for (int q = threadIdx.x; q < kGateupRowsPerCta * R; q += blockDim.x) {
-    const int rr = q / R, r = q % R, ii = blockIdx.y * kGateupRowsPerCta + rr;
-    if (ii < I) a.h[size_t(p0 + r) * I + ii] = f32_to_bf16(silu_mul(s_gu[2 * rr][r], s_gu[2 * rr + 1][r]));
   }
 }
 
-// Shared memory: hs4 [T*(k+1)][8*nch] float4 (chunk-major h rows in
-// (token, slot) order, slot k = shared expert), hsum [T*(k+1)][nch], and the
-// routing weight of each row. One warp per output column d; the (slot, chunk)
-// items of a token are spread over the lanes, kDownBatch per lane per pass.
-constexpr int kDownBatch = 6;
+// Shared-memory layout of a down CTA (k+1 slots, I input columns).
+struct DownSmem {
+  size_t codes, sc, bi, hs4, hsum, w, total;
+  __host__ __device__ DownSmem(int k, int I) {
+    const size_t S = size_t(k) + 1;
+    codes = 16;  // bytes 0..15: mbarrier and abort flag
+    sc = codes + S * kDownCols * (I / 2);
+    bi = sc + S * kDownCols * (I / 64) * 2;
+    hs4 = (bi + S * kDownCols * (I / 64) * 2 + 15) & ~size_t(15);
+    hsum = hs4 + S * size_t(I) * 4;
+    w = hsum + S * size_t(I / 32) * 4;
+    total = w + S * 4;
+  }
+};
 
-__global__ void __launch_bounds__(kGemvWarps * 32, 4) gemv_down_kernel(GemvArgs a) {
-  extern __shared__ float4 gv_smem[];
-  const int T = a.T, k = a.k, I = a.I, D = a.D, nch = I / 32;
-  const int nrows = T * (k + 1), A = T * k, nitems = (k + 1) * nch;
-  float4* hs4 = gv_smem;
-  float* hsum = reinterpret_cast<float*>(hs4 + size_t(nrows) * 8 * nch);
-  float* s_w = hsum + nrows * nch;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int d = blockIdx.x * kGemvWarps + warp;
-  const bool d_ok = d < D;
-
-  uint4 w4[kDownBatch];
-  uint32_t sb[kDownBatch];
-  auto load = [&](int t, int base) {
-#pragma unroll
-    for (int u = 0; u < kDownBatch; ++u) {
-      const int it = base + 32 * u + lane;
-      w4[u] = make_uint4(0u, 0u, 0u, 0u);
-      sb[u] = 0u;
-      if (d_ok && it < nitems) {
-        const int j = it / nch, c = it % nch;
-        const bool sh = (j == k);
-        const int ex = sh ? 0 : a.topk_idx[t * k + j];
-        const moe_qmatrix& m = sh ? a.s_down : a.down;
-        const size_t row = size_t(ex) * D + d;
-        w4[u] = __ldcs(reinterpret_cast<const uint4*>(m.codes + row * (I / 8)) + c);
-        sb[u] = uint32_t(m.scales[row * (I / 64) + c / 2]) | (uint32_t(m.biases[row * (I / 64) + c / 2]) << 16);
-      }
+// grid (D / kDownCols, T): blockIdx.y is the token.
+__global__ void __launch_bounds__(kGemvWarps * 32) gemv_down_kernel(GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  const int k = a.k, I = a.I, D = a.D, nch = I / 32, G = I / 64, S = k + 1;
+  const int t = blockIdx.y, d0 = blockIdx.x * kDownCols, A = a.T * k;
+  const DownSmem L(k, I);
+  const uint32_t bar = smem_u32(dsm);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(dsm + 8);
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar, S);  // one arrival (with its byte count) per slot
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (threadIdx.x < S) {  // slot j: rows d0..d0+15 of its expert's down matrix
+    const int j = threadIdx.x;
+    const bool sh = (j == k);
+    int ex = sh ? 0 : a.topk_idx[t * k + j];
+    if (ex < 0 || ex >= a.E) {
+      report(a.hdr, MOE_ERR_DEVICE_CHECK, 8);
+      ex = 0;
     }
-  };
-  load(0, 0);  // the first token's weights fly while h is staged
-
-  for (int q = threadIdx.x; q < nrows * (I / 8); q += blockDim.x) {
-    const int rr = q / (I / 8), q8 = q % (I / 8);
-    const int t = rr / (k + 1), j = rr % (k + 1);
+    const moe_qmatrix& m = sh ? a.s_down : a.down;
+    const size_t row0 = size_t(ex) * D + d0;
+    const uint32_t cb = kDownCols * (I / 2), sbb = kDownCols * G * 2;
+    mbar_arrive_tx(bar, cb + 2 * sbb);
+    bulk_g2s(bar + uint32_t(L.codes + size_t(j) * cb), m.codes + row0 * (I / 8), cb, bar);
+    bulk_g2s(bar + uint32_t(L.sc + size_t(j) * sbb), m.scales + row0 * G, sbb, bar);
+    bulk_g2s(bar + uint32_t(L.bi + size_t(j) * sbb), m.biases + row0 * G, sbb, bar);
+  }
+  float4* hs4 = reinterpret_cast<float4*>(dsm + L.hs4);
+  float* hsum = reinterpret_cast<float*>(dsm + L.hsum);
+  float* s_w = reinterpret_cast<float*>(dsm + L.w);
+  for (int q = threadIdx.x; q < S * (I / 8); q += blockDim.x) {
+    const int j = q / (I / 8), q8 = q % (I / 8);
     const int p = j < k ? a.inv[t * k + j] : A + t;
-    stage_bf16x8(hs4 + size_t(rr) * 8 * nch, nch, q8, *reinterpret_cast<const uint4*>(a.h + size_t(p) * I + q8 * 8));
+    stage_bf16x8(hs4 + size_t(j) * 8 * nch, nch, q8, *reinterpret_cast<const uint4*>(a.h + size_t(p) * I + q8 * 8));
   }
-  for (int rr = threadIdx.x; rr < nrows; rr += blockDim.x) {
-    const int t = rr / (k + 1), j = rr % (k + 1);
-    s_w[rr] = j < k ? a.topk_w[t * k + j] : 1.f;
-  }
+  for (int j = threadIdx.x; j < S; j += blockDim.x) s_w[j] = j < k ? a.topk_w[t * k + j] : 1.f;
   __syncthreads();
-  chunk_sums(hs4, hsum, nrows, nch);
+  chunk_sums(hs4, hsum, S, nch);
   __syncthreads();
-  if (!d_ok) return;
+  if (!mbar_wait(bar, 0, abort_flag, a.hdr, kWaitLimit, true)) return;
 
-  for (int t = 0; t < T; ++t) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint8_t* codes = dsm + L.codes;
+  const uint16_t* sc = reinterpret_cast<const uint16_t*>(dsm + L.sc);
+  const uint16_t* bi = reinterpret_cast<const uint16_t*>(dsm + L.bi);
+  for (int cl = warp; cl < kDownCols; cl += kGemvWarps) {
     float part = 0.f;
-    for (int base = 0; base < nitems; base += 32 * kDownBatch) {
-      if (t > 0 || base > 0) load(t, base);
-#pragma unroll
-      for (int u = 0; u < kDownBatch; ++u) {
-        const int it = base + 32 * u + lane;
-        if (it < nitems) {
-          const int j = it / nch, c = it % nch;
-          const int rr = t * (k + 1) + j;
-          part += s_w[rr] * chunk_dot(w4[u], hs4 + size_t(rr) * 8 * nch, nch, c, hsum[rr * nch + c], sb[u]);
-        }
-      }
+    for (int it = lane; it < S * nch; it += 32) {
+      const int j = it / nch, c = it % nch;
+      const int rowi = j * kDownCols + cl;  // row of slot j's copy
+      const uint4 w4 = reinterpret_cast<const uint4*>(codes + size_t(rowi) * (I / 2))[c];
+      const int gi = rowi * G + c / 2;
+      part += s_w[j] * chunk_dot(w4, hs4 + size_t(j) * 8 * nch, nch, c, hsum[j * nch + c], sc[gi], bi[gi]);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if (lane == 0) a.y[size_t(t) * D + d] = f32_to_bf16(part);
+    if (lane == 0) a.y[size_t(t) * D + d0 + cl] = f32_to_bf16(part);
   }
-}
-
-size_t gateup_smem(const Ctx& c) {
-  return size_t(std::min(c.T, kMaxGemvRows)) * (size_t(c.D) * 4 + size_t(c.D / 32) * 4);
-}
-size_t down_smem(const Ctx& c) {
-  return size_t(c.T) * (c.k + 1) * (size_t(c.I) * 4 + size_t(c.I / 32) * 4 + 4);
 }
 
 }  // namespace
 
 bool gemv_supported(const Ctx& c) {
-  return c.T >= 1 && c.T <= kMaxGemvRows && c.D <= 4096 && gateup_smem(c) <= 200 * 1024 &&
-         down_smem(c) <= 200 * 1024;
+  if (c.T < 1 || c.T > kMaxGemvRows || c.k + 1 > kGemvWarps * 32) return false;
+  const size_t lim = 200 * 1024;
+  return GateupSmem(c.D, std::min(c.T, kMaxGemvRows)).total <= lim && DownSmem(c.k, c.I).total <= lim;
 }
 
 cudaError_t gemv(const Ctx& c) {
   const moe_weights* w = c.w;
   GemvArgs a{c.x, w->gate, w->up, w->down, w->s_gate, w->s_up, w->s_down, c.blocks, c.n_blocks,
              c.perm, c.inv, c.topk_idx, c.topk_w, c.h, c.y, c.hdr, c.T, c.D, c.E, c.k, c.I};
-  const size_t s1 = gateup_smem(c), s2 = down_smem(c);
-  const int cpl = (c.D / 32 + 31) / 32;
-  void (*gk)(GemvArgs) = cpl <= 1 ? gemv_gateup_kernel<1> : cpl <= 2 ? gemv_gateup_kernel<2> : gemv_gateup_kernel<4>;
-  if (!ensure_smem_limit(reinterpret_cast<const void*>(gk), int(s1)) ||
+  const size_t s1 = GateupSmem(c.D, std::min(c.T, kMaxGemvRows)).total, s2 = DownSmem(c.k, c.I).total;
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(gemv_gateup_kernel), int(s1)) ||
       !ensure_smem_limit(reinterpret_cast<const void*>(gemv_down_kernel), int(s2)))
     return cudaErrorInvalidValue;
   cudaError_t err;
-  gk<<<dim3(c.max_blocks, (c.I + kGateupRowsPerCta - 1) / kGateupRowsPerCta), kGemvWarps * 32, s1, c.stream>>>(a);
+  gemv_gateup_kernel<<<dim3(c.max_blocks, (c.I + kGateupRows - 1) / kGateupRows), kGemvWarps * 32, s1, c.stream>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done("gemv_gateup", c.stream);
-  gemv_down_kernel<<<(c.D + kGemvWarps - 1) / kGemvWarps, kGemvWarps * 32, s2, c.stream>>>(a);
+  gemv_down_kernel<<<dim3(c.D / kDownCols, c.T), kGemvWarps * 32, s2, c.stream>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done("gemv_down", c.stream);
   return cudaSuccess;

@@ -14,6 +14,9 @@ struct WsHeader;
 // Chunk of tokens handled by one CTA of the top-k/histogram and scatter steps.
 constexpr int kChunkTokens = 64;
 
+// Rows per block-map entry consumed by the tensor-core GEMM.
+constexpr int kTcBlockRows = 128;
+
 // One call's resolved sizes and device pointers.
 struct Ctx {
   const moe_weights* w;

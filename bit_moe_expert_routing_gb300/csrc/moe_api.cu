@@ -167,6 +167,24 @@ void fill_view(const Ctx& c, moe_route_view* v) {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+enum class Path { Gemv, GemmTc, GemmSimt };
+
+// Chooses the expert path for this call and the block-map row count it
+// consumes (the tensor-core GEMM takes 256-row blocks, the others 128).
+Path plan(Ctx& c) {
+  int path = g_opt.force_path;
+  if (path == 0) path = (c.T <= g_opt.gemv_max_rows) ? 1 : 2;
+  Path p;
+  if (path == 1 && gemv_supported(c))
+    p = Path::Gemv;
+  else if (g_opt.gemm_impl == 0 && gemm_tc_supported(c))
+    p = Path::GemmTc;
+  else
+    p = Path::GemmSimt;
+  c.BM = (p == Path::GemmTc) ? kTcBlockRows : kDefaultBlockM;
+  return p;
+}
+
 }  // namespace
 
 bool ensure_smem_limit(const void* func, int bytes) {
@@ -218,6 +236,7 @@ moe_status moe_route(const moe_weights* w, const uint16_t* x, int T, void* works
   if (moe_status s = make_ctx(w, x, T, nullptr, workspace, workspace_bytes, stream, &c)) return s;
   if (T > 0 && (!x || !aligned16(x))) return MOE_ERR_ARG;
   t_launches = 0;
+  plan(c);
   if (view) fill_view(c, view);
   if (T == 0) return MOE_OK;
   timing_begin(c.stream);
@@ -229,6 +248,7 @@ moe_status moe_workspace_view(const moe_weights* w, int T, void* workspace, size
   Ctx c;
   if (!view) return MOE_ERR_ARG;
   if (moe_status s = make_ctx(w, nullptr, T, nullptr, workspace, workspace_bytes, nullptr, &c)) return s;
+  plan(c);
   fill_view(c, view);
   return MOE_OK;
 }
@@ -240,14 +260,12 @@ moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uin
   t_launches = 0;
   if (T == 0) return MOE_OK;
   if (!x || !y || !aligned16(x) || !aligned16(y) || x == y) return MOE_ERR_ARG;
+  const Path path = plan(c);
   timing_begin(c.stream);
   cudaError_t err = route(c);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
-  int path = g_opt.force_path;
-  if (path == 0) path = (T <= g_opt.gemv_max_rows) ? 1 : 2;
-  if (path == 1 && !gemv_supported(c)) path = 2;
-  if (path == 1) return cuda_status(gemv(c));
-  if (g_opt.gemm_impl == 0 && gemm_tc_supported(c)) return cuda_status(gemm_tc(c));
+  if (path == Path::Gemv) return cuda_status(gemv(c));
+  if (path == Path::GemmTc) return cuda_status(gemm_tc(c));
   return cuda_status(gemm_simt(c));
 }
 

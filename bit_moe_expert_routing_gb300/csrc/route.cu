@@ -15,6 +15,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -311,45 +312,56 @@ __global__ void __launch_bounds__(256)
 // ---- small token counts (decode): two kernels for the whole routing ----------------------
 
 // Router logits for T <= TT tokens: one warp per expert, every token of the
-// call in the same warp. Each lane first loads kSmallBatch of its W_r values
-// (one DRAM round trip for them all), then runs its fixed-order FMA chain.
-constexpr int kSmallBatch = 32;
+// call in the same warp. The CTA's kRouterSmallExperts rows of W_r are
+// contiguous, so one bulk (TMA) copy brings them into shared memory while the
+// token rows are staged; each lane then runs its fixed-order FMA chain.
+constexpr int kRouterSmallExperts = 2;
+
+__host__ __device__ constexpr size_t router_small_smem(int TT, int D) {
+  return 16 + size_t(kRouterSmallExperts) * D * 4 + size_t(TT) * D * 2;
+}
 
 template <int TT>
-__global__ void __launch_bounds__(kRouterWarps * 32)
+__global__ void __launch_bounds__(kRouterSmallExperts * 32)
     router_small_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
                         const float* __restrict__ bias, int T, int D, int E, float* __restrict__ logits,
                         WsHeader* hdr) {
-  extern __shared__ uint4 xsm4[];  // x rows [TT][D] bf16, rows >= T zero
+  extern __shared__ __align__(128) uint8_t rsm[];
+  const uint32_t bar = smem_u32(rsm);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(rsm + 8);
+  const float* ws = reinterpret_cast<const float*>(rsm + 16);
+  uint4* xsm4 = reinterpret_cast<uint4*>(rsm + 16 + size_t(kRouterSmallExperts) * D * 4);
   const uint16_t* xsm = reinterpret_cast<const uint16_t*>(xsm4);
-  if (blockIdx.x == 0 && threadIdx.x == 0) {  // first kernel of the call
-    hdr->status = 0;
-    hdr->detail = 0;
+  const int e0 = blockIdx.x * kRouterSmallExperts;
+  const int ne = min(kRouterSmallExperts, E - e0);
+  if (threadIdx.x == 0) {
+    if (blockIdx.x == 0) {  // first kernel of the call: start its status afresh
+      hdr->status = 0;
+      hdr->detail = 0;
+    }
+    *abort_flag = 0;
+    mbar_init(bar, 1);
+    mbar_init_fence();
+    mbar_arrive_tx(bar, uint32_t(ne) * D * 4);
+    bulk_g2s(bar + 16, wr + size_t(e0) * D, uint32_t(ne) * D * 4, bar);
   }
   for (int i = threadIdx.x; i < TT * (D / 8); i += blockDim.x) {
     const int t = i / (D / 8), c8 = i % (D / 8);
     xsm4[i] = t < T ? *reinterpret_cast<const uint4*>(x + size_t(t) * D + c8 * 8) : make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
+  if (!mbar_wait(bar, 0, abort_flag, hdr, kWaitLimit, true)) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int e = blockIdx.x * kRouterWarps + warp;
-  if (e >= E) return;
-  const float* w = wr + size_t(e) * D;
-  const int nch = D / 32;
+  if (warp >= ne) return;
+  const int e = e0 + warp;
+  const float* w = ws + size_t(warp) * D;
   float acc[TT];
 #pragma unroll
   for (int t = 0; t < TT; ++t) acc[t] = 0.f;
-  for (int c0 = 0; c0 < nch; c0 += kSmallBatch) {
-    float wv[kSmallBatch];
+  for (int c = 0; c < D / 32; ++c) {
+    const float wv = w[c * 32 + lane];
 #pragma unroll
-    for (int u = 0; u < kSmallBatch; ++u) wv[u] = (c0 + u < nch) ? __ldg(w + (c0 + u) * 32 + lane) : 0.f;
-#pragma unroll
-    for (int u = 0; u < kSmallBatch; ++u) {
-      if (c0 + u < nch) {
-#pragma unroll
-        for (int t = 0; t < TT; ++t) acc[t] = fmaf(bf16_to_f32(xsm[t * D + (c0 + u) * 32 + lane]), wv[u], acc[t]);
-      }
-    }
+    for (int t = 0; t < TT; ++t) acc[t] = fmaf(bf16_to_f32(xsm[t * D + c * 32 + lane]), wv, acc[t]);
   }
 #pragma unroll
   for (int t = 0; t < TT; ++t) {
@@ -448,9 +460,9 @@ cudaError_t route(const Ctx& c) {
     const int tt = c.T <= 2 ? 2 : c.T <= 8 ? 8 : 16;
     void (*rk)(const uint16_t*, const float*, const float*, int, int, int, float*, WsHeader*) =
         tt == 2 ? router_small_kernel<2> : tt == 8 ? router_small_kernel<8> : router_small_kernel<16>;
-    const size_t smem = size_t(tt) * c.D * 2;
+    const size_t smem = router_small_smem(tt, c.D);
     if (!ensure_smem_limit(reinterpret_cast<const void*>(rk), int(smem))) return cudaErrorInvalidValue;
-    rk<<<(c.E + kRouterWarps - 1) / kRouterWarps, kRouterWarps * 32, smem, c.stream>>>(
+    rk<<<(c.E + kRouterSmallExperts - 1) / kRouterSmallExperts, kRouterSmallExperts * 32, smem, c.stream>>>(
         c.x, w->router_w, w->router_bias, c.T, c.D, c.E, c.logits, c.hdr);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     launch_done("router_small", c.stream);

@@ -92,7 +92,8 @@ typedef struct {
  *   inv       int32 [T*k]      inv[perm[p]] = p
  *   blocks    int32 [max_blocks][3] = (group, first row, rows): for each
  *             expert in ascending order its segment cut into blocks of
- *             block_m rows, then the shared expert as group E over rows
+ *             block_m rows (256 when the call takes the tensor-core GEMM
+ *             path, 128 otherwise), then the shared expert as group E over rows
  *             T*k .. T*k+T-1 (token t at row T*k+t)
  *   n_blocks  int32 [1]        number of valid entries of blocks
  *   h         bf16 [T*k + T, I]  SwiGLU intermediate in the permuted order
