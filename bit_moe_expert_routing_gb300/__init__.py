@@ -32,7 +32,7 @@ MOE_OPT_GEMM_IMPL = 4
 MOE_OPT_TEST_WAIT_CYCLES = 5
 
 PATH_AUTO, PATH_GEMV, PATH_GEMM = 0, 1, 2
-GEMM_TENSOR_CORE, GEMM_CUDA_CORE = 0, 1
+GEMM_TENSOR_CORE, GEMM_CUDA_CORE, GEMM_TENSOR_CORE_SMEM = 0, 1, 2
 
 
 class moe_qmatrix(ctypes.Structure):

@@ -528,47 +528,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
 
 // ---- host side ------------------------------------------------------------------------------
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiled encoder() {
-  static EncodeTiled fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(p);
-  }
-  return fn;
-}
-
-// 2-D tensor map over a row-major [rows, cols] array.
-bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t elem, const void* ptr, uint64_t rows, uint64_t cols,
-              uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
-  EncodeTiled enc = encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * elem};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
-
-long long g_epi_wait_limit = 0;  // 0: no test wait
 
 __global__ void debug_dequant_kernel(moe_qmatrix m, int expert, int rows, int K, uint16_t* out) {
   const int words = K / 8;
@@ -587,7 +547,52 @@ __global__ void debug_dequant_kernel(moe_qmatrix m, int expert, int rows, int K,
 
 }  // namespace
 
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+
+// 2-D tensor map over a row-major [rows, cols] array.
+bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t elem, const void* ptr, uint64_t rows, uint64_t cols,
+              uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * elem};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tmap_encoder_available() { return encoder() != nullptr; }
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+long long g_epi_wait_limit = 0;  // 0: no test wait
+
 void set_tc_epilogue_wait_limit(long long cycles) { g_epi_wait_limit = cycles > 0 ? cycles : 0; }
+long long tc_epilogue_wait_limit() { return g_epi_wait_limit; }
 
 cudaError_t debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, uint16_t* out, cudaStream_t s) {
   debug_dequant_kernel<<<256, 256, 0, s>>>(*m, expert, rows, K, out);
@@ -609,10 +614,10 @@ cudaError_t gemm_tc(const Ctx& c) {
   std::memset(&maps, 0, sizeof(maps));
   const auto U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
   const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
-  bool ok = make_map(&maps.c0, U32, 4, w->gate.codes, uint64_t(c.E) * c.I, c.D / 8, 8, 128, NOSW) &&
-            make_map(&maps.c1, U32, 4, w->up.codes, uint64_t(c.E) * c.I, c.D / 8, 8, 128, NOSW) &&
-            make_map(&maps.cs0, U32, 4, w->s_gate.codes, c.I, c.D / 8, 8, 128, NOSW) &&
-            make_map(&maps.cs1, U32, 4, w->s_up.codes, c.I, c.D / 8, 8, 128, NOSW);
+  bool ok = make_tmap_2d(&maps.c0, U32, 4, w->gate.codes, uint64_t(c.E) * c.I, c.D / 8, 8, 128, NOSW) &&
+            make_tmap_2d(&maps.c1, U32, 4, w->up.codes, uint64_t(c.E) * c.I, c.D / 8, 8, 128, NOSW) &&
+            make_tmap_2d(&maps.cs0, U32, 4, w->s_gate.codes, c.I, c.D / 8, 8, 128, NOSW) &&
+            make_tmap_2d(&maps.cs1, U32, 4, w->s_up.codes, c.I, c.D / 8, 8, 128, NOSW);
   if (!ok) return cudaErrorInvalidValue;
 
   cudaError_t err = zero_yacc(c);
@@ -625,9 +630,9 @@ cudaError_t gemm_tc(const Ctx& c) {
   a.m0 = w->down;
   a.s0 = w->s_down;
   std::memset(&maps, 0, sizeof(maps));
-  ok = make_map(&maps.c0, U32, 4, w->down.codes, uint64_t(c.E) * c.D, c.I / 8, 8, BN, NOSW) &&
-       make_map(&maps.cs0, U32, 4, w->s_down.codes, c.D, c.I / 8, 8, BN, NOSW) &&
-       make_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.h, uint64_t(A + c.T), c.I, BK, kTileRows,
+  ok = make_tmap_2d(&maps.c0, U32, 4, w->down.codes, uint64_t(c.E) * c.D, c.I / 8, 8, BN, NOSW) &&
+       make_tmap_2d(&maps.cs0, U32, 4, w->s_down.codes, c.D, c.I / 8, 8, BN, NOSW) &&
+       make_tmap_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.h, uint64_t(A + c.T), c.I, BK, kTileRows,
                 CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   const int grid2 = std::max(1, std::min(num_sms(), c.max_blocks * (c.D / BN)));

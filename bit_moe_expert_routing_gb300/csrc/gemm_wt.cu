@@ -1,0 +1,610 @@
+// Tensor-core grouped GEMMs of the prefill expert path with the dequantised
+// weights in tensor memory ("Optimizing on-device inference for Apple
+// Silicon", section "Dequantise weights during matrix multiplication": the
+// 4-bit weights are expanded one small tile at a time on chip and never exist
+// expanded in DRAM; section "Reduce intermediate and state traffic": gate/up
+// fused with the gated activation, down fused with the routing weights, the
+// shared expert and the un-permute).
+//
+// The MMA computes D[weight row, token] = W[128 x K] * X[N x K]^T:
+//   A = 128 weight rows, dequantised by eight warps from registers straight
+//       into a tensor-memory stage (tcgen05.st): no shared-memory round trip
+//       for the expanded weights, and the MMA does not read them from shared
+//       memory either;
+//   B = the block's token rows (N <= 192, rounded up to 16), in shared memory
+//       in the 128-byte-swizzled K-major layout: gathered from x with
+//       cp.async (gate/up) or loaded by TMA from h (down);
+//   D = fp32 in tensor memory, two 192-column buffers so the epilogue of one
+//       tile overlaps the next tile's MMAs.
+// Tensor memory (512 columns): accumulators 0..383, A stages 384..511.
+//
+// gate/up tiles take 64 intermediate rows with the gate and up rows
+// interleaved (lane 2i = gate row i, lane 2i+1 = up row i), so the epilogue
+// pairs g and u with one shuffle; down tiles take 128 output columns.
+//
+// Warp roles (22 warps): 0 TMA for the packed codes, 1 TMEM allocator and MMA
+// issuer, 2..5 the token operand (gate/up: cp.async gather of x rows, eight
+// consecutive lanes per 128-byte row so every warp instruction covers four
+// whole cache lines; down: a 2-D TMA tile of h), 6..13 dequantisation (two
+// warps per TMEM lane quarter, 32 of the 64 K values each), 14..21 epilogue
+// (two warps per lane quarter, alternate 16-token column chunks).
+// Every mbarrier wait is bounded; on expiry the CTA records
+// MOE_ERR_DEVICE_TIMEOUT, drains what it has in flight and exits.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int WM = 128;               // weight rows per tile (MMA M, TMEM lanes)
+constexpr int kMaxN = kWtBlockRows;   // token rows per tile (MMA N <= 192)
+constexpr int WK = 64;                // one quantisation group per k-step
+constexpr int kBStages = 4;           // token operand / TMEM A ring
+constexpr int kCStages = 8;           // packed-code ring
+constexpr uint32_t kBBytes = kMaxN * WK * 2;  // 24 KB
+constexpr uint32_t kCBytes = WM * WK / 2;     // 4 KB of codes
+constexpr uint32_t kAccCols = kMaxN;          // fp32 columns of one accumulator
+constexpr uint32_t kAStageCols = WK / 2;      // 32 columns: 64 bf16 per lane
+constexpr uint32_t kAColBase = 2 * kAccCols;  // 384
+constexpr uint32_t kTmemCols = 512;
+static_assert(kAColBase + kBStages * kAStageCols <= kTmemCols, "tensor memory budget");
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpB0 = 2, kNumBWarps = 4, kWarpDq0 = 6, kNumDqWarps = 8,
+              kWarpEpi0 = 14, kNumEpiWarps = 8;
+constexpr int kNumWarps = 22;
+constexpr int kGatherLag = 3;  // cp.async groups in flight (< kBStages)
+static_assert(kGatherLag < kBStages, "the gather may not wait on a stage it has not released");
+constexpr int kGatherPerThread = kMaxN * 8 / (kNumBWarps * 32);  // 16-byte chunks per thread per k-step
+constexpr int kNumThreads = kNumWarps * 32;
+constexpr int kXposeStride = 36;  // floats per row of an epilogue transpose buffer (conflict-free float4 reads)
+
+constexpr uint32_t kOffB = 0;
+constexpr uint32_t kOffC = kOffB + kBStages * kBBytes;
+constexpr uint32_t kOffXpose = kOffC + kCStages * kCBytes;       // down epilogue: [warp][16][36] floats
+constexpr uint32_t kOffBar = kOffXpose + kNumEpiWarps * 16 * kXposeStride * 4;
+// bfull, afull, empty [kBStages]; cfull, cempty [kCStages]; accf, acce [2]; drain; never
+constexpr uint32_t kNumBars = 3 * kBStages + 2 * kCStages + 6;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr size_t kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart, descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+  return uint64_t((addr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
+         (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_n(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(WM >> 4) << 24);
+}
+
+// D (tensor memory) += A (tensor memory) * B (shared memory)^T.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Byte offset of 16-byte chunk c of row r inside a 1024-aligned SW128 K-major tile.
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return uint32_t((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// bf16 number gi (0..7) of a 16-byte vector, without indexing registers.
+__device__ __forceinline__ uint16_t pick_bf16(uint4 v, int gi) {
+  const uint32_t w = (gi & 4) ? ((gi & 2) ? v.w : v.z) : ((gi & 2) ? v.y : v.x);
+  return uint16_t((gi & 1) ? (w >> 16) : (w & 0xFFFFu));
+}
+
+struct WtArgs {
+  const uint16_t* x;
+  moe_qmatrix m0, m1;  // routed: gate, up (gate/up kernel) or down in m0
+  moe_qmatrix s0, s1;  // shared expert
+  const int32_t* blocks;
+  const int32_t* n_blocks;
+  const int32_t* perm;
+  const float* topk_w;
+  uint16_t* h;
+  float* y_acc;
+  WsHeader* hdr;
+  int T, D, E, k, I;
+  int max_blocks;
+  long long epi_wait_limit;  // > 0: test hook, the epilogue first waits this long on a barrier nothing arrives on
+};
+
+struct WtMaps {
+  CUtensorMap c0, c1;    // routed codes: gate, up (box 8 words x 64 rows) or down (box 8 x 128)
+  CUtensorMap cs0, cs1;  // shared-expert codes
+  CUtensorMap b;         // down only: h [T*k+T, I] (SW128, box 64 x kMaxN)
+};
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs args, const __grid_constant__ WtMaps maps) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bar0 = base + kOffBar;
+  auto bfull = [&](int s) { return bar0 + 8u * s; };
+  auto afull = [&](int s) { return bar0 + 8u * (kBStages + s); };
+  auto empty = [&](int s) { return bar0 + 8u * (2 * kBStages + s); };
+  auto cfull = [&](int s) { return bar0 + 8u * (3 * kBStages + s); };
+  auto cempty = [&](int s) { return bar0 + 8u * (3 * kBStages + kCStages + s); };
+  constexpr uint32_t kBarAcc = 3 * kBStages + 2 * kCStages;
+  auto accf = [&](int b) { return bar0 + 8u * (kBarAcc + b); };
+  auto acce = [&](int b) { return bar0 + 8u * (kBarAcc + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (kBarAcc + 4);
+  const uint32_t never_bar = bar0 + 8u * (kBarAcc + 5);  // test hook: nothing arrives here
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WtArgs& a = args;
+  const int NT = GATEUP ? a.I / 64 : a.D / WM;  // weight-row tiles per block-map entry
+  const int K = GATEUP ? a.D : a.I;
+  const int KS = K / WK;
+  const int A_rows = a.T * a.k;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(bfull(s), GATEUP ? kNumBWarps : 1);
+      mbar_init(afull(s), kNumDqWarps);
+      mbar_init(empty(s), 1);
+    }
+    for (int s = 0; s < kCStages; ++s) {
+      mbar_init(cfull(s), 1);
+      mbar_init(cempty(s), kNumDqWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf(b), 1);
+      mbar_init(acce(b), kNumEpiWarps);  // every epilogue warp drains its chunks
+    }
+    mbar_init(drain_bar, 1);
+    mbar_init(never_bar, 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == kWarpMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  int nb = *a.n_blocks;
+  if (nb > a.max_blocks || nb < 0) {
+    if (threadIdx.x == 0) report(a.hdr, MOE_ERR_DEVICE_CHECK, 20);
+    nb = 0;
+  }
+  const int n_tiles = nb * NT;
+
+  auto tile_info = [&](int tile, int& g, int& p0, int& R, int& j) {
+    const int b = tile / NT;
+    j = tile % NT;
+    g = a.blocks[3 * b];
+    p0 = a.blocks[3 * b + 1];
+    R = a.blocks[3 * b + 2];
+    if (g < 0 || g > a.E || R < 1 || R > kMaxN || p0 < 0 || p0 + R > A_rows + a.T) {
+      report(a.hdr, MOE_ERR_DEVICE_CHECK, 21);
+      return false;
+    }
+    return true;
+  };
+
+  if (warp == kWarpTma) {
+    // ---------------- TMA producer: codes (and h rows for down) ----------------
+    if (lane == 0) {
+      uint32_t it = 0, c_issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        int g, p0, R, j;
+        if (!tile_info(tile, g, p0, R, j)) {
+          *abort_flag = 1;
+          break;
+        }
+        const bool sh = (g == a.E);
+        const int ex = sh ? 0 : g;
+        for (int ks = 0; ks < KS; ++ks, ++it) {
+          const int cs = it % kCStages;
+          const uint32_t cph = (it / kCStages) & 1u;
+          if (!(ok = mbar_wait(cempty(cs), cph ^ 1u, abort_flag, a.hdr))) break;
+          const uint32_t cdst = base + kOffC + cs * kCBytes;
+          mbar_arrive_tx(cfull(cs), kCBytes);
+          if (GATEUP) {  // 64 gate rows, then the same 64 up rows
+            const int row = ex * a.I + j * 64;
+            tma_load_2d(cdst, sh ? &maps.cs0 : &maps.c0, ks * 8, row, cfull(cs));
+            tma_load_2d(cdst + kCBytes / 2, sh ? &maps.cs1 : &maps.c1, ks * 8, row, cfull(cs));
+          } else {
+            tma_load_2d(cdst, sh ? &maps.cs0 : &maps.c0, ks * 8, ex * a.D + j * WM, cfull(cs));
+          }
+          c_issued = it + 1;
+        }
+      }
+      // drain: every load this thread issued lands before the CTA exits
+      for (uint32_t s = 0; s < uint32_t(kCStages); ++s)
+        if (s < c_issued) {
+          const uint32_t last = c_issued - 1 - ((c_issued - 1 - s) % kCStages);
+          mbar_wait(cfull(s), (last / kCStages) & 1u, abort_flag, a.hdr, kWaitLimit, true);
+        }
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t it = 0, tc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
+        int g, p0, R, j;
+        if (!tile_info(tile, g, p0, R, j)) {
+          *abort_flag = 1;
+          break;
+        }
+        const uint32_t idesc = idesc_n((R + 15) & ~15);
+        const int buf = tc & 1;
+        if (!(ok = mbar_wait(acce(buf), ((tc >> 1) & 1u) ^ 1u, abort_flag, a.hdr))) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * kAccCols;
+        for (int ks = 0; ks < KS; ++ks, ++it) {
+          const int s = it % kBStages;
+          const uint32_t ph = (it / kBStages) & 1u;
+          if (!(ok = mbar_wait(bfull(s), ph, abort_flag, a.hdr))) break;
+          if (!(ok = mbar_wait(afull(s), ph, abort_flag, a.hdr))) break;
+          tc_fence_after();
+          const uint32_t at = tmem + kAColBase + s * kAStageCols, sb = base + kOffB + s * kBBytes;
+#pragma unroll
+          for (int kk = 0; kk < WK / 16; ++kk) umma_ts(d, at + kk * 8, smem_desc(sb + kk * 32), idesc, (ks | kk) != 0);
+          umma_commit(empty(s));
+        }
+        if (!ok) break;
+        umma_commit(accf(buf));
+      }
+      umma_commit(drain_bar);  // all MMAs complete before tensor memory is released
+      mbar_wait(drain_bar, 0, abort_flag, a.hdr, kWaitLimit, true);
+    }
+  } else if (warp >= kWarpB0 && warp < kWarpB0 + kNumBWarps) {
+    // ---------------- the token operand (B) ----------------
+    const int bt = threadIdx.x - kWarpB0 * 32;  // 0..127
+    if (GATEUP) {
+      // chunk m of this thread: row (bt + 128m) / 8, 16-byte chunk (bt + 128m) % 8
+      uint32_t it = 0, pending = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        int g, p0, R, j;
+        if (!tile_info(tile, g, p0, R, j)) {
+          *abort_flag = 1;
+          break;
+        }
+        const int n = (R + 15) & ~15;  // rows the MMA reads; R..n-1 repeat a valid row
+        const char* src[kGatherPerThread];
+#pragma unroll
+        for (int m = 0; m < kGatherPerThread; ++m) {
+          const int lin = bt + 128 * m, row = lin >> 3, ch = lin & 7;
+          const int rr = row < R ? row : 0;
+          int t = (g == a.E) ? (p0 + rr - A_rows) : (a.perm[p0 + rr] / a.k);
+          if (t < 0 || t >= a.T) {
+            report(a.hdr, MOE_ERR_DEVICE_CHECK, 22);
+            t = 0;
+          }
+          src[m] = reinterpret_cast<const char*>(a.x + size_t(t) * a.D) + ch * 16;
+        }
+        for (int ks = 0; ks < KS; ++ks, ++it) {
+          const int s = it % kBStages;
+          const uint32_t ph = (it / kBStages) & 1u;
+          if (!(ok = mbar_wait(empty(s), ph ^ 1u, abort_flag, a.hdr))) break;
+          const uint32_t dst = base + kOffB + s * kBBytes;
+#pragma unroll
+          for (int m = 0; m < kGatherPerThread; ++m) {
+            const int lin = bt + 128 * m, row = lin >> 3, ch = lin & 7;
+            if (row < n) cp_async16(dst + sw128(row, ch), src[m] + ks * 128, 16u);
+          }
+          cp_async_commit();
+          ++pending;
+          if (pending > kGatherLag) {
+            cp_async_wait<kGatherLag>();
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bfull((it - kGatherLag) % kBStages));
+            --pending;
+          }
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async();
+      __syncwarp();
+      if (ok && !*abort_flag)
+        for (uint32_t q = it - pending; q < it; ++q)
+          if (lane == 0) mbar_arrive(bfull(q % kBStages));
+    } else if (bt == 0) {
+      // down: rows p0.. of h as one 2-D TMA tile per k-step
+      uint32_t it = 0, issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        int g, p0, R, j;
+        if (!tile_info(tile, g, p0, R, j)) {
+          *abort_flag = 1;
+          break;
+        }
+        for (int ks = 0; ks < KS; ++ks, ++it) {
+          const int s = it % kBStages;
+          const uint32_t ph = (it / kBStages) & 1u;
+          if (!(ok = mbar_wait(empty(s), ph ^ 1u, abort_flag, a.hdr))) break;
+          mbar_arrive_tx(bfull(s), kBBytes);
+          tma_load_2d(base + kOffB + s * kBBytes, &maps.b, ks * WK, p0, bfull(s));
+          issued = it + 1;
+        }
+      }
+      for (uint32_t s = 0; s < uint32_t(kBStages); ++s)  // drain
+        if (s < issued) {
+          const uint32_t last = issued - 1 - ((issued - 1 - s) % kBStages);
+          mbar_wait(bfull(s), (last / kBStages) & 1u, abort_flag, a.hdr, kWaitLimit, true);
+        }
+    }
+  } else if (warp >= kWarpDq0 && warp < kWarpDq0 + kNumDqWarps) {
+    // ---------------- dequantisation into the tensor-memory A stage ----------------
+    const int q = warp & 3;                   // TMEM lane quarter of this warp
+    const int hk = (warp - kWarpDq0) >> 2;    // which 32 of the 64 K values
+    const int L = q * 32 + lane;              // TMEM lane = weight row of the tile
+    const int srow_stage = GATEUP ? ((L & 1) ? 64 + (L >> 1) : (L >> 1)) : L;  // row in the code stage
+    const bool vec_sb = (K / 64) % 8 == 0;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      int g, p0, R, j;
+      if (!tile_info(tile, g, p0, R, j)) {
+        *abort_flag = 1;
+        break;
+      }
+      const bool sh = (g == a.E);
+      const int ex = sh ? 0 : g;
+      const moe_qmatrix& m = GATEUP ? ((L & 1) ? (sh ? a.s1 : a.m1) : (sh ? a.s0 : a.m0)) : (sh ? a.s0 : a.m0);
+      const size_t row = GATEUP ? size_t(ex) * a.I + j * 64 + (L >> 1) : size_t(ex) * a.D + j * WM + L;
+      const uint16_t* srow = m.scales + row * (K / 64);
+      const uint16_t* brow = m.biases + row * (K / 64);
+      uint4 s_cur = make_uint4(0u, 0u, 0u, 0u), b_cur = s_cur, s_nxt = s_cur, b_nxt = s_cur;
+      uint16_t s_one = 0, b_one = 0;
+      if (vec_sb) {
+        s_cur = *reinterpret_cast<const uint4*>(srow);
+        b_cur = *reinterpret_cast<const uint4*>(brow);
+        if (KS > 8) {
+          s_nxt = *reinterpret_cast<const uint4*>(srow + 8);
+          b_nxt = *reinterpret_cast<const uint4*>(brow + 8);
+        }
+      } else {
+        s_one = srow[0];
+        b_one = brow[0];
+      }
+      for (int ks = 0; ks < KS; ++ks, ++it) {
+        const int s = it % kBStages, cs = it % kCStages;
+        const uint32_t ph = (it / kBStages) & 1u, cph = (it / kCStages) & 1u;
+        uint16_t sc, bi;
+        if (vec_sb) {
+          const int gi = ks & 7;
+          sc = pick_bf16(s_cur, gi);
+          bi = pick_bf16(b_cur, gi);
+          if (gi == 7) {
+            s_cur = s_nxt;
+            b_cur = b_nxt;
+            if (ks + 9 < KS) {
+              s_nxt = *reinterpret_cast<const uint4*>(srow + ks + 9);
+              b_nxt = *reinterpret_cast<const uint4*>(brow + ks + 9);
+            }
+          }
+        } else {
+          sc = s_one;
+          bi = b_one;
+          if (ks + 1 < KS) {
+            s_one = srow[ks + 1];
+            b_one = brow[ks + 1];
+          }
+        }
+        if (!(ok = mbar_wait(cfull(cs), cph, abort_flag, a.hdr))) break;
+        const uint4 w4 = *reinterpret_cast<const uint4*>(gbase + kOffC + cs * kCBytes + srow_stage * 32 + hk * 16);
+        const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16(sc), __ushort_as_bfloat16(sc));
+        const __nv_bfloat162 b2 = __halves2bfloat162(__ushort_as_bfloat16(bi), __ushort_as_bfloat16(bi));
+        uint32_t o0[4], o1[4], o2[4], o3[4];
+        dq8_bf16(w4.x, s2, b2, o0);
+        dq8_bf16(w4.y, s2, b2, o1);
+        dq8_bf16(w4.z, s2, b2, o2);
+        dq8_bf16(w4.w, s2, b2, o3);
+        const uint32_t o[16] = {o0[0], o0[1], o0[2], o0[3], o1[0], o1[1], o1[2], o1[3],
+                                o2[0], o2[1], o2[2], o2[3], o3[0], o3[1], o3[2], o3[3]};
+        // the code stage goes back to the TMA only after the reads above have
+        // returned (the dequantised values depend on them)
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cempty(cs));
+        if (!(ok = mbar_wait(empty(s), ph ^ 1u, abort_flag, a.hdr))) break;
+        tmem_st16(tmem + (uint32_t(q * 32) << 16) + kAColBase + s * kAStageCols + hk * 16, o);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(afull(s));
+      }
+    }
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kNumEpiWarps) {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;
+    const int L = q * 32 + lane;                    // TMEM lane: weight row of the tile
+    const int half = (warp - kWarpEpi0) >> 2;       // this warp takes 16-column chunks half, half+2, ...
+    float* xb = reinterpret_cast<float*>(gbase + kOffXpose) + (warp - kWarpEpi0) * 16 * kXposeStride;
+    uint32_t tc = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
+      int g, p0, R, j;
+      if (!tile_info(tile, g, p0, R, j)) {
+        *abort_flag = 1;
+        break;
+      }
+      const int buf = tc & 1;
+      if (a.epi_wait_limit > 0 && !(ok = mbar_wait(never_bar, 0, abort_flag, a.hdr, a.epi_wait_limit))) break;
+      if (!(ok = mbar_wait(accf(buf), (tc >> 1) & 1u, abort_flag, a.hdr))) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + buf * kAccCols;
+      const bool sh = (g == a.E);
+      for (int n0 = half * 16; n0 < R; n0 += 32) {
+        uint32_t v[16];
+        tmem_ld16(tbase + n0, v);
+        tmem_wait_ld();
+        if (GATEUP) {
+          // lane 2i holds gate row i, lane 2i+1 up row i; lanes 4m keep rows 2m, 2m+1
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float mine = __uint_as_float(v[c]);
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+            const float hv = silu_mul(mine, other);  // meaningful on even lanes
+            const float hn = __shfl_down_sync(0xffffffffu, hv, 2);
+            const int nn = n0 + c;
+            if ((lane & 3) == 0 && nn < R) {
+              const uint32_t pk = uint32_t(f32_to_bf16(hv)) | (uint32_t(f32_to_bf16(hn)) << 16);
+              *reinterpret_cast<uint32_t*>(a.h + size_t(p0 + nn) * a.I + j * 64 + (L >> 1)) = pk;
+            }
+          }
+        } else {
+          // transpose the warp's 32 columns x 16 tokens so that each lane adds
+          // four consecutive output columns of one token (16-byte reductions)
+#pragma unroll
+          for (int c = 0; c < 16; ++c) xb[c * kXposeStride + lane] = __uint_as_float(v[c]);
+          __syncwarp();
+          const int c = lane >> 1, nn = n0 + c;
+          if (nn < R) {
+            const int p = p0 + nn;
+            int t;
+            float w;
+            if (sh) {
+              t = p - A_rows;
+              w = 1.f;
+            } else {
+              const int asg = a.perm[p];
+              t = asg / a.k;
+              w = a.topk_w[asg];
+            }
+            float* dst = a.y_acc + size_t(t) * a.D + j * WM + q * 32;
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {
+              const int quad = (lane & 1) * 4 + kq;
+              const float4 val = *reinterpret_cast<const float4*>(xb + c * kXposeStride + quad * 4);
+              red_add_v4(dst + quad * 4, w * val.x, w * val.y, w * val.z, w * val.w);
+            }
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce(buf));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+}  // namespace
+
+bool gemm_wt_supported(const Ctx& c) { return c.I % 64 == 0 && c.D % WM == 0 && tmap_encoder_available(); }
+
+cudaError_t gemm_wt(const Ctx& c) {
+  const moe_weights* w = c.w;
+  if (c.BM != kWtBlockRows) return cudaErrorInvalidValue;
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(gemm_wt_kernel<true>), int(kSmemBytes)) ||
+      !ensure_smem_limit(reinterpret_cast<const void*>(gemm_wt_kernel<false>), int(kSmemBytes)))
+    return cudaErrorInvalidValue;
+  const int A = c.T * c.k;
+  WtArgs a{c.x,      w->gate, w->up,   w->s_gate, w->s_up, c.blocks, c.n_blocks, c.perm, c.topk_w,
+           c.h,      c.y_acc, c.hdr,   c.T,       c.D,     c.E,      c.k,        c.I,    c.max_blocks,
+           tc_epilogue_wait_limit()};
+  WtMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  const auto U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
+  const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
+  bool ok = make_tmap_2d(&maps.c0, U32, 4, w->gate.codes, uint64_t(c.E) * c.I, c.D / 8, 8, 64, NOSW) &&
+            make_tmap_2d(&maps.c1, U32, 4, w->up.codes, uint64_t(c.E) * c.I, c.D / 8, 8, 64, NOSW) &&
+            make_tmap_2d(&maps.cs0, U32, 4, w->s_gate.codes, c.I, c.D / 8, 8, 64, NOSW) &&
+            make_tmap_2d(&maps.cs1, U32, 4, w->s_up.codes, c.I, c.D / 8, 8, 64, NOSW);
+  if (!ok) return cudaErrorInvalidValue;
+  cudaError_t err = zero_yacc(c);
+  if (err != cudaSuccess) return err;
+  const int grid1 = std::max(1, std::min(num_sms(), c.max_blocks * (c.I / 64)));
+  gemm_wt_kernel<true><<<grid1, kNumThreads, kSmemBytes, c.stream>>>(a, maps);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  launch_done("gateup_tc", c.stream);
+
+  a.m0 = w->down;
+  a.s0 = w->s_down;
+  std::memset(&maps, 0, sizeof(maps));
+  ok = make_tmap_2d(&maps.c0, U32, 4, w->down.codes, uint64_t(c.E) * c.D, c.I / 8, 8, WM, NOSW) &&
+       make_tmap_2d(&maps.cs0, U32, 4, w->s_down.codes, c.D, c.I / 8, 8, WM, NOSW) &&
+       make_tmap_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.h, uint64_t(A + c.T), c.I, WK, kMaxN,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+  const int grid2 = std::max(1, std::min(num_sms(), c.max_blocks * (c.D / WM)));
+  gemm_wt_kernel<false><<<grid2, kNumThreads, kSmemBytes, c.stream>>>(a, maps);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  launch_done("down_tc", c.stream);
+  return cast_y(c);
+}
+
+}  // namespace moe

@@ -108,7 +108,6 @@ __device__ __forceinline__ void chunk_sums(const float4* xs4, float* xsum, int r
   }
 }
 
-__device__ __forceinline__ size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
 // Shared-memory layout of a gate/up CTA (D input columns, R token rows).
 struct GateupSmem {

@@ -1,6 +1,7 @@
 // Internal interface between the translation units of the MoE library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -14,8 +15,9 @@ struct WsHeader;
 // Chunk of tokens handled by one CTA of the top-k/histogram and scatter steps.
 constexpr int kChunkTokens = 64;
 
-// Rows per block-map entry consumed by the tensor-core GEMM.
-constexpr int kTcBlockRows = 128;
+// Rows per block-map entry consumed by the tensor-core GEMMs.
+constexpr int kTcBlockRows = 128;  // weights dequantised into shared memory (MMA M = tokens)
+constexpr int kWtBlockRows = 192;  // weights dequantised into tensor memory (MMA N = tokens)
 
 // One call's resolved sizes and device pointers.
 struct Ctx {
@@ -60,6 +62,16 @@ cudaError_t gemm_simt(const Ctx& c);
 cudaError_t gemm_tc(const Ctx& c);
 bool gemm_tc_supported(const Ctx& c);
 void set_tc_epilogue_wait_limit(long long cycles);  // <= 0: the normal limit
+long long tc_epilogue_wait_limit();
+cudaError_t gemm_wt(const Ctx& c);
+bool gemm_wt_supported(const Ctx& c);
+int num_sms();
+
+// 2-D TMA tensor map over a row-major [rows, cols] array (false if the
+// driver's encoder is unavailable or rejects the map).
+bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t elem, const void* ptr, uint64_t rows,
+                  uint64_t cols, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
+bool tmap_encoder_available();
 
 // Decode GEMV path (a few rows).
 cudaError_t gemv(const Ctx& c);

@@ -167,21 +167,24 @@ void fill_view(const Ctx& c, moe_route_view* v) {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-enum class Path { Gemv, GemmTc, GemmSimt };
+enum class Path { Gemv, GemmWt, GemmTc, GemmSimt };
 
 // Chooses the expert path for this call and the block-map row count it
-// consumes (the tensor-core GEMM takes 256-row blocks, the others 128).
+// consumes: 192 tokens per block for the tensor-core GEMM with weights in
+// tensor memory, 128 for the others.
 Path plan(Ctx& c) {
   int path = g_opt.force_path;
   if (path == 0) path = (c.T <= g_opt.gemv_max_rows) ? 1 : 2;
   Path p;
   if (path == 1 && gemv_supported(c))
     p = Path::Gemv;
-  else if (g_opt.gemm_impl == 0 && gemm_tc_supported(c))
+  else if (g_opt.gemm_impl == 0 && gemm_wt_supported(c))
+    p = Path::GemmWt;
+  else if (g_opt.gemm_impl == 2 && gemm_tc_supported(c))
     p = Path::GemmTc;
   else
     p = Path::GemmSimt;
-  c.BM = (p == Path::GemmTc) ? kTcBlockRows : kDefaultBlockM;
+  c.BM = (p == Path::GemmWt) ? kWtBlockRows : (p == Path::GemmTc) ? kTcBlockRows : kDefaultBlockM;
   return p;
 }
 
@@ -265,6 +268,7 @@ moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uin
   cudaError_t err = route(c);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (path == Path::Gemv) return cuda_status(gemv(c));
+  if (path == Path::GemmWt) return cuda_status(gemm_wt(c));
   if (path == Path::GemmTc) return cuda_status(gemm_tc(c));
   return cuda_status(gemm_simt(c));
 }
@@ -317,7 +321,7 @@ moe_status moe_set_option(int option, int value) {
       g_opt.kernel_timing = value;
       return MOE_OK;
     case MOE_OPT_GEMM_IMPL:
-      if (value < 0 || value > 1) return MOE_ERR_ARG;
+      if (value < 0 || value > 2) return MOE_ERR_ARG;
       g_opt.gemm_impl = value;
       return MOE_OK;
     case MOE_OPT_TEST_WAIT_CYCLES:

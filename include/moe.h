@@ -92,8 +92,8 @@ typedef struct {
  *   inv       int32 [T*k]      inv[perm[p]] = p
  *   blocks    int32 [max_blocks][3] = (group, first row, rows): for each
  *             expert in ascending order its segment cut into blocks of
- *             block_m rows (256 when the call takes the tensor-core GEMM
- *             path, 128 otherwise), then the shared expert as group E over rows
+ *             block_m rows (192 on the default tensor-core GEMM path, 128
+ *             otherwise), then the shared expert as group E over rows
  *             T*k .. T*k+T-1 (token t at row T*k+t)
  *   n_blocks  int32 [1]        number of valid entries of blocks
  *   h         bf16 [T*k + T, I]  SwiGLU intermediate in the permuted order
@@ -120,8 +120,12 @@ typedef enum {
   MOE_OPT_FORCE_PATH = 2,    /* 0 auto by row count, 1 GEMV, 2 grouped GEMM */
   MOE_OPT_KERNEL_TIMING = 3, /* 1: record CUDA events around each kernel of
                                 the next forwards (read with moe_kernel_times) */
-  MOE_OPT_GEMM_IMPL = 4,     /* 0 tensor-core (tcgen05) grouped GEMM, 1 CUDA-core
-                                grouped GEMM (the comparison baseline) */
+  MOE_OPT_GEMM_IMPL = 4,     /* grouped GEMM used above the GEMV threshold:
+                                0 tensor cores (tcgen05) with the dequantised weights
+                                  in tensor memory (default),
+                                1 CUDA cores (the comparison baseline),
+                                2 tensor cores with the dequantised weights in
+                                  shared memory */
   MOE_OPT_TEST_WAIT_CYCLES = 5 /* test hook: > 0 makes the tensor-core epilogue
                                 first wait, for at most this many cycles, on a
                                 barrier that nothing arrives on, so the
