@@ -57,8 +57,6 @@ static_assert(kAColBase + kBStages * kAStageCols <= kTmemCols, "tensor memory bu
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpB0 = 2, kNumBWarps = 4, kWarpDq0 = 6, kNumDqWarps = 8,
               kWarpEpi0 = 14, kNumEpiWarps = 8;
 constexpr int kNumWarps = 22;
-constexpr int kGatherLag = 3;  // cp.async groups in flight (< kBStages)
-static_assert(kGatherLag < kBStages, "the gather may not wait on a stage it has not released");
 constexpr int kGatherPerThread = kMaxN * 8 / (kNumBWarps * 32);  // 16-byte chunks per thread per k-step
 constexpr int kNumThreads = kNumWarps * 32;
 constexpr int kXposeStride = 36;  // floats per row of an epilogue transpose buffer (conflict-free float4 reads)
@@ -82,10 +80,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Arrives on `bar` once every cp.async this thread has issued so far has
+// landed; the barrier's expected count includes this arrival.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kBStages; ++s) {
-      mbar_init(bfull(s), GATEUP ? kNumBWarps : 1);
+      mbar_init(bfull(s), GATEUP ? kNumBWarps * 32 : 1);
       mbar_init(afull(s), kNumDqWarps);
       mbar_init(empty(s), 1);
     }
@@ -309,6 +311,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
           if (!(ok = mbar_wait(bfull(s), ph, abort_flag, a.hdr))) break;
           if (!(ok = mbar_wait(afull(s), ph, abort_flag, a.hdr))) break;
           tc_fence_after();
+          // the gathered tokens were written by cp.async (generic proxy): order them
+          // before the tensor cores' (async proxy) reads
+          if (GATEUP) fence_proxy_async();
           const uint32_t at = tmem + kAColBase + s * kAStageCols, sb = base + kOffB + s * kBBytes;
 #pragma unroll
           for (int kk = 0; kk < WK / 16; ++kk) umma_ts(d, at + kk * 8, smem_desc(sb + kk * 32), idesc, (ks | kk) != 0);
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
     const int bt = threadIdx.x - kWarpB0 * 32;  // 0..127
     if (GATEUP) {
       // chunk m of this thread: row (bt + 128m) / 8, 16-byte chunk (bt + 128m) % 8
-      uint32_t it = 0, pending = 0;
+      uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         int g, p0, R, j;
@@ -356,23 +361,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
             const int lin = bt + 128 * m, row = lin >> 3, ch = lin & 7;
             if (row < n) cp_async16(dst + sw128(row, ch), src[m] + ks * 128, 16u);
           }
-          cp_async_commit();
-          ++pending;
-          if (pending > kGatherLag) {
-            cp_async_wait<kGatherLag>();
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bfull((it - kGatherLag) % kBStages));
-            --pending;
-          }
+          cp_async_arrive_noinc(bfull(s));
         }
       }
       cp_async_wait<0>();
-      fence_proxy_async();
-      __syncwarp();
-      if (ok && !*abort_flag)
-        for (uint32_t q = it - pending; q < it; ++q)
-          if (lane == 0) mbar_arrive(bfull(q % kBStages));
     } else if (bt == 0) {
       // down: rows p0.. of h as one 2-D TMA tile per k-step
       uint32_t it = 0, issued = 0;
