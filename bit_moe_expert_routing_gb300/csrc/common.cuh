@@ -31,7 +31,10 @@ __device__ __forceinline__ void report(WsHeader* hdr, int status, int detail) {
   if (atomicCAS(&hdr->status, 0, status) == 0) hdr->detail = detail;
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+// SiLU(g) * u with the hardware exponential and approximate division: a few
+// ulp of fp32, far below the bf16 rounding of the result. For g below about
+// -88 the denominator is +inf and the quotient the limit 0.
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 // Low-half and high-half bf16 of a packed pair, as fp32.
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }

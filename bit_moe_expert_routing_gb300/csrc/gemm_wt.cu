@@ -497,16 +497,24 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
         tmem_ld16(tbase + n0, v);
         tmem_wait_ld();
         if (GATEUP) {
-          // lane 2i holds gate row i, lane 2i+1 up row i; lanes 4m keep rows 2m, 2m+1
+          // lane 2i holds gate row i, lane 2i+1 up row i, for tokens n0..n0+15.
+          // The pair swaps halves so that the even lane finishes the even
+          // tokens and the odd lane the odd ones: each value computed once.
+          const bool odd = lane & 1;
+          float hv[8];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float mine = __uint_as_float(v[c]);
-            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-            const float hv = silu_mul(mine, other);  // meaningful on even lanes
-            const float hn = __shfl_down_sync(0xffffffffu, hv, 2);
-            const int nn = n0 + c;
-            if ((lane & 3) == 0 && nn < R) {
-              const uint32_t pk = uint32_t(f32_to_bf16(hv)) | (uint32_t(f32_to_bf16(hn)) << 16);
+          for (int m = 0; m < 8; ++m) {
+            const float keep = __uint_as_float(odd ? v[2 * m + 1] : v[2 * m]);
+            const float recv = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? v[2 * m] : v[2 * m + 1]), 1);
+            hv[m] = odd ? silu_mul(recv, keep) : silu_mul(keep, recv);
+          }
+          // lanes 4m and 4m+1 pack rows 2m, 2m+1 of their token parity
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            const float hn = __shfl_down_sync(0xffffffffu, hv[m], 2);
+            const int nn = n0 + 2 * m + (odd ? 1 : 0);
+            if ((lane & 2) == 0 && nn < R) {
+              const uint32_t pk = uint32_t(f32_to_bf16(hv[m])) | (uint32_t(f32_to_bf16(hn)) << 16);
               *reinterpret_cast<uint32_t*>(a.h + size_t(p0 + nn) * a.I + j * 64 + (L >> 1)) = pk;
             }
           }
