@@ -16,7 +16,9 @@
 //       cp.async (gate/up) or loaded by TMA from h (down);
 //   D = fp32 in tensor memory, two 192-column buffers so the epilogue of one
 //       tile overlaps the next tile's MMAs.
-// Tensor memory (512 columns): accumulators 0..383, A stages 384..511.
+// Tensor memory (512 columns): accumulators 0..383, two A stages 384..511.
+// A pipeline stage spans 128 of K (two quantisation groups), so the MMA warp
+// issues eight MMAs per pair of barrier waits.
 //
 // gate/up tiles take 64 intermediate rows with the gate and up rows
 // interleaved (lane 2i = gate row i, lane 2i+1 = up row i), so the epilogue
@@ -25,8 +27,8 @@
 // Warp roles (22 warps): 0 TMA for the packed codes, 1 TMEM allocator and MMA
 // issuer, 2..5 the token operand (gate/up: cp.async gather of x rows, eight
 // consecutive lanes per 128-byte row so every warp instruction covers four
-// whole cache lines; down: a 2-D TMA tile of h), 6..13 dequantisation (two
-// warps per TMEM lane quarter, 32 of the 64 K values each), 14..21 epilogue
+// whole cache lines; down: 2-D TMA tiles of h), 6..13 dequantisation (two
+// warps per TMEM lane quarter, one for each group of a stage), 14..21 epilogue
 // (two warps per lane quarter, alternate 16-token column chunks).
 // Every mbarrier wait is bounded; on expiry the CTA records
 // MOE_ERR_DEVICE_TIMEOUT, drains what it has in flight and exits.
@@ -44,20 +46,24 @@ namespace {
 
 constexpr int WM = 128;               // weight rows per tile (MMA M, TMEM lanes)
 constexpr int kMaxN = kWtBlockRows;   // token rows per tile (MMA N <= 192)
-constexpr int WK = 64;                // one quantisation group per k-step
-constexpr int kBStages = 4;           // token operand / TMEM A ring
-constexpr int kCStages = 8;           // packed-code ring
-constexpr uint32_t kBBytes = kMaxN * WK * 2;  // 24 KB
-constexpr uint32_t kCBytes = WM * WK / 2;     // 4 KB of codes
-constexpr uint32_t kAccCols = kMaxN;          // fp32 columns of one accumulator
-constexpr uint32_t kAStageCols = WK / 2;      // 32 columns: 64 bf16 per lane
+constexpr int WK = 64;                // one quantisation group
+constexpr int kGroupsPerStage = 2;    // a pipeline stage spans 128 of K
+constexpr int kBStages = 3;           // token operand ring (shared memory)
+constexpr int kAStages = 2;           // dequantised weight ring (tensor memory)
+constexpr int kCStages = 8;           // packed-code ring, one group per stage
+constexpr uint32_t kBHalf = kMaxN * WK * 2;             // 24 KB: one 128-byte-swizzled K block of 64
+constexpr uint32_t kBBytes = kBHalf * kGroupsPerStage;  // 48 KB
+constexpr uint32_t kCBytes = WM * WK / 2;               // 4 KB of codes
+constexpr uint32_t kAccCols = kMaxN;                    // fp32 columns of one accumulator
+constexpr uint32_t kAGroupCols = WK / 2;                // 32 columns: one group's 64 bf16 per lane
+constexpr uint32_t kAStageCols = kAGroupCols * kGroupsPerStage;
 constexpr uint32_t kAColBase = 2 * kAccCols;  // 384
 constexpr uint32_t kTmemCols = 512;
-static_assert(kAColBase + kBStages * kAStageCols <= kTmemCols, "tensor memory budget");
+static_assert(kAColBase + kAStages * kAStageCols <= kTmemCols, "tensor memory budget");
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpB0 = 2, kNumBWarps = 4, kWarpDq0 = 6, kNumDqWarps = 8,
               kWarpEpi0 = 14, kNumEpiWarps = 8;
 constexpr int kNumWarps = 22;
-constexpr int kGatherPerThread = kMaxN * 8 / (kNumBWarps * 32);  // 16-byte chunks per thread per k-step
+constexpr int kGatherPerThread = kMaxN * 8 / (kNumBWarps * 32);  // 16-byte chunks per thread per K block
 constexpr int kNumThreads = kNumWarps * 32;
 constexpr int kXposeStride = 36;  // floats per row of an epilogue transpose buffer (conflict-free float4 reads)
 
@@ -65,10 +71,11 @@ constexpr uint32_t kOffB = 0;
 constexpr uint32_t kOffC = kOffB + kBStages * kBBytes;
 constexpr uint32_t kOffXpose = kOffC + kCStages * kCBytes;       // down epilogue: [warp][16][36] floats
 constexpr uint32_t kOffBar = kOffXpose + kNumEpiWarps * 16 * kXposeStride * 4;
-// bfull, afull, empty [kBStages]; cfull, cempty [kCStages]; accf, acce [2]; drain; never
-constexpr uint32_t kNumBars = 3 * kBStages + 2 * kCStages + 6;
+// bfull, bempty [kBStages]; afull, aempty [kAStages]; cfull, cempty [kCStages]; accf, acce [2]; drain; never
+constexpr uint32_t kNumBars = 2 * kBStages + 2 * kAStages + 2 * kCStages + 6;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr size_t kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
   asm volatile(
@@ -94,38 +101,68 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart, descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
-  return uint64_t((addr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
-         (uint64_t(1) << 46) | (uint64_t(2) << 61);
-}
+// 1024 bytes apart, descriptor version 1. Split in two 32-bit halves: the low
+// half holds the start address (bits 0-13, in 16-byte units) and the leading
+// byte offset; the high half the stride byte offset, the version bit and the
+// swizzle mode, and is the same for every tile.
+__device__ __forceinline__ uint32_t smem_desc_lo(uint32_t addr) { return ((addr & 0x3FFFFu) >> 4) | (1u << 16); }
+constexpr uint32_t kSmemDescHi = (1024u >> 4) | (1u << (46 - 32)) | (2u << (61 - 32));
 
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 D, K-major, M = 128, N = n.
 __device__ __forceinline__ uint32_t idesc_n(int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(WM >> 4) << 24);
 }
 
-// D (tensor memory) += A (tensor memory) * B (shared memory)^T.
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t accumulate) {
+// One stage of 128 of K: eight K = 16 MMAs D (tensor memory) += A (tensor
+// memory, columns a .. a+63) * B (shared memory: two 128-byte-swizzled K
+// blocks of 64, the first with descriptor low half b_lo, the second kBHalf
+// bytes further)^T, then commits that arrive on `bar_b` and `bar_a` (the two
+// operand stages' release barriers) when they complete. The first MMA
+// overwrites D when `accumulate` is 0. Executed by the whole warp so that every
+// operand is warp-uniform; one elected lane issues.
+__device__ __forceinline__ void umma_stage(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t idesc, uint32_t accumulate,
+                                           uint32_t bar_b, uint32_t bar_a) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
-          d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n"
+      " .reg .pred e, p, t;\n"
+      " .reg .b32 a1, a2, a3, a4, a5, a6, a7, l1, l2, l3, l4, l5, l6, l7;\n"
+      " .reg .b64 b0, b1, b2, b3, b4, b5, b6, b7;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " add.u32 a1, %1, 8;\n add.u32 a2, %1, 16;\n add.u32 a3, %1, 24;\n"
+      " add.u32 a4, %1, 32;\n add.u32 a5, %1, 40;\n add.u32 a6, %1, 48;\n add.u32 a7, %1, 56;\n"
+      " add.u32 l1, %2, 2;\n add.u32 l2, %2, 4;\n add.u32 l3, %2, 6;\n"
+      " add.u32 l4, %2, %8;\n add.u32 l5, l4, 2;\n add.u32 l6, l4, 4;\n add.u32 l7, l4, 6;\n"
+      " mov.b64 b0, {%2, %3};\n mov.b64 b1, {l1, %3};\n mov.b64 b2, {l2, %3};\n mov.b64 b3, {l3, %3};\n"
+      " mov.b64 b4, {l4, %3};\n mov.b64 b5, {l5, %3};\n mov.b64 b6, {l6, %3};\n mov.b64 b7, {l7, %3};\n"
+      " setp.ne.b32 p, %5, 0;\n"
+      " setp.eq.b32 t, %5, %5;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b0, %4, p;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %4, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %4, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %4, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %4, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %4, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %4, t;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n"
+      "}" ::"r"(d),
+      "r"(a), "r"(b_lo), "r"(kSmemDescHi), "r"(idesc), "r"(accumulate), "r"(bar_b), "r"(bar_a), "r"(kBHalf >> 4)
       : "memory");
 }
 
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+// Commit by one elected lane of a converged warp: `bar` receives one arrival
+// when every MMA this thread issued before has completed.
+__device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
+      : "memory");
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+               : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -184,11 +221,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bar0 = base + kOffBar;
   auto bfull = [&](int s) { return bar0 + 8u * s; };
-  auto afull = [&](int s) { return bar0 + 8u * (kBStages + s); };
-  auto empty = [&](int s) { return bar0 + 8u * (2 * kBStages + s); };
-  auto cfull = [&](int s) { return bar0 + 8u * (3 * kBStages + s); };
-  auto cempty = [&](int s) { return bar0 + 8u * (3 * kBStages + kCStages + s); };
-  constexpr uint32_t kBarAcc = 3 * kBStages + 2 * kCStages;
+  auto bempty = [&](int s) { return bar0 + 8u * (kBStages + s); };
+  auto afull = [&](int s) { return bar0 + 8u * (2 * kBStages + s); };
+  auto aempty = [&](int s) { return bar0 + 8u * (2 * kBStages + kAStages + s); };
+  auto cfull = [&](int s) { return bar0 + 8u * (2 * kBStages + 2 * kAStages + s); };
+  auto cempty = [&](int s) { return bar0 + 8u * (2 * kBStages + 2 * kAStages + kCStages + s); };
+  constexpr uint32_t kBarAcc = 2 * kBStages + 2 * kAStages + 2 * kCStages;
   auto accf = [&](int b) { return bar0 + 8u * (kBarAcc + b); };
   auto acce = [&](int b) { return bar0 + 8u * (kBarAcc + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (kBarAcc + 4);
@@ -200,18 +238,22 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
   const WtArgs& a = args;
   const int NT = GATEUP ? a.I / 64 : a.D / WM;  // weight-row tiles per block-map entry
   const int K = GATEUP ? a.D : a.I;
-  const int KS = K / WK;
+  const int KS = K / WK;                   // quantisation groups per tile
+  const int KT = KS / kGroupsPerStage;     // pipeline stages per tile
   const int A_rows = a.T * a.k;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kBStages; ++s) {
       mbar_init(bfull(s), GATEUP ? kNumBWarps * 32 : 1);
-      mbar_init(afull(s), kNumDqWarps);
-      mbar_init(empty(s), 1);
+      mbar_init(bempty(s), 1);
+    }
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(afull(s), kNumDqWarps);  // both groups of the stage, four warps each
+      mbar_init(aempty(s), 1);
     }
     for (int s = 0; s < kCStages; ++s) {
       mbar_init(cfull(s), 1);
-      mbar_init(cempty(s), kNumDqWarps);
+      mbar_init(cempty(s), kNumDqWarps / 2);  // the four warps of one group parity
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf(b), 1);
@@ -290,41 +332,41 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
         }
     }
   } else if (warp == kWarpMma) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      uint32_t it = 0, tc = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
-        int g, p0, R, j;
-        if (!tile_info(tile, g, p0, R, j)) {
-          *abort_flag = 1;
-          break;
-        }
-        const uint32_t idesc = idesc_n((R + 15) & ~15);
-        const int buf = tc & 1;
-        if (!(ok = mbar_wait(acce(buf), ((tc >> 1) & 1u) ^ 1u, abort_flag, a.hdr))) break;
-        tc_fence_after();
-        const uint32_t d = tmem + buf * kAccCols;
-        for (int ks = 0; ks < KS; ++ks, ++it) {
-          const int s = it % kBStages;
-          const uint32_t ph = (it / kBStages) & 1u;
-          if (!(ok = mbar_wait(bfull(s), ph, abort_flag, a.hdr))) break;
-          if (!(ok = mbar_wait(afull(s), ph, abort_flag, a.hdr))) break;
-          tc_fence_after();
-          // the gathered tokens were written by cp.async (generic proxy): order them
-          // before the tensor cores' (async proxy) reads
-          if (GATEUP) fence_proxy_async();
-          const uint32_t at = tmem + kAColBase + s * kAStageCols, sb = base + kOffB + s * kBBytes;
-#pragma unroll
-          for (int kk = 0; kk < WK / 16; ++kk) umma_ts(d, at + kk * 8, smem_desc(sb + kk * 32), idesc, (ks | kk) != 0);
-          umma_commit(empty(s));
-        }
-        if (!ok) break;
-        umma_commit(accf(buf));
+    // ---------------- MMA issuer: the whole warp runs the loop, one lane issues ----------------
+    // lane 0's wait result decides for the warp, so every branch stays uniform
+    auto warp_wait = [&](uint32_t bar, uint32_t parity, bool draining) {
+      const bool r = mbar_wait(bar, parity, abort_flag, a.hdr, kWaitLimit, draining);
+      return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+    };
+    uint32_t it = 0, tc = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
+      int g, p0, R, j;
+      if (!tile_info(tile, g, p0, R, j)) {
+        *abort_flag = 1;
+        break;
       }
-      umma_commit(drain_bar);  // all MMAs complete before tensor memory is released
-      mbar_wait(drain_bar, 0, abort_flag, a.hdr, kWaitLimit, true);
+      const uint32_t idesc = idesc_n((R + 15) & ~15);
+      const int buf = tc & 1;
+      if (!(ok = warp_wait(acce(buf), ((tc >> 1) & 1u) ^ 1u, false))) break;
+      tc_fence_after();
+      const uint32_t d = tmem + buf * kAccCols;
+      for (int t = 0; t < KT; ++t, ++it) {
+        const int s = it % kBStages, sa = it % kAStages;
+        if (!(ok = warp_wait(bfull(s), (it / kBStages) & 1u, false))) break;
+        if (!(ok = warp_wait(afull(sa), (it / kAStages) & 1u, false))) break;
+        tc_fence_after();
+        // the gathered tokens were written by cp.async (generic proxy): order them
+        // before the tensor cores' (async proxy) reads
+        if (GATEUP) fence_proxy_async();
+        umma_stage(d, tmem + kAColBase + sa * kAStageCols, smem_desc_lo(base + kOffB + s * kBBytes), idesc,
+                   t != 0 ? 1u : 0u, bempty(s), aempty(sa));
+      }
+      if (!ok) break;
+      umma_commit_warp(accf(buf));
     }
+    umma_commit_warp(drain_bar);  // all MMAs complete before tensor memory is released
+    warp_wait(drain_bar, 0, true);
   } else if (warp >= kWarpB0 && warp < kWarpB0 + kNumBWarps) {
     // ---------------- the token operand (B) ----------------
     const int bt = threadIdx.x - kWarpB0 * 32;  // 0..127
@@ -351,16 +393,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
           }
           src[m] = reinterpret_cast<const char*>(a.x + size_t(t) * a.D) + ch * 16;
         }
-        for (int ks = 0; ks < KS; ++ks, ++it) {
+        for (int t = 0; t < KT; ++t, ++it) {
           const int s = it % kBStages;
           const uint32_t ph = (it / kBStages) & 1u;
-          if (!(ok = mbar_wait(empty(s), ph ^ 1u, abort_flag, a.hdr))) break;
+          if (!(ok = mbar_wait(bempty(s), ph ^ 1u, abort_flag, a.hdr))) break;
           const uint32_t dst = base + kOffB + s * kBBytes;
 #pragma unroll
-          for (int m = 0; m < kGatherPerThread; ++m) {
-            const int lin = bt + 128 * m, row = lin >> 3, ch = lin & 7;
-            if (row < n) cp_async16(dst + sw128(row, ch), src[m] + ks * 128, 16u);
-          }
+          for (int hb = 0; hb < kGroupsPerStage; ++hb)
+#pragma unroll
+            for (int m = 0; m < kGatherPerThread; ++m) {
+              const int lin = bt + 128 * m, row = lin >> 3, ch = lin & 7;
+              if (row < n) cp_async16(dst + hb * kBHalf + sw128(row, ch), src[m] + (t * kGroupsPerStage + hb) * 128, 16u);
+            }
           cp_async_arrive_noinc(bfull(s));
         }
       }
@@ -375,12 +419,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
           *abort_flag = 1;
           break;
         }
-        for (int ks = 0; ks < KS; ++ks, ++it) {
+        for (int t = 0; t < KT; ++t, ++it) {
           const int s = it % kBStages;
           const uint32_t ph = (it / kBStages) & 1u;
-          if (!(ok = mbar_wait(empty(s), ph ^ 1u, abort_flag, a.hdr))) break;
+          if (!(ok = mbar_wait(bempty(s), ph ^ 1u, abort_flag, a.hdr))) break;
           mbar_arrive_tx(bfull(s), kBBytes);
-          tma_load_2d(base + kOffB + s * kBBytes, &maps.b, ks * WK, p0, bfull(s));
+          for (int hb = 0; hb < kGroupsPerStage; ++hb)
+            tma_load_2d(base + kOffB + s * kBBytes + hb * kBHalf, &maps.b, (t * kGroupsPerStage + hb) * WK, p0,
+                        bfull(s));
           issued = it + 1;
         }
       }
@@ -392,14 +438,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
     }
   } else if (warp >= kWarpDq0 && warp < kWarpDq0 + kNumDqWarps) {
     // ---------------- dequantisation into the tensor-memory A stage ----------------
-    const int q = warp & 3;                   // TMEM lane quarter of this warp
-    const int hk = (warp - kWarpDq0) >> 2;    // which 32 of the 64 K values
-    const int L = q * 32 + lane;              // TMEM lane = weight row of the tile
+    // Four warps (one per TMEM lane quarter) take the even groups of K, four the
+    // odd ones: each stage's two groups are converted side by side, a warp
+    // converting all 64 codes of its row in a group.
+    const int q = warp & 3;                          // TMEM lane quarter of this warp
+    const int par = (warp - kWarpDq0) >> 2;          // group parity = position in the stage
+    const int L = q * 32 + lane;                     // TMEM lane = weight row of the tile
     const int srow_stage = GATEUP ? ((L & 1) ? 64 + (L >> 1) : (L >> 1)) : L;  // row in the code stage
     const bool vec_sb = (K / 64) % 8 == 0;
-    uint32_t it = 0;
+    uint32_t g0 = 0, t0 = 0;  // groups and stages of the tiles before this one
     bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, g0 += KS, t0 += KT) {
       int g, p0, R, j;
       if (!tile_info(tile, g, p0, R, j)) {
         *abort_flag = 1;
@@ -411,8 +460,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
       const size_t row = GATEUP ? size_t(ex) * a.I + j * 64 + (L >> 1) : size_t(ex) * a.D + j * WM + L;
       const uint16_t* srow = m.scales + row * (K / 64);
       const uint16_t* brow = m.biases + row * (K / 64);
+      // scales and biases of 8 groups at a time (one 16-byte load each), one window ahead
       uint4 s_cur = make_uint4(0u, 0u, 0u, 0u), b_cur = s_cur, s_nxt = s_cur, b_nxt = s_cur;
-      uint16_t s_one = 0, b_one = 0;
       if (vec_sb) {
         s_cur = *reinterpret_cast<const uint4*>(srow);
         b_cur = *reinterpret_cast<const uint4*>(brow);
@@ -420,52 +469,51 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
           s_nxt = *reinterpret_cast<const uint4*>(srow + 8);
           b_nxt = *reinterpret_cast<const uint4*>(brow + 8);
         }
-      } else {
-        s_one = srow[0];
-        b_one = brow[0];
       }
-      for (int ks = 0; ks < KS; ++ks, ++it) {
-        const int s = it % kBStages, cs = it % kCStages;
-        const uint32_t ph = (it / kBStages) & 1u, cph = (it / kCStages) & 1u;
+      int win = 0;
+      for (int ks = par; ks < KS; ks += 2) {
+        const uint32_t ig = g0 + ks, is = t0 + ks / kGroupsPerStage;
+        const int s = is % kAStages, cs = ig % kCStages;
+        const uint32_t ph = (is / kAStages) & 1u, cph = (ig / kCStages) & 1u;
         uint16_t sc, bi;
         if (vec_sb) {
-          const int gi = ks & 7;
-          sc = pick_bf16(s_cur, gi);
-          bi = pick_bf16(b_cur, gi);
-          if (gi == 7) {
+          if ((ks >> 3) != win) {  // next window of 8 groups
+            win = ks >> 3;
             s_cur = s_nxt;
             b_cur = b_nxt;
-            if (ks + 9 < KS) {
-              s_nxt = *reinterpret_cast<const uint4*>(srow + ks + 9);
-              b_nxt = *reinterpret_cast<const uint4*>(brow + ks + 9);
+            if (8 * (win + 1) < KS) {
+              s_nxt = *reinterpret_cast<const uint4*>(srow + 8 * (win + 1));
+              b_nxt = *reinterpret_cast<const uint4*>(brow + 8 * (win + 1));
             }
           }
+          sc = pick_bf16(s_cur, ks & 7);
+          bi = pick_bf16(b_cur, ks & 7);
         } else {
-          sc = s_one;
-          bi = b_one;
-          if (ks + 1 < KS) {
-            s_one = srow[ks + 1];
-            b_one = brow[ks + 1];
-          }
+          sc = srow[ks];
+          bi = brow[ks];
         }
         if (!(ok = mbar_wait(cfull(cs), cph, abort_flag, a.hdr))) break;
-        const uint4 w4 = *reinterpret_cast<const uint4*>(gbase + kOffC + cs * kCBytes + srow_stage * 32 + hk * 16);
+        const uint8_t* crow = gbase + kOffC + cs * kCBytes + srow_stage * 32;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(crow);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(crow + 16);
         const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16(sc), __ushort_as_bfloat16(sc));
         const __nv_bfloat162 b2 = __halves2bfloat162(__ushort_as_bfloat16(bi), __ushort_as_bfloat16(bi));
-        uint32_t o0[4], o1[4], o2[4], o3[4];
-        dq8_bf16(w4.x, s2, b2, o0);
-        dq8_bf16(w4.y, s2, b2, o1);
-        dq8_bf16(w4.z, s2, b2, o2);
-        dq8_bf16(w4.w, s2, b2, o3);
-        const uint32_t o[16] = {o0[0], o0[1], o0[2], o0[3], o1[0], o1[1], o1[2], o1[3],
-                                o2[0], o2[1], o2[2], o2[3], o3[0], o3[1], o3[2], o3[3]};
+        uint32_t o[32];
+        dq8_bf16(w0.x, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 0));
+        dq8_bf16(w0.y, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 4));
+        dq8_bf16(w0.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 8));
+        dq8_bf16(w0.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 12));
+        dq8_bf16(w1.x, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 16));
+        dq8_bf16(w1.y, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 20));
+        dq8_bf16(w1.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 24));
+        dq8_bf16(w1.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 28));
         // the code stage goes back to the TMA only after the reads above have
         // returned (the dequantised values depend on them)
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(cempty(cs));
-        if (!(ok = mbar_wait(empty(s), ph ^ 1u, abort_flag, a.hdr))) break;
-        tmem_st16(tmem + (uint32_t(q * 32) << 16) + kAColBase + s * kAStageCols + hk * 16, o);
+        if (!(ok = mbar_wait(aempty(s), ph ^ 1u, abort_flag, a.hdr))) break;
+        tmem_st32(tmem + (uint32_t(q * 32) << 16) + kAColBase + s * kAStageCols + par * kAGroupCols, o);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -564,7 +612,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
 
 }  // namespace
 
-bool gemm_wt_supported(const Ctx& c) { return c.I % 64 == 0 && c.D % WM == 0 && tmap_encoder_available(); }
+// Both contractions run in stages of 128 of K (D for gate/up, I for down).
+bool gemm_wt_supported(const Ctx& c) {
+  return c.I % (WK * kGroupsPerStage) == 0 && c.D % WM == 0 && tmap_encoder_available();
+}
 
 cudaError_t gemm_wt(const Ctx& c) {
   const moe_weights* w = c.w;
