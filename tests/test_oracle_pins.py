@@ -101,6 +101,28 @@ def test_router_exact_integer_logits():
     assert np.array_equal(logits.astype(np.int64), xi @ wi.T + bi)
 
 
+def test_router_sequential_order_closed_form():
+    # The logit is one fp32 FMA chain over d = 0..D-1 (reading R3). With every
+    # x = 1, a row [2^24, 1, ..., 1, -2^24] loses each +1 to round-to-even at
+    # 2^24 and ends at exactly 0, while the same values ordered
+    # [1, ..., 1, 2^24, -2^24] end at exactly D-2. A reversed, pairwise or
+    # strided order gives other values for at least one of the two rows.
+    L = _small_layer(D=256, E=8, k=2)
+    big = np.float32(2.0 ** 24)
+    w = np.zeros((L.E, L.D), np.float32)
+    w[0, :] = 1.0
+    w[0, 0], w[0, -1] = big, -big
+    w[1, :] = 1.0
+    w[1, -2], w[1, -1] = big, -big
+    L.router_w = w
+    L.router_bias = np.zeros(L.E, np.float32)
+    x = synth.f32_to_bf16_bits(np.ones((3, L.D), np.float32))
+    logits, _, _ = O.route(O.OracleLayer(L), x)
+    assert np.all(logits[:, 0] == 0.0)
+    assert np.all(logits[:, 1] == np.float32(L.D - 2))
+    assert np.all(logits[:, 2:] == 0.0)
+
+
 def test_router_close_to_fp64_dot():
     L = _small_layer(D=512, E=32, k=4)
     x = synth.make_x(2, 9, L.D)
