@@ -5,12 +5,11 @@
 // Silicon", section "Keep expert routing on the GPU").
 //
 // Router logits use one fixed fp32 evaluation order so that the top-k
-// decision (an integer result) is reproducible by any implementation:
-//   acc[l] = 0, l = 0..31
-//   for c = 0 .. D/32-1:  acc[l] = fma(float(x[t, 32c+l]), W_r[e, 32c+l], acc[l])
-//   for off = 16, 8, 4, 2, 1:  acc[l] = acc[l] + acc[l+off]   (l < off)
-//   logit = acc[0] (+ bias[e])
-// Lane l of a warp owns partial sum l; the tree is a shuffle-down reduction.
+// decision (an integer result) is reproducible by any implementation: the
+// plain dot product as one fused multiply-add chain in index order,
+//   acc = 0;  for d = 0 .. D-1:  acc = fma(float(x[t, d]), W_r[e, d], acc)
+//   logit = acc (+ bias[e])
+// Each logit is one thread's accumulator; the parallelism is across logits.
 #include <climits>
 
 #include "common.cuh"
@@ -20,81 +19,156 @@
 namespace moe {
 namespace {
 
-constexpr int kRouterWarps = 8;
-constexpr int kRouterDChunk = 1024;  // x columns staged in shared memory per pass
+// Router logits as a register-tiled SIMT GEMM: a CTA computes BT tokens x BE
+// experts, a thread TT tokens x TE experts, each logit one sequential FMA chain.
+// D is walked in chunks of kRgK: the chunk of x (bf16 -> fp32) and of W_r is
+// stored transposed in shared memory ([k][token], [k][expert]) so that a
+// thread reads its tokens and its experts of one k with 16-byte loads (each
+// shared by the lanes with the same tokens or experts). The next chunk
+// is loaded into registers, consecutive lanes along a row, while the current
+// one is used. The transposed rows are XOR-swizzled in groups of four (tokens
+// by (k/8)%4, experts by (k/4)%8) so that the transposing stores hit 32
+// different banks and a 4-group stays one aligned 16-byte word.
+constexpr int kRgK = 32;
 
-// Logits of TT tokens x (kRouterWarps * EPW) experts. Tokens are processed in
-// pairs with the packed fp32 FMA (two independent correctly rounded FMAs).
-template <int TT, int EPW>
-__global__ void __launch_bounds__(kRouterWarps * 32)
-    router_logits_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
-                         const float* __restrict__ bias, int T, int D, int E,
-                         float* __restrict__ logits, WsHeader* hdr) {
-  static_assert(TT % 2 == 0, "tokens go in pairs");
+template <int BT, int BE, int TT, int TE>
+__global__ void __launch_bounds__(BT * BE / (TT * TE))
+    router_gemm_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
+                       int T, int D, int E, float* __restrict__ logits, WsHeader* hdr) {
+  constexpr int N = BT * BE / (TT * TE);  // threads
+  constexpr int XP = BT * 4 / N;          // 16-byte x pieces per thread per chunk
+  constexpr int WP = BE * 8 / N;          // 16-byte W pieces per thread per chunk
+  constexpr int XG = TT / 4, WG = TE / 4;  // 16-byte reads of x and of W per k
+  static_assert(BT >= 32 && BE >= 32 && XP >= 1 && WP >= 1 && TT % 4 == 0 && TE % 4 == 0, "tile shape");
   // First kernel of every call: start the call's device status afresh. No
   // other CTA of this kernel reports, so nothing races with the clear.
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     hdr->status = 0;
     hdr->detail = 0;
   }
-  __shared__ __align__(16) uint16_t xs[TT * kRouterDChunk];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int t0 = blockIdx.x * TT;
-  const int e0 = (blockIdx.y * kRouterWarps + warp) * EPW;
-
-  float2 acc[TT / 2][EPW];
+  __shared__ __align__(16) float xs[2][kRgK][BT];
+  __shared__ __align__(16) float ws[2][kRgK][BE];
+  const int tid = threadIdx.x;
+  const int t0 = blockIdx.x * BT, e0 = blockIdx.y * BE;
+  const int ti = tid / (BE / TE), ei = tid % (BE / TE);  // tokens TT ti .., experts TE ei ..
+  // piece c of x: token row c/4 of the tile, columns 8(c%4) .. +7 of the chunk;
+  // piece c of W: expert row c/8, columns 4(c%8) .. +3. Consecutive lanes
+  // take consecutive pieces, so a warp reads whole row segments.
+  const uint16_t* xsrc[XP];
+  const float* wsrc[WP];
 #pragma unroll
-  for (int i = 0; i < TT / 2; ++i)
+  for (int m = 0; m < XP; ++m) {
+    const int c = tid + m * N, t = t0 + (c >> 2);
+    xsrc[m] = t < T ? x + size_t(t) * D + 8 * (c & 3) : nullptr;
+  }
 #pragma unroll
-    for (int j = 0; j < EPW; ++j) acc[i][j] = make_float2(0.f, 0.f);
-
-  const float* wrow[EPW];
+  for (int m = 0; m < WP; ++m) {
+    const int c = tid + m * N;
+    wsrc[m] = wr + size_t(min(e0 + (c >> 3), E - 1)) * D + 4 * (c & 7);
+  }
+  uint4 xr[XP];
+  float4 wv_in[WP];
+  auto load = [&](int d0) {
 #pragma unroll
-  for (int j = 0; j < EPW; ++j) wrow[j] = wr + size_t(min(e0 + j, E - 1)) * D;
-
-  for (int d0 = 0; d0 < D; d0 += kRouterDChunk) {
-    const int dc = min(kRouterDChunk, D - d0);  // a multiple of 64
-    __syncthreads();
-    for (int i = threadIdx.x; i < TT * (dc / 8); i += blockDim.x) {
-      const int t = i / (dc / 8), c8 = i % (dc / 8);
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (t0 + t < T) v = *reinterpret_cast<const uint4*>(x + size_t(t0 + t) * D + d0 + c8 * 8);
-      *reinterpret_cast<uint4*>(xs + t * kRouterDChunk + c8 * 8) = v;
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int c = 0; c < dc / 32; ++c) {
-      float wv[EPW];
+    for (int m = 0; m < XP; ++m)
+      xr[m] = xsrc[m] ? *reinterpret_cast<const uint4*>(xsrc[m] + d0) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int j = 0; j < EPW; ++j) wv[j] = __ldg(wrow[j] + d0 + 32 * c + lane);
+    for (int m = 0; m < WP; ++m) wv_in[m] = *reinterpret_cast<const float4*>(wsrc[m] + d0);
+  };
+  auto store = [&](int buf) {
 #pragma unroll
-      for (int i = 0; i < TT / 2; ++i) {
-        const float2 xv = make_float2(bf16_to_f32(xs[(2 * i) * kRouterDChunk + 32 * c + lane]),
-                                      bf16_to_f32(xs[(2 * i + 1) * kRouterDChunk + 32 * c + lane]));
+    for (int m = 0; m < XP; ++m) {
+      const int c = tid + m * N, r = c >> 2, ch = c & 3;
+      const int col = r ^ (ch << 3);  // k = 8 ch + i: (k / 8) % 4 = ch
+      const uint32_t xw[4] = {xr[m].x, xr[m].y, xr[m].z, xr[m].w};
 #pragma unroll
-        for (int j = 0; j < EPW; ++j) acc[i][j] = __ffma2_rn(xv, make_float2(wv[j], wv[j]), acc[i][j]);
+      for (int i = 0; i < 4; ++i) {
+        xs[buf][8 * ch + 2 * i][col] = __uint_as_float(xw[i] << 16);
+        xs[buf][8 * ch + 2 * i + 1][col] = __uint_as_float(xw[i] & 0xFFFF0000u);
       }
     }
+#pragma unroll
+    for (int m = 0; m < WP; ++m) {
+      const int c = tid + m * N, r = c >> 3, ch = c & 7;
+      const int col = r ^ (ch << 2);  // k = 4 ch + i: (k / 4) % 8 = ch
+      const float wa[4] = {wv_in[m].x, wv_in[m].y, wv_in[m].z, wv_in[m].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ws[buf][4 * ch + i][col] = wa[i];
+    }
+  };
+
+  float2 acc[TT / 2][TE];  // [token pair][expert]: .x token TT ti + 2p, .y token TT ti + 2p + 1
+#pragma unroll
+  for (int p = 0; p < TT / 2; ++p)
+#pragma unroll
+    for (int j = 0; j < TE; ++j) acc[p][j] = make_float2(0.f, 0.f);
+
+  const int nk = D / kRgK;
+  load(0);
+  store(0);
+  __syncthreads();
+  for (int kc = 0; kc < nk; ++kc) {
+    const int buf = kc & 1;
+    if (kc + 1 < nk) load((kc + 1) * kRgK);
+    auto rd = [&](int k, float4 (&xv)[XG], float4 (&wv)[WG]) {
+#pragma unroll
+      for (int g = 0; g < XG; ++g)
+        xv[g] = *reinterpret_cast<const float4*>(&xs[buf][k][(TT * ti + 4 * g) ^ (((k >> 3) & 3) << 3)]);
+#pragma unroll
+      for (int g = 0; g < WG; ++g)
+        wv[g] = *reinterpret_cast<const float4*>(&ws[buf][k][(TE * ei + 4 * g) ^ (((k >> 2) & 7) << 2)]);
+    };
+    // shared-memory reads run one k ahead of the FMAs that use them
+    float4 xv[XG], wv[WG];
+    rd(0, xv, wv);
+#pragma unroll
+    for (int k = 0; k < kRgK; ++k) {
+      float4 xn[XG], wn[WG];
+      if (k + 1 < kRgK) rd(k + 1, xn, wn);
+#pragma unroll
+      for (int g = 0; g < WG; ++g) {
+        const float wj[4] = {wv[g].x, wv[g].y, wv[g].z, wv[g].w};
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+          for (int q = 0; q < XG; ++q) {
+            acc[2 * q][4 * g + jj] =
+                __ffma2_rn(make_float2(xv[q].x, xv[q].y), make_float2(wj[jj], wj[jj]), acc[2 * q][4 * g + jj]);
+            acc[2 * q + 1][4 * g + jj] =
+                __ffma2_rn(make_float2(xv[q].z, xv[q].w), make_float2(wj[jj], wj[jj]), acc[2 * q + 1][4 * g + jj]);
+          }
+      }
+      if (k + 1 < kRgK) {
+#pragma unroll
+        for (int g = 0; g < XG; ++g) xv[g] = xn[g];
+#pragma unroll
+        for (int g = 0; g < WG; ++g) wv[g] = wn[g];
+      }
+    }
+    if (kc + 1 < nk) store(buf ^ 1);
+    __syncthreads();
   }
 
 #pragma unroll
-  for (int i = 0; i < TT / 2; ++i)
+  for (int p = 0; p < TT / 2; ++p)
 #pragma unroll
-    for (int j = 0; j < EPW; ++j) {
-      float a = acc[i][j].x, b = acc[i][j].y;
+    for (int h = 0; h < 2; ++h) {
+      const int t = t0 + TT * ti + 2 * p + h;
+      if (t >= T) continue;
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-        a = __fadd_rn(a, __shfl_down_sync(0xffffffffu, a, off));
-        b = __fadd_rn(b, __shfl_down_sync(0xffffffffu, b, off));
-      }
-      const int e = e0 + j, t = t0 + 2 * i;
-      if (lane == 0 && e < E) {
-        const float be = bias ? bias[e] : 0.f;
-        if (t < T) logits[size_t(t) * E + e] = bias ? __fadd_rn(a, be) : a;
-        if (t + 1 < T) logits[size_t(t + 1) * E + e] = bias ? __fadd_rn(b, be) : b;
+      for (int j = 0; j < TE; ++j) {
+        const int e = e0 + TE * ei + j;
+        if (e >= E) continue;
+        const float a = h ? acc[p][j].y : acc[p][j].x;
+        logits[size_t(t) * E + e] = bias ? __fadd_rn(a, bias[e]) : a;
       }
     }
 }
+// 8 tokens x 4 experts per thread measured fastest at T = 4096, E = 256
+// (113 us with 128-token tiles, 117 us with 64; 8 x 8 and 4 x 4 per thread
+// were slower): the reads of x, shared by a thread's four neighbours with the
+// same tokens, dominate the shared-memory traffic.
+constexpr int kRgE = 64, kRgTT = 8, kRgTE = 4;
 
 // Top-k of one token's logits (larger logit first, lower expert index on
 // ties) by one warp; lane l holds logits l, l+32, ... On return lane j < k
@@ -317,8 +391,10 @@ __global__ void __launch_bounds__(256)
 // token rows are staged; each lane then runs its fixed-order FMA chain.
 constexpr int kRouterSmallExperts = 2;
 
+// Token rows are staged D/8 + 1 16-byte words apart so that the tokens' reads
+// of one column fall in different banks.
 __host__ __device__ constexpr size_t router_small_smem(int TT, int D) {
-  return 16 + size_t(kRouterSmallExperts) * D * 4 + size_t(TT) * D * 2;
+  return 16 + size_t(kRouterSmallExperts) * D * 4 + size_t(TT) * (D / 8 + 1) * 16;
 }
 
 template <int TT>
@@ -331,7 +407,6 @@ __global__ void __launch_bounds__(kRouterSmallExperts * 32)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(rsm + 8);
   const float* ws = reinterpret_cast<const float*>(rsm + 16);
   uint4* xsm4 = reinterpret_cast<uint4*>(rsm + 16 + size_t(kRouterSmallExperts) * D * 4);
-  const uint16_t* xsm = reinterpret_cast<const uint16_t*>(xsm4);
   const int e0 = blockIdx.x * kRouterSmallExperts;
   const int ne = min(kRouterSmallExperts, E - e0);
   if (threadIdx.x == 0) {
@@ -347,29 +422,32 @@ __global__ void __launch_bounds__(kRouterSmallExperts * 32)
   }
   for (int i = threadIdx.x; i < TT * (D / 8); i += blockDim.x) {
     const int t = i / (D / 8), c8 = i % (D / 8);
-    xsm4[i] = t < T ? *reinterpret_cast<const uint4*>(x + size_t(t) * D + c8 * 8) : make_uint4(0u, 0u, 0u, 0u);
+    xsm4[t * (D / 8 + 1) + c8] =
+        t < T ? *reinterpret_cast<const uint4*>(x + size_t(t) * D + c8 * 8) : make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
   if (!mbar_wait(bar, 0, abort_flag, hdr, kWaitLimit, true)) return;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp >= ne) return;
-  const int e = e0 + warp;
-  const float* w = ws + size_t(warp) * D;
-  float acc[TT];
-#pragma unroll
-  for (int t = 0; t < TT; ++t) acc[t] = 0.f;
-  for (int c = 0; c < D / 32; ++c) {
-    const float wv = w[c * 32 + lane];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) acc[t] = fmaf(bf16_to_f32(xsm[t * D + c * 32 + lane]), wv, acc[t]);
+  // thread (token t, expert el): one FMA chain over d, 8 columns per step
+  const int t = threadIdx.x % TT, el = threadIdx.x / TT;
+  if (el >= ne || t >= T) return;
+  const int e = e0 + el;
+  const float4* w4 = reinterpret_cast<const float4*>(ws + size_t(el) * D);
+  const uint4* x4 = xsm4 + size_t(t) * (D / 8 + 1);
+  float acc = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < D / 8; ++c) {
+    const uint4 xv = x4[c];
+    const float4 wa = w4[2 * c], wb = w4[2 * c + 1];
+    acc = fmaf(__uint_as_float(xv.x << 16), wa.x, acc);
+    acc = fmaf(__uint_as_float(xv.x & 0xFFFF0000u), wa.y, acc);
+    acc = fmaf(__uint_as_float(xv.y << 16), wa.z, acc);
+    acc = fmaf(__uint_as_float(xv.y & 0xFFFF0000u), wa.w, acc);
+    acc = fmaf(__uint_as_float(xv.z << 16), wb.x, acc);
+    acc = fmaf(__uint_as_float(xv.z & 0xFFFF0000u), wb.y, acc);
+    acc = fmaf(__uint_as_float(xv.w << 16), wb.z, acc);
+    acc = fmaf(__uint_as_float(xv.w & 0xFFFF0000u), wb.w, acc);
   }
-#pragma unroll
-  for (int t = 0; t < TT; ++t) {
-    float a = acc[t];
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) a = __fadd_rn(a, __shfl_down_sync(0xffffffffu, a, off));
-    if (lane == 0 && t < T) logits[size_t(t) * E + e] = bias ? __fadd_rn(a, bias[e]) : a;
-  }
+  logits[size_t(t) * E + e] = bias ? __fadd_rn(acc, bias[e]) : acc;
 }
 
 // Top-k, weights, histogram, scan, scatter and block map of up to
@@ -473,14 +551,16 @@ cudaError_t route(const Ctx& c) {
     launch_done("route_small", c.stream);
     return cudaSuccess;
   }
-  if (c.T <= 8) {
-    dim3 grid(1, (c.E + kRouterWarps - 1) / kRouterWarps);
-    router_logits_kernel<8, 1><<<grid, kRouterWarps * 32, 0, c.stream>>>(c.x, w->router_w, w->router_bias,
-                                                                          c.T, c.D, c.E, c.logits, c.hdr);
+  if (c.T >= 4096) {  // 128-token tiles still fill the GPU
+    dim3 grid((c.T + 127) / 128, (c.E + kRgE - 1) / kRgE);
+    router_gemm_kernel<128, kRgE, kRgTT, kRgTE>
+        <<<grid, 128 * kRgE / (kRgTT * kRgTE), 0, c.stream>>>(c.x, w->router_w, w->router_bias, c.T, c.D, c.E,
+                                                              c.logits, c.hdr);
   } else {
-    dim3 grid((c.T + 15) / 16, (c.E + 8 * kRouterWarps - 1) / (8 * kRouterWarps));
-    router_logits_kernel<16, 8><<<grid, kRouterWarps * 32, 0, c.stream>>>(c.x, w->router_w, w->router_bias,
-                                                                           c.T, c.D, c.E, c.logits, c.hdr);
+    dim3 grid((c.T + 63) / 64, (c.E + kRgE - 1) / kRgE);
+    router_gemm_kernel<64, kRgE, kRgTT, kRgTE>
+        <<<grid, 64 * kRgE / (kRgTT * kRgTE), 0, c.stream>>>(c.x, w->router_w, w->router_bias, c.T, c.D, c.E,
+                                                             c.logits, c.hdr);
   }
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done("router_logits", c.stream);
