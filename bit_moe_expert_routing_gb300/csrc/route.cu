@@ -32,7 +32,7 @@ namespace {
 constexpr int kRgK = 32;
 
 template <int BT, int BE, int TT, int TE>
-__global__ void __launch_bounds__(BT * BE / (TT * TE))
+__global__ void __launch_bounds__(BT * BE / (TT * TE), BT >= 128 ? 3 : 1)
     router_gemm_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
                        int T, int D, int E, float* __restrict__ logits, WsHeader* hdr) {
   constexpr int N = BT * BE / (TT * TE);  // threads
@@ -174,15 +174,15 @@ constexpr int kRgE = 64, kRgTT = 8, kRgTE = 4;
 // ties) by one warp; lane l holds logits l, l+32, ... On return lane j < k
 // holds slot j: its expert and its weight, the softmax renormalised over the
 // k kept, exp(l_j - l_max) / sum.
-constexpr int kMaxPerLane = 32;  // E <= 1024
-
+// MPL >= ceil(E / 32) logits per lane (E <= 1024).
+template <int MPL>
 __device__ __forceinline__ void select_topk(const float* __restrict__ lg, int E, int k, int& myi, float& myw) {
   const int lane = threadIdx.x & 31;
   const int M = (E + 31) / 32;
-  float v[kMaxPerLane];
+  float v[MPL];
   unsigned taken = 0;
 #pragma unroll
-  for (int m = 0; m < kMaxPerLane; ++m) {
+  for (int m = 0; m < MPL; ++m) {
     const int e = lane + 32 * m;
     v[m] = (m < M && e < E) ? lg[e] : 0.f;
     if (!(m < M && e < E)) taken |= 1u << m;
@@ -193,7 +193,7 @@ __device__ __forceinline__ void select_topk(const float* __restrict__ lg, int E,
     float bv = -INFINITY;
     int bi = INT_MAX;
 #pragma unroll
-    for (int m = 0; m < kMaxPerLane; ++m) {
+    for (int m = 0; m < MPL; ++m) {
       const int e = lane + 32 * m;
       if (!((taken >> m) & 1u) && (v[m] > bv || (v[m] == bv && e < bi))) {
         bv = v[m];
@@ -225,7 +225,9 @@ __device__ __forceinline__ void select_topk(const float* __restrict__ lg, int E,
 
 // Top-k and weights of each token of a chunk, and the chunk's per-expert
 // assignment counts. One warp per token.
-__global__ void __launch_bounds__(256)
+constexpr int kTopkThreads = 512;
+template <int MPL>
+__global__ void __launch_bounds__(kTopkThreads)
     topk_hist_kernel(const float* __restrict__ logits, int T, int E, int k,
                      int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                      int32_t* __restrict__ chunk_count) {
@@ -238,7 +240,7 @@ __global__ void __launch_bounds__(256)
     if (t >= T) break;
     int myi;
     float myw;
-    select_topk(logits + size_t(t) * E, E, k, myi, myw);
+    select_topk<MPL>(logits + size_t(t) * E, E, k, myi, myw);
     if (lane < k) {
       topk_idx[size_t(t) * k + lane] = myi;
       topk_w[size_t(t) * k + lane] = myw;
@@ -455,6 +457,7 @@ __global__ void __launch_bounds__(kRouterSmallExperts * 32)
 // for the scan; warp t selects token t's experts).
 constexpr int kSmallRouteTokens = 16;
 
+template <int MPL>
 __global__ void __launch_bounds__(1024)
     route_small_kernel(const float* __restrict__ logits, int T, int E, int k, int BM, int max_blocks,
                        int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ count,
@@ -471,7 +474,7 @@ __global__ void __launch_bounds__(1024)
   if (warp < T) {
     int myi;
     float myw;
-    select_topk(logits + size_t(warp) * E, E, k, myi, myw);
+    select_topk<MPL>(logits + size_t(warp) * E, E, k, myi, myw);
     if (lane < k) {
       topk_idx[warp * k + lane] = myi;
       topk_w[warp * k + lane] = myw;
@@ -544,7 +547,12 @@ cudaError_t route(const Ctx& c) {
         c.x, w->router_w, w->router_bias, c.T, c.D, c.E, c.logits, c.hdr);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     launch_done("router_small", c.stream);
-    route_small_kernel<<<1, 1024, 0, c.stream>>>(c.logits, c.T, c.E, c.k, c.BM, c.max_blocks, c.topk_idx,
+    const int mpl = (c.E + 31) / 32;
+    void (*rs)(const float*, int, int, int, int, int, int32_t*, float*, int32_t*, int32_t*, int32_t*, int32_t*,
+               int32_t*, int32_t*, WsHeader*) =
+        mpl <= 4 ? route_small_kernel<4> : mpl <= 8 ? route_small_kernel<8> : mpl <= 16 ? route_small_kernel<16>
+                                                                                    : route_small_kernel<32>;
+    rs<<<1, 1024, 0, c.stream>>>(c.logits, c.T, c.E, c.k, c.BM, c.max_blocks, c.topk_idx,
                                                  c.topk_w, c.count, c.off, c.perm, c.inv, c.blocks, c.n_blocks,
                                                  c.hdr);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -565,8 +573,14 @@ cudaError_t route(const Ctx& c) {
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done("router_logits", c.stream);
 
-  topk_hist_kernel<<<c.n_chunks, 256, c.E * sizeof(int), c.stream>>>(c.logits, c.T, c.E, c.k, c.topk_idx,
-                                                                     c.topk_w, c.chunk);
+  {
+    const int mpl = (c.E + 31) / 32;
+    void (*tk)(const float*, int, int, int, int32_t*, float*, int32_t*) =
+        mpl <= 4 ? topk_hist_kernel<4> : mpl <= 8 ? topk_hist_kernel<8> : mpl <= 16 ? topk_hist_kernel<16>
+                                                                                  : topk_hist_kernel<32>;
+    tk<<<c.n_chunks, kTopkThreads, c.E * sizeof(int), c.stream>>>(c.logits, c.T, c.E, c.k, c.topk_idx, c.topk_w,
+                                                                  c.chunk);
+  }
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done("topk_hist", c.stream);
 
