@@ -65,7 +65,8 @@ constexpr int kWarpTma = 0, kWarpMma = 1, kWarpB0 = 2, kNumBWarps = 4, kWarpDq0 
 constexpr int kNumWarps = 22;
 constexpr int kGatherPerThread = kMaxN * 8 / (kNumBWarps * 32);  // 16-byte chunks per thread per K block
 constexpr int kNumThreads = kNumWarps * 32;
-constexpr int kXposeStride = 36;  // floats per row of an epilogue transpose buffer (conflict-free float4 reads)
+constexpr int kXposeStride = 36;
+constexpr int kEpiChunks = (kMaxN + 31) / 32;  // 16-token chunks per epilogue warp and tile  // floats per row of an epilogue transpose buffer (conflict-free float4 reads)
 
 constexpr uint32_t kOffB = 0;
 constexpr uint32_t kOffC = kOffB + kBStages * kBBytes;
@@ -535,12 +536,41 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
         break;
       }
       const int buf = tc & 1;
+      const bool sh = (g == a.E);
+      // down: this lane's token and routing weight for each of its chunks,
+      // loaded before the accumulator is ready (perm, then topk_w)
+      int tok[kEpiChunks];
+      float wgt[kEpiChunks];
+      if (!GATEUP) {
+        int asg[kEpiChunks];
+#pragma unroll
+        for (int m = 0; m < kEpiChunks; ++m) {
+          const int nn = half * 16 + 32 * m + (lane >> 1);
+          asg[m] = -1;
+          tok[m] = 0;
+          wgt[m] = 1.f;
+          if (nn < R) {
+            if (sh)
+              tok[m] = p0 + nn - A_rows;
+            else
+              asg[m] = a.perm[p0 + nn];
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < kEpiChunks; ++m)
+          if (asg[m] >= 0) {
+            tok[m] = asg[m] / a.k;
+            wgt[m] = a.topk_w[asg[m]];
+          }
+      }
       if (a.epi_wait_limit > 0 && !(ok = mbar_wait(never_bar, 0, abort_flag, a.hdr, a.epi_wait_limit))) break;
       if (!(ok = mbar_wait(accf(buf), (tc >> 1) & 1u, abort_flag, a.hdr))) break;
       tc_fence_after();
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + buf * kAccCols;
-      const bool sh = (g == a.E);
-      for (int n0 = half * 16; n0 < R; n0 += 32) {
+#pragma unroll
+      for (int m = 0; m < kEpiChunks; ++m) {
+        const int n0 = half * 16 + 32 * m;
+        if (n0 >= R) break;
         uint32_t v[16];
         tmem_ld16(tbase + n0, v);
         tmem_wait_ld();
@@ -574,18 +604,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
           __syncwarp();
           const int c = lane >> 1, nn = n0 + c;
           if (nn < R) {
-            const int p = p0 + nn;
-            int t;
-            float w;
-            if (sh) {
-              t = p - A_rows;
-              w = 1.f;
-            } else {
-              const int asg = a.perm[p];
-              t = asg / a.k;
-              w = a.topk_w[asg];
-            }
-            float* dst = a.y_acc + size_t(t) * a.D + j * WM + q * 32;
+            const float w = wgt[m];
+            float* dst = a.y_acc + size_t(tok[m]) * a.D + j * WM + q * 32;
 #pragma unroll
             for (int kq = 0; kq < 4; ++kq) {
               const int quad = (lane & 1) * 4 + kq;
