@@ -174,7 +174,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The wait, with the registers of the outstanding load as operands: they are
+// written asynchronously, so no use of them may be scheduled before this.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
 
 __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
@@ -567,13 +575,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
       if (!(ok = mbar_wait(accf(buf), (tc >> 1) & 1u, abort_flag, a.hdr))) break;
       tc_fence_after();
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + buf * kAccCols;
+      // tensor-memory reads run one chunk ahead of the chunk being processed
+      uint32_t va[16], vb[16];
+      if (half * 16 < R) tmem_ld16(tbase + half * 16, va);
+      tmem_wait_ld(va);
 #pragma unroll
       for (int m = 0; m < kEpiChunks; ++m) {
         const int n0 = half * 16 + 32 * m;
         if (n0 >= R) break;
-        uint32_t v[16];
-        tmem_ld16(tbase + n0, v);
-        tmem_wait_ld();
+        uint32_t(&v)[16] = (m & 1) ? vb : va;
+        if (m + 1 < kEpiChunks && n0 + 32 < R) tmem_ld16(tbase + n0 + 32, (m & 1) ? va : vb);
         if (GATEUP) {
           // lane 2i holds gate row i, lane 2i+1 up row i, for tokens n0..n0+15.
           // The pair swaps halves so that the even lane finishes the even
@@ -581,18 +592,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
           const bool odd = lane & 1;
           float hv[8];
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const float keep = __uint_as_float(odd ? v[2 * m + 1] : v[2 * m]);
-            const float recv = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? v[2 * m] : v[2 * m + 1]), 1);
-            hv[m] = odd ? silu_mul(recv, keep) : silu_mul(keep, recv);
+          for (int i = 0; i < 8; ++i) {
+            const float keep = __uint_as_float(odd ? v[2 * i + 1] : v[2 * i]);
+            const float recv = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? v[2 * i] : v[2 * i + 1]), 1);
+            hv[i] = odd ? silu_mul(recv, keep) : silu_mul(keep, recv);
           }
-          // lanes 4m and 4m+1 pack rows 2m, 2m+1 of their token parity
+          // lanes 4r and 4r+1 pack rows 2r, 2r+1 of their token parity
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const float hn = __shfl_down_sync(0xffffffffu, hv[m], 2);
-            const int nn = n0 + 2 * m + (odd ? 1 : 0);
+          for (int i = 0; i < 8; ++i) {
+            const float hn = __shfl_down_sync(0xffffffffu, hv[i], 2);
+            const int nn = n0 + 2 * i + (odd ? 1 : 0);
             if ((lane & 2) == 0 && nn < R) {
-              const uint32_t pk = uint32_t(f32_to_bf16(hv[m])) | (uint32_t(f32_to_bf16(hn)) << 16);
+              const uint32_t pk = uint32_t(f32_to_bf16(hv[i])) | (uint32_t(f32_to_bf16(hn)) << 16);
               *reinterpret_cast<uint32_t*>(a.h + size_t(p0 + nn) * a.I + j * 64 + (L >> 1)) = pk;
             }
           }
@@ -615,6 +626,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
           }
           __syncwarp();
         }
+        if (m & 1)
+          tmem_wait_ld(va);
+        else
+          tmem_wait_ld(vb);
       }
       tc_fence_before();
       __syncwarp();
