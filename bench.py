@@ -47,6 +47,31 @@ def measured_peaks() -> dict:
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None
+    when there is no record or the kernel source has changed since it was taken."""
+    import glob
+    import hashlib
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*_dram.txt")):
+        rec = {}
+        with open(path) as f:
+            for line in f:
+                if line.startswith("#") or ":" not in line:
+                    continue
+                key, val = line.split(":", 1)
+                rec[key.strip()] = val.strip()
+        if kernel not in rec or "source" not in rec:
+            continue
+        src = os.path.join(ROOT, rec["source"])
+        if not os.path.exists(src):
+            continue
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec.get("source_sha256"):
+                return None
+        return int(rec[kernel])
+    return None
+
+
 # --- distributed plumbing (replicas only) ----------------------------------------------------
 
 def dist_env() -> tuple[int, int, int]:
@@ -268,7 +293,7 @@ def run_ours(args) -> dict:
     if dominant in flops_of:
         ach = flops_of[dominant] / (kernels[dominant]["ms_per_launch"] / 1e3) / 1e12
         roof = dict(kernel=dominant, bound="tensor", achieved=ach, peak=peaks["bf16_tflops"], unit="TFLOP/s",
-                    frac=ach / peaks["bf16_tflops"], traffic=None,
+                    frac=ach / peaks["bf16_tflops"], traffic=profiled_traffic(dominant),
                     peak_source=f"{peaks['source']} bf16 burst")
     elif dominant in bytes_of:
         ach = bytes_of[dominant] / (kernels[dominant]["ms_per_launch"] / 1e3) / 1e9
