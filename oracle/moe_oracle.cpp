@@ -25,10 +25,8 @@
 //   R1 code j (0..7) of a uint32 word m is bits 4j..4j+3 and is element 8m+j.
 //   R2 groups run along each matrix's input (reduction) axis: D for gate/up,
 //      I for down. w[n][kk] = s[n][kk/64] * q[n][kk] + b[n][kk/64].
-//   R3 router logits are fp32 in one fixed order, the plain dot product:
-//      one fused multiply-add chain over d = 0, 1, ..., D-1, then + bias, so
-//      that the top-k decision, an integer, is taken identically by both
-//      implementations.
+//   R3 router logits are fp32 in one fixed order (below), so that the top-k
+//      decision, an integer, is taken identically by both implementations.
 //   R4 top-k is taken on the logits: larger logit first, lower expert index
 //      on ties. Weights: softmax over all E, renormalised over the k kept.
 //   R5 the shared expert has weight 1 and no gate.
@@ -90,13 +88,20 @@ double dq(const oracle_qmat& m, int rows, int K, int ex, int n, int kk) {
   return s * code_at(words, kk) + b;
 }
 
-// Router logit of token row xt for expert e (reading R3): one fp32 fused
-// multiply-add chain over the elements in index order, then + bias[e].
+// Router logit of token row xt for expert e (reading R3): 32 fp32 partial
+// sums, partial l collecting elements 32c+l for c = 0,1,... with a fused
+// multiply-add, then the pairwise tree l += l+16, l += l+8, ..., l += l+1,
+// then + bias[e].
 float router_logit(const oracle_layer& L, const uint16_t* xt, int e) {
+  float acc[32];
+  for (int l = 0; l < 32; ++l) acc[l] = 0.0f;
   const float* w = L.router_w + size_t(e) * L.D;
-  float acc = 0.0f;
-  for (int d = 0; d < L.D; ++d) acc = std::fma(bf16_to_float(xt[d]), w[d], acc);
-  float logit = acc;
+  for (int c = 0; c < L.D / 32; ++c)
+    for (int l = 0; l < 32; ++l)
+      acc[l] = std::fma(bf16_to_float(xt[32 * c + l]), w[32 * c + l], acc[l]);
+  for (int off = 16; off >= 1; off /= 2)
+    for (int l = 0; l < off; ++l) acc[l] = acc[l] + acc[l + off];
+  float logit = acc[0];
   if (L.router_bias) logit = logit + L.router_bias[e];
   return logit;
 }

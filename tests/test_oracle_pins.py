@@ -101,25 +101,32 @@ def test_router_exact_integer_logits():
     assert np.array_equal(logits.astype(np.int64), xi @ wi.T + bi)
 
 
-def test_router_sequential_order_closed_form():
-    # The logit is one fp32 FMA chain over d = 0..D-1 (reading R3). With every
-    # x = 1, a row [2^24, 1, ..., 1, -2^24] loses each +1 to round-to-even at
-    # 2^24 and ends at exactly 0, while the same values ordered
-    # [1, ..., 1, 2^24, -2^24] end at exactly D-2. A reversed, pairwise or
-    # strided order gives other values for at least one of the two rows.
+def test_router_order_closed_form():
+    # Reading R3 fixes the fp32 order: 32 partial sums, partial l taking the
+    # elements 32c+l in order c = 0, 1, ... with an FMA, then the pairwise tree
+    # l += l+16, l += l+8, ..., l += l+1. With x = 1 and D = 256 (8 terms per
+    # partial), worked by hand:
+    #   row A = [2^24 at d=0, -2^24 at d=32, 1 elsewhere]: partial 0 cancels
+    #     to 0 after two terms and collects 6 ones; the tree then adds exact
+    #     small integers: 6 + 31*8 = 254. (One chain in index order loses the
+    #     31 ones before d=32 to round-to-even at 2^24 and gives 223.)
+    #   row B = [2^24 at d=0, -2^24 at d=1, 1 elsewhere]: partial 0 stays 2^24
+    #     (its 7 ones are lost), partial 1 is -2^24 + 7 exactly, the others 8;
+    #     the tree levels give 2^24+8, 2^24+24, 2^24+56, 2^24+120 on lane 0 and
+    #     -2^24+15, +31, +63, +127 on lane 1, then 247. (One chain gives 254.)
     L = _small_layer(D=256, E=8, k=2)
     big = np.float32(2.0 ** 24)
     w = np.zeros((L.E, L.D), np.float32)
     w[0, :] = 1.0
-    w[0, 0], w[0, -1] = big, -big
+    w[0, 0], w[0, 32] = big, -big
     w[1, :] = 1.0
-    w[1, -2], w[1, -1] = big, -big
+    w[1, 0], w[1, 1] = big, -big
     L.router_w = w
     L.router_bias = np.zeros(L.E, np.float32)
     x = synth.f32_to_bf16_bits(np.ones((3, L.D), np.float32))
     logits, _, _ = O.route(O.OracleLayer(L), x)
-    assert np.all(logits[:, 0] == 0.0)
-    assert np.all(logits[:, 1] == np.float32(L.D - 2))
+    assert np.all(logits[:, 0] == 254.0)
+    assert np.all(logits[:, 1] == 247.0)
     assert np.all(logits[:, 2:] == 0.0)
 
 
