@@ -7,13 +7,17 @@
 //   gemv_gateup: a CTA owns 32 consecutive intermediate rows of one expert
 //     block. Their gate and up codes, scales and biases are contiguous in
 //     memory, so one thread fetches all of them into shared memory with six
-//     bulk (TMA) copies on one mbarrier while the CTA stages the block's token
-//     rows. Each warp then dots four rows with every token and writes
-//     h = bf16(silu(g) * u) in the permuted order.
+//     bulk (TMA) copies on one mbarrier while the CTA stages every token row
+//     (they do not depend on the routing). A warp takes four rows: per
+//     32-code chunk it loads the activations once and runs eight independent
+//     dot products (gate and up of each row); then h = bf16(silu(g) * u) in
+//     the permuted order.
 //   gemv_down: a CTA owns 16 output columns of one token. It bulk-copies the
 //     16 rows of the down matrix of each of the token's k experts and of the
-//     shared expert, stages the token's k+1 h rows, and sums
-//     w_j * (h_j . row) in fp32; y = bf16(sum). No atomics: deterministic.
+//     shared expert and stages the token's k+1 h rows. A thread takes one
+//     (expert slot, 32-code chunk) item and adds w_j * (h_j . row) for all 16
+//     columns; lanes and warps are then summed in a fixed order, y = bf16(sum).
+//     No atomics: deterministic.
 //
 // The kernels are bound by weight reads: every byte a CTA needs is in flight
 // at once (bulk copies do not hold registers), and the grids fill the GPU in
@@ -59,16 +63,17 @@ __device__ __forceinline__ float2 dot8_128(uint32_t w, float4 xa, float4 xb, flo
   return acc;
 }
 
-// s * sum(x*q) + b * sum(x) over one 32-code chunk c of a row; xr is the
-// chunk-major activation row, s and b the bf16 scale and bias of the chunk.
-__device__ __forceinline__ float chunk_dot(const uint4 w4, const float4* xr, int nch, int c, float xsum,
-                                           uint16_t s, uint16_t b) {
-  float2 d = make_float2(0.f, 0.f);
-  d = dot8_128(w4.x, xr[0 * nch + c], xr[1 * nch + c], d);
-  d = dot8_128(w4.y, xr[2 * nch + c], xr[3 * nch + c], d);
-  d = dot8_128(w4.z, xr[4 * nch + c], xr[5 * nch + c], d);
-  d = dot8_128(w4.w, xr[6 * nch + c], xr[7 * nch + c], d);
-  return bf16_to_f32(s) * (d.x + d.y - 128.f * xsum) + bf16_to_f32(b) * xsum;
+// s * sum(x*q) + b * sum(x) over one 32-code chunk of a row: w4 holds its
+// codes, xv its 32 activations (chunk-major float4s), xsum their sum, s and b
+// the bf16 scale and bias of its group.
+__device__ __forceinline__ float chunk_dot_r(const uint4 w4, const float4 (&xv)[8], float xsum, uint16_t s,
+                                             uint16_t b) {
+  float2 d0 = make_float2(0.f, 0.f), d1 = d0;
+  d0 = dot8_128(w4.x, xv[0], xv[1], d0);
+  d1 = dot8_128(w4.y, xv[2], xv[3], d1);
+  d0 = dot8_128(w4.z, xv[4], xv[5], d0);
+  d1 = dot8_128(w4.w, xv[6], xv[7], d1);
+  return bf16_to_f32(s) * ((d0.x + d0.y) + (d1.x + d1.y) - 128.f * xsum) + bf16_to_f32(b) * xsum;
 }
 
 struct GemvArgs {
@@ -128,23 +133,25 @@ struct GateupSmem {
 
 __global__ void __launch_bounds__(kGemvWarps * 32) gemv_gateup_kernel(GemvArgs a) {
   extern __shared__ __align__(128) uint8_t gsm[];
+  __shared__ int s_tok[kMaxGemvRows];
   if (blockIdx.x >= *a.n_blocks) return;
+  const int D = a.D, I = a.I, nch = D / 32, G = D / 64;
+  const int nt = min(a.T, kMaxGemvRows);
+  const GateupSmem L(D, nt);
+  const uint32_t bar = smem_u32(gsm);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gsm + 8);
   const int g = a.blocks[3 * blockIdx.x], p0 = a.blocks[3 * blockIdx.x + 1], R = a.blocks[3 * blockIdx.x + 2];
   const int A = a.T * a.k;
   if (g < 0 || g > a.E || R < 1 || R > kMaxGemvRows || R > a.T || p0 < 0 || p0 + R > A + a.T) {
     if (threadIdx.x == 0) report(a.hdr, MOE_ERR_DEVICE_CHECK, 3);
     return;
   }
-  const int D = a.D, I = a.I, nch = D / 32, G = D / 64;
-  const GateupSmem L(D, min(a.T, kMaxGemvRows));
   const bool shared = (g == a.E);
   const int ex = shared ? 0 : g;
   const moe_qmatrix mg = shared ? a.s_gate : a.gate;
   const moe_qmatrix mu = shared ? a.s_up : a.up;
   const int i0 = blockIdx.y * kGateupRows;
   const int nr = min(kGateupRows, I - i0);
-  const uint32_t bar = smem_u32(gsm);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gsm + 8);
 
   if (threadIdx.x == 0) {  // all of this CTA's weights, in six bulk copies
     *abort_flag = 0;
@@ -160,53 +167,77 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_gateup_kernel(GemvArgs a
     bulk_g2s(bar + uint32_t(L.su), mu.scales + row0 * G, sbb, bar);
     bulk_g2s(bar + uint32_t(L.bu), mu.biases + row0 * G, sbb, bar);
   }
-
+  // every token row (T <= 8), staged while the weights are in flight
   float4* xs4 = reinterpret_cast<float4*>(gsm + L.xs4);
   float* xsum = reinterpret_cast<float*>(gsm + L.xsum);
-  for (int q = threadIdx.x; q < R * (D / 8); q += blockDim.x) {
-    const int r = q / (D / 8), q8 = q % (D / 8);
-    const int p = p0 + r;
-    const int t = shared ? p - A : a.perm[p] / a.k;
-    stage_bf16x8(xs4 + size_t(r) * 8 * nch, nch, q8, *reinterpret_cast<const uint4*>(a.x + size_t(t) * D + q8 * 8));
+  for (int q = threadIdx.x; q < nt * (D / 8); q += blockDim.x) {
+    const int t = q / (D / 8), q8 = q % (D / 8);
+    stage_bf16x8(xs4 + size_t(t) * 8 * nch, nch, q8, *reinterpret_cast<const uint4*>(a.x + size_t(t) * D + q8 * 8));
+  }
+  if (threadIdx.x < R) {
+    const int p = p0 + threadIdx.x;
+    int t = shared ? p - A : a.perm[p] / a.k;
+    if (t < 0 || t >= nt) {
+      report(a.hdr, MOE_ERR_DEVICE_CHECK, 4);
+      t = 0;
+    }
+    s_tok[threadIdx.x] = t;
   }
   __syncthreads();
-  chunk_sums(xs4, xsum, R, nch);
+  chunk_sums(xs4, xsum, nt, nch);
   __syncthreads();
   if (!mbar_wait(bar, 0, abort_flag, a.hdr, kWaitLimit, true)) return;
 
+  // warp w takes rows w, w+8, w+16, w+24: for each 32-code chunk of the token
+  // row the activations are loaded once and feed eight independent dot products
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kRowsPerWarp = kGateupRows / kGemvWarps;
   const uint8_t* cg = gsm + L.codes_g;
   const uint8_t* cu = gsm + L.codes_u;
   const uint16_t* sg = reinterpret_cast<const uint16_t*>(gsm + L.sg);
   const uint16_t* bg = reinterpret_cast<const uint16_t*>(gsm + L.bg);
   const uint16_t* su = reinterpret_cast<const uint16_t*>(gsm + L.su);
   const uint16_t* bu = reinterpret_cast<const uint16_t*>(gsm + L.bu);
-  for (int rr = warp; rr < nr; rr += kGemvWarps) {
-    const uint4* rg = reinterpret_cast<const uint4*>(cg + size_t(rr) * D / 2);
-    const uint4* ru = reinterpret_cast<const uint4*>(cu + size_t(rr) * D / 2);
 #pragma unroll 1
-    for (int r = 0; r < R; ++r) {
-      const float4* xr = xs4 + size_t(r) * 8 * nch;
-      float gv = 0.f, uv = 0.f;
-      for (int c = lane; c < nch; c += 32) {  // 32-code chunk c lies in group c/2
-        const float sx = xsum[r * nch + c];
-        const int gi = rr * G + c / 2;
-        gv += chunk_dot(rg[c], xr, nch, c, sx, sg[gi], bg[gi]);
-        uv += chunk_dot(ru[c], xr, nch, c, sx, su[gi], bu[gi]);
+  for (int r = 0; r < R; ++r) {
+    const int t = s_tok[r];
+    const float4* xr = xs4 + size_t(t) * 8 * nch;
+    float gacc[kRowsPerWarp], uacc[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) gacc[i] = uacc[i] = 0.f;
+    for (int c = lane; c < nch; c += 32) {  // 32-code chunk c lies in group c/2
+      float4 xv[8];
+#pragma unroll
+      for (int jq = 0; jq < 8; ++jq) xv[jq] = xr[jq * nch + c];
+      const float sx = xsum[t * nch + c];
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int rr = warp + kGemvWarps * i;
+        if (rr < nr) {
+          const uint4 wg = reinterpret_cast<const uint4*>(cg + size_t(rr) * D / 2)[c];
+          const uint4 wu = reinterpret_cast<const uint4*>(cu + size_t(rr) * D / 2)[c];
+          const int gi = rr * G + c / 2;
+          gacc[i] += chunk_dot_r(wg, xv, sx, sg[gi], bg[gi]);
+          uacc[i] += chunk_dot_r(wu, xv, sx, su[gi], bu[gi]);
+        }
       }
+    }
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
 #pragma unroll
       for (int off = 16; off >= 1; off >>= 1) {
-        gv += __shfl_xor_sync(0xffffffffu, gv, off);
-        uv += __shfl_xor_sync(0xffffffffu, uv, off);
+        gacc[i] += __shfl_xor_sync(0xffffffffu, gacc[i], off);
+        uacc[i] += __shfl_xor_sync(0xffffffffu, uacc[i], off);
       }
-      if (lane == 0) a.h[size_t(p0 + r) * I + i0 + rr] = f32_to_bf16(silu_mul(gv, uv));
+      const int rr = warp + kGemvWarps * i;
+      if (lane == 0 && rr < nr) a.h[size_t(p0 + r) * I + i0 + rr] = f32_to_bf16(silu_mul(gacc[i], uacc[i]));
     }
   }
 }
 
 // Shared-memory layout of a down CTA (k+1 slots, I input columns).
 struct DownSmem {
-  size_t codes, sc, bi, hs4, hsum, w, total;
+  size_t codes, sc, bi, hs4, hsum, w, red, total;
   __host__ __device__ DownSmem(int k, int I) {
     const size_t S = size_t(k) + 1;
     codes = 16;  // bytes 0..15: mbarrier and abort flag
@@ -215,7 +246,8 @@ struct DownSmem {
     hs4 = (bi + S * kDownCols * (I / 64) * 2 + 15) & ~size_t(15);
     hsum = hs4 + S * size_t(I) * 4;
     w = hsum + S * size_t(I / 32) * 4;
-    total = w + S * 4;
+    red = (w + S * 4 + 15) & ~size_t(15);
+    total = red + size_t(kGemvWarps) * kDownCols * 4;
   }
 };
 
@@ -263,22 +295,47 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_down_kernel(GemvArgs a) 
   __syncthreads();
   if (!mbar_wait(bar, 0, abort_flag, a.hdr, kWaitLimit, true)) return;
 
+  // thread item it = (slot j, 32-code chunk c): its activations are loaded
+  // once and feed the dot products of all 16 output columns; the partial sums
+  // are then reduced over the lanes and over the warps in a fixed order
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint8_t* codes = dsm + L.codes;
   const uint16_t* sc = reinterpret_cast<const uint16_t*>(dsm + L.sc);
   const uint16_t* bi = reinterpret_cast<const uint16_t*>(dsm + L.bi);
-  for (int cl = warp; cl < kDownCols; cl += kGemvWarps) {
-    float part = 0.f;
-    for (int it = lane; it < S * nch; it += 32) {
-      const int j = it / nch, c = it % nch;
+  float part[kDownCols];
+#pragma unroll
+  for (int cl = 0; cl < kDownCols; ++cl) part[cl] = 0.f;
+  for (int it = threadIdx.x; it < S * nch; it += blockDim.x) {
+    const int j = it / nch, c = it % nch;
+    float4 xv[8];
+    const float4* xr = hs4 + size_t(j) * 8 * nch;
+#pragma unroll
+    for (int jq = 0; jq < 8; ++jq) xv[jq] = xr[jq * nch + c];
+    const float sx = hsum[j * nch + c], wj = s_w[j];
+#pragma unroll
+    for (int cl = 0; cl < kDownCols; ++cl) {
       const int rowi = j * kDownCols + cl;  // row of slot j's copy
       const uint4 w4 = reinterpret_cast<const uint4*>(codes + size_t(rowi) * (I / 2))[c];
       const int gi = rowi * G + c / 2;
-      part += s_w[j] * chunk_dot(w4, hs4 + size_t(j) * 8 * nch, nch, c, hsum[j * nch + c], sc[gi], bi[gi]);
+      part[cl] += wj * chunk_dot_r(w4, xv, sx, sc[gi], bi[gi]);
     }
+  }
+  float* red = reinterpret_cast<float*>(dsm + L.red);  // [kGemvWarps][kDownCols]
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if (lane == 0) a.y[size_t(t) * D + d0 + cl] = f32_to_bf16(part);
+  for (int cl = 0; cl < kDownCols; ++cl) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) part[cl] += __shfl_xor_sync(0xffffffffu, part[cl], off);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int cl = 0; cl < kDownCols; ++cl) red[warp * kDownCols + cl] = part[cl];
+  }
+  __syncthreads();
+  if (threadIdx.x < kDownCols) {
+    float y = 0.f;
+#pragma unroll
+    for (int w = 0; w < kGemvWarps; ++w) y += red[w * kDownCols + threadIdx.x];
+    a.y[size_t(t) * D + d0 + threadIdx.x] = f32_to_bf16(y);
   }
 }
 

@@ -5,11 +5,12 @@
 // Silicon", section "Keep expert routing on the GPU").
 //
 // Router logits use one fixed fp32 evaluation order so that the top-k
-// decision (an integer result) is reproducible by any implementation: the
-// plain dot product as one fused multiply-add chain in index order,
-//   acc = 0;  for d = 0 .. D-1:  acc = fma(float(x[t, d]), W_r[e, d], acc)
-//   logit = acc (+ bias[e])
-// Each logit is one thread's accumulator; the parallelism is across logits.
+// decision (an integer result) is reproducible by any implementation:
+//   acc[l] = 0, l = 0..31
+//   for c = 0 .. D/32-1:  acc[l] = fma(float(x[t, 32c+l]), W_r[e, 32c+l], acc[l])
+//   for off = 16, 8, 4, 2, 1:  acc[l] = acc[l] + acc[l+off]   (l < off)
+//   logit = acc[0] (+ bias[e])
+// Lane l of a warp owns partial sum l; the tree is a shuffle-down reduction.
 #include <climits>
 
 #include "common.cuh"
@@ -19,156 +20,199 @@
 namespace moe {
 namespace {
 
-// Router logits as a register-tiled SIMT GEMM: a CTA computes BT tokens x BE
-// experts, a thread TT tokens x TE experts, each logit one sequential FMA chain.
-// D is walked in chunks of kRgK: the chunk of x (bf16 -> fp32) and of W_r is
-// stored transposed in shared memory ([k][token], [k][expert]) so that a
-// thread reads its tokens and its experts of one k with 16-byte loads (each
-// shared by the lanes with the same tokens or experts). The next chunk
-// is loaded into registers, consecutive lanes along a row, while the current
-// one is used. The transposed rows are XOR-swizzled in groups of four (tokens
-// by (k/8)%4, experts by (k/4)%8) so that the transposing stores hit 32
-// different banks and a 4-group stays one aligned 16-byte word.
-constexpr int kRgK = 32;
+// Router logits in the order above for larger T. A warp computes 8 tokens x
+// 8 experts: lane l holds partial sum l of each of those 64 logits (as 32
+// pairs of tokens for the packed FMA), and the shuffle tree reduces them at
+// the end. A CTA of kRtWarps warps covers kRtTok tokens x kRtExp experts. D
+// is walked in chunks of kRtDC, staged in shared memory one chunk ahead:
+//   W  (router-weight rows): WDUP = false, fp32 as in memory (cp.async);
+//      WDUP = true, each value twice, the (w, w) operand of the packed FMA;
+//   x  (token rows): XF = false, words holding one column of two tokens as
+//      bf16; XF = true, the same pair as two fp32 values.
+// With both set the inner step is loads and paired FMAs only.
+constexpr int kRtTok = 32, kRtExp = 32, kRtWarps = 16, kRtDC = 128;
+template <bool WDUP, bool XF>
+constexpr size_t rt_w_bytes() { return size_t(2) * kRtExp * kRtDC * (WDUP ? 8 : 4); }
+template <bool WDUP, bool XF>
+constexpr size_t rt_smem() { return rt_w_bytes<WDUP, XF>() + size_t(2) * (kRtTok / 2) * kRtDC * (XF ? 8 : 4); }
+static_assert((kRtTok / 8) * (kRtExp / 8) == kRtWarps, "one 8 x 8 logit tile per warp");
+static_assert((kRtTok / 2) * (kRtDC / 4) == kRtWarps * 32, "one token-pair item per thread and chunk");
+static_assert(kRtExp * (kRtDC / 4) == 2 * kRtWarps * 32, "two router-weight pieces per thread and chunk");
 
-template <int BT, int BE, int TT, int TE>
-__global__ void __launch_bounds__(BT * BE / (TT * TE), BT >= 128 ? 3 : 1)
-    router_gemm_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
+__device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_all() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+template <bool WDUP, bool XF>
+__global__ void __launch_bounds__(kRtWarps * 32, 1)
+    router_tree_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
                        int T, int D, int E, float* __restrict__ logits, WsHeader* hdr) {
-  constexpr int N = BT * BE / (TT * TE);  // threads
-  constexpr int XP = BT * 4 / N;          // 16-byte x pieces per thread per chunk
-  constexpr int WP = BE * 8 / N;          // 16-byte W pieces per thread per chunk
-  constexpr int XG = TT / 4, WG = TE / 4;  // 16-byte reads of x and of W per k
-  static_assert(BT >= 32 && BE >= 32 && XP >= 1 && WP >= 1 && TT % 4 == 0 && TE % 4 == 0, "tile shape");
   // First kernel of every call: start the call's device status afresh. No
   // other CTA of this kernel reports, so nothing races with the clear.
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     hdr->status = 0;
     hdr->detail = 0;
   }
-  __shared__ __align__(16) float xs[2][kRgK][BT];
-  __shared__ __align__(16) float ws[2][kRgK][BE];
-  const int tid = threadIdx.x;
-  const int t0 = blockIdx.x * BT, e0 = blockIdx.y * BE;
-  const int ti = tid / (BE / TE), ei = tid % (BE / TE);  // tokens TT ti .., experts TE ei ..
-  // piece c of x: token row c/4 of the tile, columns 8(c%4) .. +7 of the chunk;
-  // piece c of W: expert row c/8, columns 4(c%8) .. +3. Consecutive lanes
-  // take consecutive pieces, so a warp reads whole row segments.
-  const uint16_t* xsrc[XP];
-  const float* wsrc[WP];
-#pragma unroll
-  for (int m = 0; m < XP; ++m) {
-    const int c = tid + m * N, t = t0 + (c >> 2);
-    xsrc[m] = t < T ? x + size_t(t) * D + 8 * (c & 3) : nullptr;
-  }
-#pragma unroll
-  for (int m = 0; m < WP; ++m) {
-    const int c = tid + m * N;
-    wsrc[m] = wr + size_t(min(e0 + (c >> 3), E - 1)) * D + 4 * (c & 7);
-  }
-  uint4 xr[XP];
-  float4 wv_in[WP];
-  auto load = [&](int d0) {
-#pragma unroll
-    for (int m = 0; m < XP; ++m)
-      xr[m] = xsrc[m] ? *reinterpret_cast<const uint4*>(xsrc[m] + d0) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int m = 0; m < WP; ++m) wv_in[m] = *reinterpret_cast<const float4*>(wsrc[m] + d0);
+  extern __shared__ __align__(16) uint8_t rt_smem_raw[];
+  uint8_t* wsb = rt_smem_raw;                            // [2][kRtExp][kRtDC] of float or float2
+  uint8_t* xpb = rt_smem_raw + rt_w_bytes<WDUP, XF>();  // [2][kRtTok/2][kRtDC] of bf16 pair or float2
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * kRtTok, eb = blockIdx.y * kRtExp;
+  const int tg = warp / (kRtExp / 8), eg = warp % (kRtExp / 8);  // token pairs 4tg.., experts 8eg..
+
+  // W pieces: 16 bytes (4 columns) of router-weight row r, rows eb .. (clamped to E-1)
+  float4 wreg[2];
+  auto w_piece = [&](int m, int& r, int& c4) {
+    const int i = threadIdx.x + m * blockDim.x;
+    r = i / (kRtDC / 4);
+    c4 = i % (kRtDC / 4);
   };
-  auto store = [&](int buf) {
+  auto issue_w = [&](int buf, int d0, int dc) {
 #pragma unroll
-    for (int m = 0; m < XP; ++m) {
-      const int c = tid + m * N, r = c >> 2, ch = c & 3;
-      const int col = r ^ (ch << 3);  // k = 8 ch + i: (k / 8) % 4 = ch
-      const uint32_t xw[4] = {xr[m].x, xr[m].y, xr[m].z, xr[m].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        xs[buf][8 * ch + 2 * i][col] = __uint_as_float(xw[i] << 16);
-        xs[buf][8 * ch + 2 * i + 1][col] = __uint_as_float(xw[i] & 0xFFFF0000u);
+    for (int m = 0; m < 2; ++m) {
+      int r, c4;
+      w_piece(m, r, c4);
+      const float* src = wr + size_t(min(eb + r, E - 1)) * D + d0 + c4 * 4;
+      if (WDUP) {
+        wreg[m] = 4 * c4 < dc ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+      } else if (4 * c4 < dc) {
+        cp_async16_cg(smem_u32(wsb + ((size_t(buf) * kRtExp + r) * kRtDC + c4 * 4) * 4), src);
       }
     }
+    if (!WDUP) cp_async_commit_all();
+  };
+  auto store_w = [&](int buf) {
+    if (WDUP) {
 #pragma unroll
-    for (int m = 0; m < WP; ++m) {
-      const int c = tid + m * N, r = c >> 3, ch = c & 7;
-      const int col = r ^ (ch << 2);  // k = 4 ch + i: (k / 4) % 8 = ch
-      const float wa[4] = {wv_in[m].x, wv_in[m].y, wv_in[m].z, wv_in[m].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) ws[buf][4 * ch + i][col] = wa[i];
+      for (int m = 0; m < 2; ++m) {
+        int r, c4;
+        w_piece(m, r, c4);
+        float4* dst = reinterpret_cast<float4*>(wsb + ((size_t(buf) * kRtExp + r) * kRtDC + c4 * 4) * 8);
+        dst[0] = make_float4(wreg[m].x, wreg[m].x, wreg[m].y, wreg[m].y);
+        dst[1] = make_float4(wreg[m].z, wreg[m].z, wreg[m].w, wreg[m].w);
+      }
+    }
+  };
+  // this thread's x item: token pair ip, columns 4 dq .. +3 of the chunk
+  const int ip = threadIdx.x / (kRtDC / 4), dq = threadIdx.x % (kRtDC / 4);
+  const int ta = t0 + 2 * ip, tb = ta + 1;
+  uint2 xa = make_uint2(0u, 0u), xb = xa;
+  auto load_x = [&](int d0, int dc) {
+    const bool in = 4 * dq < dc;
+    xa = (in && ta < T) ? *reinterpret_cast<const uint2*>(x + size_t(ta) * D + d0 + 4 * dq) : make_uint2(0u, 0u);
+    xb = (in && tb < T) ? *reinterpret_cast<const uint2*>(x + size_t(tb) * D + d0 + 4 * dq) : make_uint2(0u, 0u);
+  };
+  auto store_x = [&](int buf) {
+    if (XF) {  // (token ta, token tb) of each column as two fp32 values
+      float4* dst = reinterpret_cast<float4*>(xpb + ((size_t(buf) * (kRtTok / 2) + ip) * kRtDC + 4 * dq) * 8);
+      dst[0] = make_float4(__uint_as_float(xa.x << 16), __uint_as_float(xb.x << 16),
+                           __uint_as_float(xa.x & 0xFFFF0000u), __uint_as_float(xb.x & 0xFFFF0000u));
+      dst[1] = make_float4(__uint_as_float(xa.y << 16), __uint_as_float(xb.y << 16),
+                           __uint_as_float(xa.y & 0xFFFF0000u), __uint_as_float(xb.y & 0xFFFF0000u));
+    } else {  // word = (token ta, token tb) of one column, bf16
+      *reinterpret_cast<uint4*>(xpb + ((size_t(buf) * (kRtTok / 2) + ip) * kRtDC + 4 * dq) * 4) =
+          make_uint4(__byte_perm(xa.x, xb.x, 0x5410), __byte_perm(xa.x, xb.x, 0x7632),
+                     __byte_perm(xa.y, xb.y, 0x5410), __byte_perm(xa.y, xb.y, 0x7632));
     }
   };
 
-  float2 acc[TT / 2][TE];  // [token pair][expert]: .x token TT ti + 2p, .y token TT ti + 2p + 1
+  float2 acc[4][8];  // [token pair][expert]: .x token 8tg+2p, .y token 8tg+2p+1
 #pragma unroll
-  for (int p = 0; p < TT / 2; ++p)
+  for (int p = 0; p < 4; ++p)
 #pragma unroll
-    for (int j = 0; j < TE; ++j) acc[p][j] = make_float2(0.f, 0.f);
+    for (int j = 0; j < 8; ++j) acc[p][j] = make_float2(0.f, 0.f);
 
-  const int nk = D / kRgK;
-  load(0);
-  store(0);
+  const int nchunks = (D + kRtDC - 1) / kRtDC;
+  issue_w(0, 0, min(kRtDC, D));
+  load_x(0, min(kRtDC, D));
+  store_w(0);
+  store_x(0);
+  if (!WDUP) cp_async_wait_all();
   __syncthreads();
-  for (int kc = 0; kc < nk; ++kc) {
-    const int buf = kc & 1;
-    if (kc + 1 < nk) load((kc + 1) * kRgK);
-    auto rd = [&](int k, float4 (&xv)[XG], float4 (&wv)[WG]) {
+  for (int kc = 0; kc < nchunks; ++kc) {
+    const int buf = kc & 1, d0 = kc * kRtDC, dc = min(kRtDC, D - d0);
+    const bool nxt = kc + 1 < nchunks;
+    if (nxt) {
+      const int dn = min(kRtDC, D - d0 - kRtDC);
+      issue_w(buf ^ 1, d0 + kRtDC, dn);
+      load_x(d0 + kRtDC, dn);
+    }
+#pragma unroll 2
+    for (int c = 0; c < dc / 32; ++c) {
+      const int col = 32 * c + lane;
+      float2 wv[8];
 #pragma unroll
-      for (int g = 0; g < XG; ++g)
-        xv[g] = *reinterpret_cast<const float4*>(&xs[buf][k][(TT * ti + 4 * g) ^ (((k >> 3) & 3) << 3)]);
-#pragma unroll
-      for (int g = 0; g < WG; ++g)
-        wv[g] = *reinterpret_cast<const float4*>(&ws[buf][k][(TE * ei + 4 * g) ^ (((k >> 2) & 7) << 2)]);
-    };
-    // shared-memory reads run one k ahead of the FMAs that use them
-    float4 xv[XG], wv[WG];
-    rd(0, xv, wv);
-#pragma unroll
-    for (int k = 0; k < kRgK; ++k) {
-      float4 xn[XG], wn[WG];
-      if (k + 1 < kRgK) rd(k + 1, xn, wn);
-#pragma unroll
-      for (int g = 0; g < WG; ++g) {
-        const float wj[4] = {wv[g].x, wv[g].y, wv[g].z, wv[g].w};
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-          for (int q = 0; q < XG; ++q) {
-            acc[2 * q][4 * g + jj] =
-                __ffma2_rn(make_float2(xv[q].x, xv[q].y), make_float2(wj[jj], wj[jj]), acc[2 * q][4 * g + jj]);
-            acc[2 * q + 1][4 * g + jj] =
-                __ffma2_rn(make_float2(xv[q].z, xv[q].w), make_float2(wj[jj], wj[jj]), acc[2 * q + 1][4 * g + jj]);
-          }
+      for (int j = 0; j < 8; ++j) {
+        const size_t wi = (size_t(buf) * kRtExp + 8 * eg + j) * kRtDC + col;
+        if (WDUP) {
+          wv[j] = reinterpret_cast<const float2*>(wsb)[wi];
+        } else {
+          const float w = reinterpret_cast<const float*>(wsb)[wi];
+          wv[j] = make_float2(w, w);
+        }
       }
-      if (k + 1 < kRgK) {
 #pragma unroll
-        for (int g = 0; g < XG; ++g) xv[g] = xn[g];
+      for (int p = 0; p < 4; ++p) {
+        const size_t xi = (size_t(buf) * (kRtTok / 2) + 4 * tg + p) * kRtDC + col;
+        float2 xv;
+        if (XF) {
+          xv = reinterpret_cast<const float2*>(xpb)[xi];
+        } else {
+          const uint32_t w2 = reinterpret_cast<const uint32_t*>(xpb)[xi];
+          xv = make_float2(__uint_as_float(w2 << 16), __uint_as_float(w2 & 0xFFFF0000u));
+        }
 #pragma unroll
-        for (int g = 0; g < WG; ++g) wv[g] = wn[g];
+        for (int j = 0; j < 8; ++j) acc[p][j] = __ffma2_rn(xv, wv[j], acc[p][j]);
       }
     }
-    if (kc + 1 < nk) store(buf ^ 1);
+    if (nxt) {
+      store_w(buf ^ 1);
+      store_x(buf ^ 1);
+      if (!WDUP) cp_async_wait_all();
+    }
     __syncthreads();
   }
 
+  // The 32 partial sums of each of the 64 logits are reduced by the tree of
+  // the canonical order (lane offsets 16, 8, 4, 2, 1) as a recursive halving:
+  // at each level a lane keeps half of its values, sends the other half to
+  // its partner and adds what it receives. Every addition joins the same two
+  // sub-tree sums as the shuffle-down tree (fp32 addition is commutative), so
+  // the logits are bit-identical, with 62 shuffles instead of 320. Lane l
+  // ends with entry l = 8p + j of the tile: v[0] for token 8tg+2p, v[1] for
+  // token 8tg+2p+1, expert 8eg+j.
+  float v[64];
 #pragma unroll
-  for (int p = 0; p < TT / 2; ++p)
+  for (int p = 0; p < 4; ++p)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int t = t0 + TT * ti + 2 * p + h;
-      if (t >= T) continue;
-#pragma unroll
-      for (int j = 0; j < TE; ++j) {
-        const int e = e0 + TE * ei + j;
-        if (e >= E) continue;
-        const float a = h ? acc[p][j].y : acc[p][j].x;
-        logits[size_t(t) * E + e] = bias ? __fadd_rn(a, bias[e]) : a;
-      }
+    for (int j = 0; j < 8; ++j) {
+      v[2 * (8 * p + j)] = acc[p][j].x;
+      v[2 * (8 * p + j) + 1] = acc[p][j].y;
     }
+#pragma unroll
+  for (int lvl = 0; lvl < 5; ++lvl) {
+    const int o = 16 >> lvl, half = 32 >> lvl;  // partner offset; values kept after this level
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+    }
+  }
+  {
+    const int p = lane >> 3, j = lane & 7;
+    const int e = eb + 8 * eg + j, t = t0 + 8 * tg + 2 * p;
+    if (e < E) {
+      const float be = bias ? bias[e] : 0.f;
+      if (t < T) logits[size_t(t) * E + e] = bias ? __fadd_rn(v[0], be) : v[0];
+      if (t + 1 < T) logits[size_t(t + 1) * E + e] = bias ? __fadd_rn(v[1], be) : v[1];
+    }
+  }
 }
-// 8 tokens x 4 experts per thread measured fastest at T = 4096, E = 256
-// (113 us with 128-token tiles, 117 us with 64; 8 x 8 and 4 x 4 per thread
-// were slower): the reads of x, shared by a thread's four neighbours with the
-// same tokens, dominate the shared-memory traffic.
-constexpr int kRgE = 64, kRgTT = 8, kRgTE = 4;
+constexpr bool kRtWdup = false, kRtXf = false;  // measured fastest: the extra shared-memory bytes cost more
 
 // Top-k of one token's logits (larger logit first, lower expert index on
 // ties) by one warp; lane l holds logits l, l+32, ... On return lane j < k
@@ -393,10 +437,8 @@ __global__ void __launch_bounds__(256)
 // token rows are staged; each lane then runs its fixed-order FMA chain.
 constexpr int kRouterSmallExperts = 2;
 
-// Token rows are staged D/8 + 1 16-byte words apart so that the tokens' reads
-// of one column fall in different banks.
 __host__ __device__ constexpr size_t router_small_smem(int TT, int D) {
-  return 16 + size_t(kRouterSmallExperts) * D * 4 + size_t(TT) * (D / 8 + 1) * 16;
+  return 16 + size_t(kRouterSmallExperts) * D * 4 + size_t(TT) * D * 2;
 }
 
 template <int TT>
@@ -409,6 +451,7 @@ __global__ void __launch_bounds__(kRouterSmallExperts * 32)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(rsm + 8);
   const float* ws = reinterpret_cast<const float*>(rsm + 16);
   uint4* xsm4 = reinterpret_cast<uint4*>(rsm + 16 + size_t(kRouterSmallExperts) * D * 4);
+  const uint16_t* xsm = reinterpret_cast<const uint16_t*>(xsm4);
   const int e0 = blockIdx.x * kRouterSmallExperts;
   const int ne = min(kRouterSmallExperts, E - e0);
   if (threadIdx.x == 0) {
@@ -424,32 +467,29 @@ __global__ void __launch_bounds__(kRouterSmallExperts * 32)
   }
   for (int i = threadIdx.x; i < TT * (D / 8); i += blockDim.x) {
     const int t = i / (D / 8), c8 = i % (D / 8);
-    xsm4[t * (D / 8 + 1) + c8] =
-        t < T ? *reinterpret_cast<const uint4*>(x + size_t(t) * D + c8 * 8) : make_uint4(0u, 0u, 0u, 0u);
+    xsm4[i] = t < T ? *reinterpret_cast<const uint4*>(x + size_t(t) * D + c8 * 8) : make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
   if (!mbar_wait(bar, 0, abort_flag, hdr, kWaitLimit, true)) return;
-  // thread (token t, expert el): one FMA chain over d, 8 columns per step
-  const int t = threadIdx.x % TT, el = threadIdx.x / TT;
-  if (el >= ne || t >= T) return;
-  const int e = e0 + el;
-  const float4* w4 = reinterpret_cast<const float4*>(ws + size_t(el) * D);
-  const uint4* x4 = xsm4 + size_t(t) * (D / 8 + 1);
-  float acc = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < D / 8; ++c) {
-    const uint4 xv = x4[c];
-    const float4 wa = w4[2 * c], wb = w4[2 * c + 1];
-    acc = fmaf(__uint_as_float(xv.x << 16), wa.x, acc);
-    acc = fmaf(__uint_as_float(xv.x & 0xFFFF0000u), wa.y, acc);
-    acc = fmaf(__uint_as_float(xv.y << 16), wa.z, acc);
-    acc = fmaf(__uint_as_float(xv.y & 0xFFFF0000u), wa.w, acc);
-    acc = fmaf(__uint_as_float(xv.z << 16), wb.x, acc);
-    acc = fmaf(__uint_as_float(xv.z & 0xFFFF0000u), wb.y, acc);
-    acc = fmaf(__uint_as_float(xv.w << 16), wb.z, acc);
-    acc = fmaf(__uint_as_float(xv.w & 0xFFFF0000u), wb.w, acc);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp >= ne) return;
+  const int e = e0 + warp;
+  const float* w = ws + size_t(warp) * D;
+  float acc[TT];
+#pragma unroll
+  for (int t = 0; t < TT; ++t) acc[t] = 0.f;
+  for (int c = 0; c < D / 32; ++c) {
+    const float wv = w[c * 32 + lane];
+#pragma unroll
+    for (int t = 0; t < TT; ++t) acc[t] = fmaf(bf16_to_f32(xsm[t * D + c * 32 + lane]), wv, acc[t]);
   }
-  logits[size_t(t) * E + e] = bias ? __fadd_rn(acc, bias[e]) : acc;
+#pragma unroll
+  for (int t = 0; t < TT; ++t) {
+    float a = acc[t];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) a = __fadd_rn(a, __shfl_down_sync(0xffffffffu, a, off));
+    if (lane == 0 && t < T) logits[size_t(t) * E + e] = bias ? __fadd_rn(a, bias[e]) : a;
+  }
 }
 
 // Top-k, weights, histogram, scan, scatter and block map of up to
@@ -559,16 +599,12 @@ cudaError_t route(const Ctx& c) {
     launch_done("route_small", c.stream);
     return cudaSuccess;
   }
-  if (c.T >= 4096) {  // 128-token tiles still fill the GPU
-    dim3 grid((c.T + 127) / 128, (c.E + kRgE - 1) / kRgE);
-    router_gemm_kernel<128, kRgE, kRgTT, kRgTE>
-        <<<grid, 128 * kRgE / (kRgTT * kRgTE), 0, c.stream>>>(c.x, w->router_w, w->router_bias, c.T, c.D, c.E,
-                                                              c.logits, c.hdr);
-  } else {
-    dim3 grid((c.T + 63) / 64, (c.E + kRgE - 1) / kRgE);
-    router_gemm_kernel<64, kRgE, kRgTT, kRgTE>
-        <<<grid, 64 * kRgE / (kRgTT * kRgTE), 0, c.stream>>>(c.x, w->router_w, w->router_bias, c.T, c.D, c.E,
-                                                             c.logits, c.hdr);
+  {
+    auto* rk = router_tree_kernel<kRtWdup, kRtXf>;
+    const size_t smem = rt_smem<kRtWdup, kRtXf>();
+    if (!ensure_smem_limit(reinterpret_cast<const void*>(rk), int(smem))) return cudaErrorInvalidValue;
+    rk<<<dim3((c.T + kRtTok - 1) / kRtTok, (c.E + kRtExp - 1) / kRtExp), kRtWarps * 32, smem, c.stream>>>(
+        c.x, w->router_w, w->router_bias, c.T, c.D, c.E, c.logits, c.hdr);
   }
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done("router_logits", c.stream);

@@ -135,16 +135,16 @@ def test_routing_ties_go_to_lower_index():
 
 
 @pytest.mark.parametrize("T", [3, 16, 70])
-def test_routing_logit_order_is_sequential(T):
-    # Rows whose fp32 result depends on the summation order (0 and D-2 for the
-    # same values in two orders): the kernels for small T and for larger T
-    # both evaluate one FMA chain in index order, like the oracle.
+def test_routing_logit_order_matches_the_canonical_tree(T):
+    # Rows whose fp32 logit depends on the summation order (the tree gives
+    # 254 and 247, one sequential chain 223 and 254): the kernels for small T
+    # and for larger T both follow the oracle's order bit for bit.
     layer = synth.make_layer(34, 256, 16, 4, 128)
     big = np.float32(2.0 ** 24)
     layer.router_w[0, :] = 1.0
-    layer.router_w[0, 0], layer.router_w[0, -1] = big, -big
+    layer.router_w[0, 0], layer.router_w[0, 32] = big, -big
     layer.router_w[5, :] = 1.0
-    layer.router_w[5, -2], layer.router_w[5, -1] = big, -big
+    layer.router_w[5, 0], layer.router_w[5, 1] = big, -big
     x = synth.f32_to_bf16_bits(np.ones((T, 256), np.float32))
     check_routing(layer, x, f"order{T}")
 
