@@ -654,7 +654,7 @@ bool gemm_wt_supported(const Ctx& c) {
 
 cudaError_t gemm_wt(const Ctx& c) {
   const moe_weights* w = c.w;
-  if (c.BM != kWtBlockRows) return cudaErrorInvalidValue;
+  if (c.BM < 1 || c.BM > kWtBlockRows) return cudaErrorInvalidValue;  // a tile takes one block of <= 192 rows
   if (!ensure_smem_limit(reinterpret_cast<const void*>(gemm_wt_kernel<true>), int(kSmemBytes)) ||
       !ensure_smem_limit(reinterpret_cast<const void*>(gemm_wt_kernel<false>), int(kSmemBytes)))
     return cudaErrorInvalidValue;

@@ -18,6 +18,7 @@ constexpr int kChunkTokens = 64;
 // Rows per block-map entry consumed by the tensor-core GEMMs.
 constexpr int kTcBlockRows = 128;  // weights dequantised into shared memory (MMA M = tokens)
 constexpr int kWtBlockRows = 192;  // weights dequantised into tensor memory (MMA N = tokens)
+constexpr int kMinBlockM = 16;      // smallest block size MOE_OPT_BLOCK_M accepts; sizes the block map
 
 // One call's resolved sizes and device pointers.
 struct Ctx {

@@ -22,6 +22,7 @@ struct Options {
   int kernel_timing = 0;
   int gemm_impl = 0;
   int test_wait_cycles = 0;
+  int block_m = 0;  // 0: the path's own block size
 };
 Options g_opt;
 std::mutex g_mu;
@@ -68,7 +69,8 @@ Layout layout(const moe_weights* w, int T) {
   const size_t A = size_t(T) * w->k;
   L.BM = kDefaultBlockM;
   L.n_chunks = (T + kChunkTokens - 1) / kChunkTokens;
-  L.max_blocks = int(A / L.BM + std::min<size_t>(w->E, A) + (T + L.BM - 1) / L.BM + 1);
+  // room for the smallest block size any path or option can use
+  L.max_blocks = int(A / kMinBlockM + std::min<size_t>(w->E, A) + (T + kMinBlockM - 1) / kMinBlockM + 1);
   size_t o = sizeof(WsHeader);
   auto put = [&](size_t bytes) {
     const size_t at = o;
@@ -184,7 +186,8 @@ Path plan(Ctx& c) {
     p = Path::GemmTc;
   else
     p = Path::GemmSimt;
-  c.BM = (p == Path::GemmWt) ? kWtBlockRows : (p == Path::GemmTc) ? kTcBlockRows : kDefaultBlockM;
+  const int path_bm = (p == Path::GemmWt) ? kWtBlockRows : (p == Path::GemmTc) ? kTcBlockRows : kDefaultBlockM;
+  c.BM = g_opt.block_m > 0 ? std::min(g_opt.block_m, path_bm) : path_bm;
   return p;
 }
 
@@ -324,6 +327,10 @@ moe_status moe_set_option(int option, int value) {
       if (value < 0 || value > 2) return MOE_ERR_ARG;
       g_opt.gemm_impl = value;
       return MOE_OK;
+    case MOE_OPT_BLOCK_M:
+      if (value != 0 && (value < kMinBlockM || value > kWtBlockRows || value % 16 != 0)) return MOE_ERR_ARG;
+      g_opt.block_m = value;
+      return MOE_OK;
     case MOE_OPT_TEST_WAIT_CYCLES:
       if (value < 0) return MOE_ERR_ARG;
       g_opt.test_wait_cycles = value;
@@ -341,6 +348,7 @@ int moe_get_option(int option) {
     case MOE_OPT_KERNEL_TIMING: return g_opt.kernel_timing;
     case MOE_OPT_GEMM_IMPL: return g_opt.gemm_impl;
     case MOE_OPT_TEST_WAIT_CYCLES: return g_opt.test_wait_cycles;
+    case MOE_OPT_BLOCK_M: return g_opt.block_m;
     default: return -1;
   }
 }

@@ -577,7 +577,8 @@ __global__ void __launch_bounds__(1024)
 cudaError_t route(const Ctx& c) {
   const moe_weights* w = c.w;
   cudaError_t err;
-  if (c.T <= kSmallRouteTokens && c.D <= 4096) {
+  // one CTA of 1024 threads does the small-T top-k: up to 16 logits per lane
+  if (c.T <= kSmallRouteTokens && c.D <= 4096 && c.E <= 512) {
     const int tt = c.T <= 2 ? 2 : c.T <= 8 ? 8 : 16;
     void (*rk)(const uint16_t*, const float*, const float*, int, int, int, float*, WsHeader*) =
         tt == 2 ? router_small_kernel<2> : tt == 8 ? router_small_kernel<8> : router_small_kernel<16>;
@@ -590,8 +591,7 @@ cudaError_t route(const Ctx& c) {
     const int mpl = (c.E + 31) / 32;
     void (*rs)(const float*, int, int, int, int, int, int32_t*, float*, int32_t*, int32_t*, int32_t*, int32_t*,
                int32_t*, int32_t*, WsHeader*) =
-        mpl <= 4 ? route_small_kernel<4> : mpl <= 8 ? route_small_kernel<8> : mpl <= 16 ? route_small_kernel<16>
-                                                                                    : route_small_kernel<32>;
+        mpl <= 4 ? route_small_kernel<4> : mpl <= 8 ? route_small_kernel<8> : route_small_kernel<16>;
     rs<<<1, 1024, 0, c.stream>>>(c.logits, c.T, c.E, c.k, c.BM, c.max_blocks, c.topk_idx,
                                                  c.topk_w, c.count, c.off, c.perm, c.inv, c.blocks, c.n_blocks,
                                                  c.hdr);

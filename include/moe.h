@@ -126,12 +126,18 @@ typedef enum {
                                 1 CUDA cores (the comparison baseline),
                                 2 tensor cores with the dequantised weights in
                                   shared memory */
-  MOE_OPT_TEST_WAIT_CYCLES = 5 /* test hook: > 0 makes the tensor-core epilogue
+  MOE_OPT_TEST_WAIT_CYCLES = 5, /* test hook: > 0 makes the tensor-core epilogue
                                 first wait, for at most this many cycles, on a
                                 barrier that nothing arrives on, so the
                                 bounded-wait failure path (status
                                 MOE_ERR_DEVICE_TIMEOUT, drain, clean exit) runs;
                                 0 (the default) turns the hook off */
+  MOE_OPT_BLOCK_M = 6        /* rows per block-map entry (the grouped GEMMs' token
+                                tile): 0 (default) uses the path's own size,
+                                192 on the tensor-memory path and 128 on the
+                                others; 16..192 in steps of 16 is clamped to
+                                the path's size. The workspace always has
+                                room for 16-row blocks. */
 } moe_option;
 
 /* Bytes of workspace one call with T tokens needs (pure host; 0 on bad

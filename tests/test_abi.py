@@ -100,6 +100,20 @@ def test_options(lib):
     moe.moe_set_option(moe.MOE_OPT_GEMV_MAX_ROWS, old)
 
 
+def test_block_m_option(lib):
+    old = moe.moe_get_option(moe.MOE_OPT_BLOCK_M)
+    for bad in (8, 17, 200, -16):
+        assert moe.moe_set_option(moe.MOE_OPT_BLOCK_M, bad) == moe.MOE_ERR_ARG, bad
+    w = _weights()
+    n0 = moe.moe_workspace_size(w, 300)
+    for good in (0, 16, 64, 192):
+        assert moe.moe_set_option(moe.MOE_OPT_BLOCK_M, good) == moe.MOE_OK
+        assert moe.moe_get_option(moe.MOE_OPT_BLOCK_M) == good
+        # the workspace is sized for the smallest block, whatever the option
+        assert moe.moe_workspace_size(w, 300) == n0
+    moe.moe_set_option(moe.MOE_OPT_BLOCK_M, old)
+
+
 def test_status_strings(lib):
     for s in range(7):
         assert moe.moe_status_string(s)

@@ -149,6 +149,32 @@ def test_routing_logit_order_matches_the_canonical_tree(T):
     check_routing(layer, x, f"order{T}")
 
 
+@pytest.mark.parametrize("bm", [16, 48, 192])
+def test_routing_block_size_option(bm):
+    layer = synth.make_layer(35, 256, 16, 4, 128)
+    assert moe.moe_set_option(moe.MOE_OPT_BLOCK_M, bm) == moe.MOE_OK
+    try:
+        tb = check_routing(layer, synth.make_x(35, 200, 256), f"bm{bm}")
+        assert tb["blocks"][:, 2].max() <= bm
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_BLOCK_M, 0)
+
+
+@pytest.mark.parametrize("impl", [moe.GEMM_TENSOR_CORE, moe.GEMM_TENSOR_CORE_SMEM, moe.GEMM_CUDA_CORE],
+                         ids=["tc", "tc_smem", "simt"])
+def test_layer_small_blocks(impl):
+    # 16- and 48-row blocks: many partly filled tiles on every GEMM path
+    layer, x = config("prefill512")
+    for bm in (16, 48):
+        assert moe.moe_set_option(moe.MOE_OPT_BLOCK_M, bm) == moe.MOE_OK
+        try:
+            y, ws = run_forward(dev_layer("prefill512", layer), x, moe.PATH_GEMM, impl)
+        finally:
+            moe.moe_set_option(moe.MOE_OPT_BLOCK_M, 0)
+        toks = np.arange(0, x.shape[0], 7)
+        check_output(y[toks], O.forward(O.OracleLayer(layer), x, tokens=toks), f"prefill512 bm={bm} impl={impl}")
+
+
 def test_routing_all_equal_logits():
     layer = synth.make_layer(33, 128, 8, 8, 64)
     layer.router_w[:] = 0
