@@ -4,18 +4,18 @@
 // traffic"; the switch to matrix kernels above a row count follows
 // "Why continuous batching halved LLM throughput on an M2 Mac mini").
 //
-//   gemv_gateup: a CTA owns 32 consecutive intermediate rows of one expert
+//   gemv_gateup: a CTA owns 16 consecutive intermediate rows of one expert
 //     block. Their gate and up codes, scales and biases are contiguous in
 //     memory, so one thread fetches all of them into shared memory with six
 //     bulk (TMA) copies on one mbarrier while the CTA stages every token row
-//     (they do not depend on the routing). A warp takes four rows: per
-//     32-code chunk it loads the activations once and runs eight independent
+//     (they do not depend on the routing). A warp takes two rows: per
+//     32-code chunk it loads the activations once and runs four independent
 //     dot products (gate and up of each row); then h = bf16(silu(g) * u) in
 //     the permuted order.
-//   gemv_down: a CTA owns 16 output columns of one token. It bulk-copies the
-//     16 rows of the down matrix of each of the token's k experts and of the
+//   gemv_down: a CTA owns 8 output columns of one token. It bulk-copies the
+//     8 rows of the down matrix of each of the token's k experts and of the
 //     shared expert and stages the token's k+1 h rows. A thread takes one
-//     (expert slot, 32-code chunk) item and adds w_j * (h_j . row) for all 16
+//     (expert slot, 32-code chunk) item and adds w_j * (h_j . row) for all 8
 //     columns; lanes and warps are then summed in a fixed order, y = bf16(sum).
 //     No atomics: deterministic.
 //
@@ -34,18 +34,21 @@
 // Lane l works on chunk c = l + 32m, so the lanes of a warp read consecutive
 // float4s and consecutive 16-byte code chunks (no bank conflicts).
 #include <algorithm>
+#include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kMaxGemvRows = 8;
 constexpr int kGemvWarps = 8;
-constexpr int kGateupRows = 32;  // intermediate rows per gate/up CTA
-constexpr int kDownCols = 16;    // output columns per down CTA
+constexpr int kGateupRows = 16;  // intermediate rows per gate/up CTA
+constexpr int kDownCols = 8;     // output columns per down CTA
 
 // fp32 value 128 + q of the nibble in bits 16..19 of w_shifted.
 __device__ __forceinline__ float q128(uint32_t w_shifted) {
@@ -339,6 +342,296 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_down_kernel(GemvArgs a) 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Fused decode for one token: top-k, gate/up + SwiGLU and down + combine in
+// one cooperative kernel after the router logits. Every CTA takes the top-k
+// of the 256 logits itself (the same deterministic selection), so no grid-wide
+// step separates the routing from the weight reads: each CTA at once bulk-
+// copies its two gate/up items (expert slot x 16 intermediate rows) and the
+// down rows of its 16 output columns for all k+1 slots, computes its h rows,
+// waits at one grid barrier for the other CTAs' h, and finishes its columns.
+// Slot j < k is the token's j-th expert, slot k the shared expert.
+constexpr int kFdRows = 16;  // intermediate rows per gate/up item
+constexpr int kFdCols = 16;  // output columns per down group
+constexpr int kFdWarps = 8;
+
+struct FusedSmem {
+  size_t xs4, xsum, item[2], down, dsc, dbi, hs4, hsum, red, total;
+  size_t item_codes, item_sb;  // bytes of one matrix's codes / scales of an item
+  __host__ __device__ FusedSmem(int D, int I, int k) {
+    const size_t S = size_t(k) + 1;
+    item_codes = size_t(kFdRows) * D / 2;
+    item_sb = size_t(kFdRows) * (D / 64) * 2;
+    xs4 = 64;  // bytes 0..63: three mbarriers, abort flag, grid-barrier result
+    xsum = xs4 + size_t(D) * 4;
+    item[0] = (xsum + size_t(D / 32) * 4 + 127) & ~size_t(127);
+    item[1] = item[0] + 2 * item_codes + 4 * item_sb;
+    down = (item[1] + 2 * item_codes + 4 * item_sb + 127) & ~size_t(127);
+    dsc = down + S * kFdCols * (I / 2);
+    dbi = dsc + S * kFdCols * (I / 64) * 2;
+    hs4 = (dbi + S * kFdCols * (I / 64) * 2 + 15) & ~size_t(15);
+    hsum = hs4 + S * size_t(I) * 4;
+    red = hsum + S * size_t(I / 32) * 4;
+    total = red + size_t(kFdWarps) * kFdCols * 4;
+  }
+};
+
+struct FusedArgs {
+  const uint16_t* x;
+  moe_qmatrix gate, up, down, s_gate, s_up, s_down;
+  const float* logits;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* count;
+  int32_t* off;
+  int32_t* perm;
+  int32_t* inv;
+  int32_t* blocks;
+  int32_t* n_blocks;
+  uint16_t* h;  // [k+1][I]: slot-major for the one token
+  uint16_t* y;
+  WsHeader* hdr;
+  int D, E, k, I;
+  int n_items, n_groups;
+};
+
+// Grid-wide barrier of a cooperative launch: every CTA arrives once on the
+// header's counter (zeroed by the router kernel before this launch) and waits,
+// for at most kWaitLimit cycles, until all have. Returns false on expiry
+// (MOE_ERR_DEVICE_TIMEOUT recorded).
+__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned target, volatile int* result) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&hdr->counter, 1u);
+    const long long t0 = clock64();
+    int ok = 1;
+    while (true) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(&hdr->counter) : "memory");
+      if (v >= target) break;
+      if (clock64() - t0 > kWaitLimit) {
+        report(hdr, MOE_ERR_DEVICE_TIMEOUT, 110);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    *result = ok;
+  }
+  __syncthreads();
+  return *result != 0;
+}
+
+template <int MPL>
+__global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArgs a) {
+  extern __shared__ __align__(128) uint8_t fsm[];
+  __shared__ int s_exp[kMaxGemvRows * 8 + 1];
+  __shared__ float s_w[kMaxGemvRows * 8 + 1];
+  const int D = a.D, I = a.I, k = a.k, E = a.E, S = k + 1, nch = D / 32, G = D / 64, Gi = I / 64;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const FusedSmem L(D, I, k);
+  const uint32_t bar0 = smem_u32(fsm);  // item 0, item 1, down
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(fsm + 24);
+  volatile int* gb_result = reinterpret_cast<volatile int*>(fsm + 28);
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < 3; ++i) mbar_init(bar0 + 8u * i, 1);
+    mbar_init_fence();
+  }
+  // the token row, chunk-major fp32, staged while the logits are read
+  float4* xs4 = reinterpret_cast<float4*>(fsm + L.xs4);
+  float* xsum = reinterpret_cast<float*>(fsm + L.xsum);
+  for (int q = threadIdx.x; q < D / 8; q += blockDim.x)
+    stage_bf16x8(xs4, nch, q, *reinterpret_cast<const uint4*>(a.x + size_t(q) * 8));
+  if (warp == 0) {
+    int myi;
+    float myw;
+    select_topk<MPL>(a.logits, E, k, myi, myw);
+    if (lane < k) {
+      s_exp[lane] = myi;
+      s_w[lane] = myw;
+      if (blockIdx.x == 0) {
+        a.topk_idx[lane] = myi;
+        a.topk_w[lane] = myw;
+      }
+    }
+    if (lane == 0) {
+      s_exp[k] = E;
+      s_w[k] = 1.f;
+    }
+  }
+  __syncthreads();
+  if (blockIdx.x == 0)  // the routing tables of one token, for the workspace view
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int slot = -1, below = 0;
+    for (int j = 0; j < k; ++j) {
+      slot = (s_exp[j] == e) ? j : slot;
+      below += s_exp[j] < e;
+    }
+    a.count[e] = slot >= 0;
+    a.off[e] = below;
+    if (e == E - 1) a.off[E] = k;
+    if (slot >= 0) {
+      a.perm[below] = slot;
+      a.inv[slot] = below;
+      a.blocks[3 * below] = e;
+      a.blocks[3 * below + 1] = below;
+      a.blocks[3 * below + 2] = 1;
+    }
+    if (e == 0) {
+      a.blocks[3 * k] = E;
+      a.blocks[3 * k + 1] = k;
+      a.blocks[3 * k + 2] = 1;
+      *a.n_blocks = k + 1;
+    }
+  }
+  const int RB = I / kFdRows;  // row blocks per slot
+  const bool has_down = blockIdx.x < a.n_groups;
+  const int d0 = blockIdx.x * kFdCols;
+  if (threadIdx.x == 0) {  // every weight this CTA needs, at once
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const int item = blockIdx.x + m * gridDim.x;
+      if (item >= a.n_items) continue;
+      const int slot = item / RB, i0 = (item % RB) * kFdRows, e = s_exp[slot];
+      const bool sh = (e == E);
+      const moe_qmatrix mg = sh ? a.s_gate : a.gate, mu = sh ? a.s_up : a.up;
+      const size_t row0 = size_t(sh ? 0 : e) * I + i0;
+      const uint32_t cb = uint32_t(L.item_codes), sbb = uint32_t(L.item_sb);
+      const uint32_t dst = bar0 + uint32_t(L.item[m]), bar = bar0 + 8u * m;
+      mbar_arrive_tx(bar, 2 * cb + 4 * sbb);
+      bulk_g2s(dst, mg.codes + row0 * (D / 8), cb, bar);
+      bulk_g2s(dst + cb, mu.codes + row0 * (D / 8), cb, bar);
+      bulk_g2s(dst + 2 * cb, mg.scales + row0 * G, sbb, bar);
+      bulk_g2s(dst + 2 * cb + sbb, mg.biases + row0 * G, sbb, bar);
+      bulk_g2s(dst + 2 * cb + 2 * sbb, mu.scales + row0 * G, sbb, bar);
+      bulk_g2s(dst + 2 * cb + 3 * sbb, mu.biases + row0 * G, sbb, bar);
+    }
+    if (has_down) {
+      const uint32_t cb = kFdCols * (I / 2), sbb = kFdCols * Gi * 2, bar = bar0 + 16u;
+      mbar_arrive_tx(bar, uint32_t(S) * (cb + 2 * sbb));
+      for (int j = 0; j < S; ++j) {
+        const int e = s_exp[j];
+        const bool sh = (e == E);
+        const moe_qmatrix m = sh ? a.s_down : a.down;
+        const size_t row0 = size_t(sh ? 0 : e) * D + d0;
+        bulk_g2s(bar0 + uint32_t(L.down) + j * cb, m.codes + row0 * (I / 8), cb, bar);
+        bulk_g2s(bar0 + uint32_t(L.dsc) + j * sbb, m.scales + row0 * Gi, sbb, bar);
+        bulk_g2s(bar0 + uint32_t(L.dbi) + j * sbb, m.biases + row0 * Gi, sbb, bar);
+      }
+    }
+  }
+  chunk_sums(xs4, xsum, 1, nch);
+  __syncthreads();
+
+  // gate/up: warp w takes rows w and w+8 of each item
+  bool ok = true;
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const int item = blockIdx.x + m * gridDim.x;
+    if (item >= a.n_items) continue;
+    if (!mbar_wait(bar0 + 8u * m, 0, abort_flag, a.hdr, kWaitLimit, true)) {
+      ok = false;
+      continue;
+    }
+    const int slot = item / RB, i0 = (item % RB) * kFdRows;
+    const uint8_t* base = fsm + L.item[m];
+    const uint8_t* cg = base;
+    const uint8_t* cu = base + L.item_codes;
+    const uint16_t* sg = reinterpret_cast<const uint16_t*>(base + 2 * L.item_codes);
+    const uint16_t* bg = sg + kFdRows * G;
+    const uint16_t* su = bg + kFdRows * G;
+    const uint16_t* bu = su + kFdRows * G;
+    constexpr int kRowsPerWarp = kFdRows / kFdWarps;
+    float gacc[kRowsPerWarp], uacc[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) gacc[i] = uacc[i] = 0.f;
+    for (int c = lane; c < nch; c += 32) {
+      float4 xv[8];
+#pragma unroll
+      for (int jq = 0; jq < 8; ++jq) xv[jq] = xs4[jq * nch + c];
+      const float sx = xsum[c];
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int rr = warp + kFdWarps * i;
+        const uint4 wg = reinterpret_cast<const uint4*>(cg + size_t(rr) * D / 2)[c];
+        const uint4 wu = reinterpret_cast<const uint4*>(cu + size_t(rr) * D / 2)[c];
+        const int gi = rr * G + c / 2;
+        gacc[i] += chunk_dot_r(wg, xv, sx, sg[gi], bg[gi]);
+        uacc[i] += chunk_dot_r(wu, xv, sx, su[gi], bu[gi]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        gacc[i] += __shfl_xor_sync(0xffffffffu, gacc[i], off);
+        uacc[i] += __shfl_xor_sync(0xffffffffu, uacc[i], off);
+      }
+      if (lane == 0) a.h[size_t(slot) * I + i0 + warp + kFdWarps * i] = f32_to_bf16(silu_mul(gacc[i], uacc[i]));
+    }
+  }
+
+  // every CTA's h rows are written: the down projection may read them
+  const bool gb_ok = grid_barrier(a.hdr, gridDim.x, gb_result);
+  if (!has_down) return;
+  const uint32_t dbar = bar0 + 16u;
+  if (!ok || !gb_ok) {  // drain the down copies before leaving
+    mbar_wait(dbar, 0, abort_flag, a.hdr, kWaitLimit, true);
+    return;
+  }
+  float4* hs4 = reinterpret_cast<float4*>(fsm + L.hs4);
+  float* hsum = reinterpret_cast<float*>(fsm + L.hsum);
+  const int nchi = I / 32;
+  for (int q = threadIdx.x; q < S * (I / 8); q += blockDim.x) {
+    const int j = q / (I / 8), q8 = q % (I / 8);
+    stage_bf16x8(hs4 + size_t(j) * 8 * nchi, nchi, q8, __ldcg(reinterpret_cast<const uint4*>(a.h + size_t(j) * I) + q8));
+  }
+  __syncthreads();
+  chunk_sums(hs4, hsum, S, nchi);
+  __syncthreads();
+  if (!mbar_wait(dbar, 0, abort_flag, a.hdr, kWaitLimit, true)) return;
+  const uint8_t* codes = fsm + L.down;
+  const uint16_t* sc = reinterpret_cast<const uint16_t*>(fsm + L.dsc);
+  const uint16_t* bi = reinterpret_cast<const uint16_t*>(fsm + L.dbi);
+  float part[kFdCols];
+#pragma unroll
+  for (int cl = 0; cl < kFdCols; ++cl) part[cl] = 0.f;
+  for (int it = threadIdx.x; it < S * nchi; it += blockDim.x) {
+    const int j = it / nchi, c = it % nchi;
+    float4 xv[8];
+    const float4* xr = hs4 + size_t(j) * 8 * nchi;
+#pragma unroll
+    for (int jq = 0; jq < 8; ++jq) xv[jq] = xr[jq * nchi + c];
+    const float sx = hsum[j * nchi + c], wj = s_w[j];
+#pragma unroll
+    for (int cl = 0; cl < kFdCols; ++cl) {
+      const int rowi = j * kFdCols + cl;
+      const uint4 w4 = reinterpret_cast<const uint4*>(codes + size_t(rowi) * (I / 2))[c];
+      const int gi = rowi * Gi + c / 2;
+      part[cl] += wj * chunk_dot_r(w4, xv, sx, sc[gi], bi[gi]);
+    }
+  }
+  float* red = reinterpret_cast<float*>(fsm + L.red);
+#pragma unroll
+  for (int cl = 0; cl < kFdCols; ++cl) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) part[cl] += __shfl_xor_sync(0xffffffffu, part[cl], off);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int cl = 0; cl < kFdCols; ++cl) red[warp * kFdCols + cl] = part[cl];
+  }
+  __syncthreads();
+  if (threadIdx.x < kFdCols) {
+    float yv = 0.f;
+#pragma unroll
+    for (int w = 0; w < kFdWarps; ++w) yv += red[w * kFdCols + threadIdx.x];
+    a.y[d0 + threadIdx.x] = f32_to_bf16(yv);
+  }
+}
+
 }  // namespace
 
 bool gemv_supported(const Ctx& c) {
@@ -362,6 +655,79 @@ cudaError_t gemv(const Ctx& c) {
   gemv_down_kernel<<<dim3(c.D / kDownCols, c.T), kGemvWarps * 32, s2, c.stream>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done("gemv_down", c.stream);
+  return cudaSuccess;
+}
+
+namespace {
+
+struct FusedPlan {
+  int grid = 0, n_items = 0, n_groups = 0, mpl = 0;
+  size_t smem = 0;
+};
+
+// Launch shape of the fused decode for this layer, or grid 0 when it does not
+// apply (more than one token, shared memory, too many logits per lane, or not
+// all CTAs co-resident).
+FusedPlan fused_plan_uncached(const Ctx& c) {
+  FusedPlan p;
+  if (c.T != 1 || c.I % kFdRows != 0 || c.D % kFdCols != 0 || c.E > 512 || c.k + 1 > kMaxGemvRows * 8 + 1)
+    return p;
+  p.mpl = (c.E + 31) / 32 <= 8 ? 8 : 16;
+  p.smem = FusedSmem(c.D, c.I, c.k).total;
+  if (p.smem > 227 * 1024) return p;
+  p.n_items = (c.k + 1) * (c.I / kFdRows);
+  p.n_groups = c.D / kFdCols;
+  const int grid = std::max(p.n_groups, (p.n_items + 1) / 2);
+  int dev = 0, coop = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return p;
+  const void* f = p.mpl == 8 ? reinterpret_cast<const void*>(decode_fused_kernel<8>)
+                             : reinterpret_cast<const void*>(decode_fused_kernel<16>);
+  if (!ensure_smem_limit(f, int(p.smem)) ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f, kFdWarps * 32, p.smem) != cudaSuccess)
+    return p;
+  if (grid > per_sm * sms) return p;
+  p.grid = grid;
+  return p;
+}
+
+// The plan depends on the device and the layer shape only: computed once.
+FusedPlan fused_plan(const Ctx& c) {
+  struct Entry {
+    int dev, T, D, I, k, E;
+    FusedPlan p;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FusedPlan{};
+  std::lock_guard<std::mutex> lk(mu);
+  for (const Entry& e : cache)
+    if (e.dev == dev && e.T == c.T && e.D == c.D && e.I == c.I && e.k == c.k && e.E == c.E) return e.p;
+  const FusedPlan p = fused_plan_uncached(c);
+  cache.push_back({dev, c.T, c.D, c.I, c.k, c.E, p});
+  return p;
+}
+
+}  // namespace
+
+bool decode_fused_supported(const Ctx& c) { return fused_plan(c).grid > 0; }
+
+cudaError_t decode_fused(const Ctx& c) {
+  const FusedPlan p = fused_plan(c);
+  if (p.grid == 0) return cudaErrorInvalidValue;
+  const moe_weights* w = c.w;
+  FusedArgs a{c.x,     w->gate, w->up,     w->down,  w->s_gate, w->s_up, w->s_down, c.logits, c.topk_idx,
+              c.topk_w, c.count, c.off,    c.perm,   c.inv,     c.blocks, c.n_blocks, c.h,     c.y,
+              c.hdr,   c.D,     c.E,       c.k,      c.I,       p.n_items, p.n_groups};
+  void* args[] = {&a};
+  const void* f = p.mpl == 8 ? reinterpret_cast<const void*>(decode_fused_kernel<8>)
+                             : reinterpret_cast<const void*>(decode_fused_kernel<16>);
+  cudaError_t err = cudaLaunchCooperativeKernel(f, dim3(p.grid), dim3(kFdWarps * 32), args, p.smem, c.stream);
+  if (err != cudaSuccess) return err;
+  launch_done("decode_fused", c.stream);
   return cudaSuccess;
 }
 

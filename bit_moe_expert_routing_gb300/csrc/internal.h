@@ -77,6 +77,12 @@ bool tmap_encoder_available();
 // Decode GEMV path (a few rows).
 cudaError_t gemv(const Ctx& c);
 bool gemv_supported(const Ctx& c);
+// One token: top-k, gate/up and down in one cooperative kernel after the
+// router logits (route_logits_small).
+cudaError_t decode_fused(const Ctx& c);
+bool decode_fused_supported(const Ctx& c);
+// Router logits only, for up to 16 tokens; also zeroes the header counter.
+cudaError_t route_logits_small(const Ctx& c);
 
 cudaError_t debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, uint16_t* out,
                           cudaStream_t s);

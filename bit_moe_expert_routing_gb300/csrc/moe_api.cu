@@ -23,6 +23,7 @@ struct Options {
   int gemm_impl = 0;
   int test_wait_cycles = 0;
   int block_m = 0;  // 0: the path's own block size
+  int decode_fused = 1;
 };
 Options g_opt;
 std::mutex g_mu;
@@ -169,7 +170,7 @@ void fill_view(const Ctx& c, moe_route_view* v) {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-enum class Path { Gemv, GemmWt, GemmTc, GemmSimt };
+enum class Path { DecodeFused, Gemv, GemmWt, GemmTc, GemmSimt };
 
 // Chooses the expert path for this call and the block-map row count it
 // consumes: 192 tokens per block for the tensor-core GEMM with weights in
@@ -179,7 +180,7 @@ Path plan(Ctx& c) {
   if (path == 0) path = (c.T <= g_opt.gemv_max_rows) ? 1 : 2;
   Path p;
   if (path == 1 && gemv_supported(c))
-    p = Path::Gemv;
+    p = (g_opt.decode_fused && decode_fused_supported(c)) ? Path::DecodeFused : Path::Gemv;
   else if (g_opt.gemm_impl == 0 && gemm_wt_supported(c))
     p = Path::GemmWt;
   else if (g_opt.gemm_impl == 2 && gemm_tc_supported(c))
@@ -268,9 +269,10 @@ moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uin
   if (!x || !y || !aligned16(x) || !aligned16(y) || x == y) return MOE_ERR_ARG;
   const Path path = plan(c);
   timing_begin(c.stream);
-  cudaError_t err = route(c);
+  cudaError_t err = (path == Path::DecodeFused) ? route_logits_small(c) : route(c);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (path == Path::Gemv) return cuda_status(gemv(c));
+  if (path == Path::DecodeFused) return cuda_status(decode_fused(c));
   if (path == Path::GemmWt) return cuda_status(gemm_wt(c));
   if (path == Path::GemmTc) return cuda_status(gemm_tc(c));
   return cuda_status(gemm_simt(c));
@@ -327,6 +329,10 @@ moe_status moe_set_option(int option, int value) {
       if (value < 0 || value > 2) return MOE_ERR_ARG;
       g_opt.gemm_impl = value;
       return MOE_OK;
+    case MOE_OPT_DECODE_FUSED:
+      if (value < 0 || value > 1) return MOE_ERR_ARG;
+      g_opt.decode_fused = value;
+      return MOE_OK;
     case MOE_OPT_BLOCK_M:
       if (value != 0 && (value < kMinBlockM || value > kWtBlockRows || value % 16 != 0)) return MOE_ERR_ARG;
       g_opt.block_m = value;
@@ -349,6 +355,7 @@ int moe_get_option(int option) {
     case MOE_OPT_GEMM_IMPL: return g_opt.gemm_impl;
     case MOE_OPT_TEST_WAIT_CYCLES: return g_opt.test_wait_cycles;
     case MOE_OPT_BLOCK_M: return g_opt.block_m;
+    case MOE_OPT_DECODE_FUSED: return g_opt.decode_fused;
     default: return -1;
   }
 }

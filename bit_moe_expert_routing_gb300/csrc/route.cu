@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -54,6 +55,7 @@ __global__ void __launch_bounds__(kRtWarps * 32, 1)
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     hdr->status = 0;
     hdr->detail = 0;
+    hdr->counter = 0;
   }
   extern __shared__ __align__(16) uint8_t rt_smem_raw[];
   uint8_t* wsb = rt_smem_raw;                            // [2][kRtExp][kRtDC] of float or float2
@@ -213,59 +215,6 @@ __global__ void __launch_bounds__(kRtWarps * 32, 1)
   }
 }
 constexpr bool kRtWdup = false, kRtXf = false;  // measured fastest: the extra shared-memory bytes cost more
-
-// Top-k of one token's logits (larger logit first, lower expert index on
-// ties) by one warp; lane l holds logits l, l+32, ... On return lane j < k
-// holds slot j: its expert and its weight, the softmax renormalised over the
-// k kept, exp(l_j - l_max) / sum.
-// MPL >= ceil(E / 32) logits per lane (E <= 1024).
-template <int MPL>
-__device__ __forceinline__ void select_topk(const float* __restrict__ lg, int E, int k, int& myi, float& myw) {
-  const int lane = threadIdx.x & 31;
-  const int M = (E + 31) / 32;
-  float v[MPL];
-  unsigned taken = 0;
-#pragma unroll
-  for (int m = 0; m < MPL; ++m) {
-    const int e = lane + 32 * m;
-    v[m] = (m < M && e < E) ? lg[e] : 0.f;
-    if (!(m < M && e < E)) taken |= 1u << m;
-  }
-  float first = 0.f, myv = 0.f;
-  myi = 0;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = INT_MAX;
-#pragma unroll
-    for (int m = 0; m < MPL; ++m) {
-      const int e = lane + 32 * m;
-      if (!((taken >> m) & 1u) && (v[m] > bv || (v[m] == bv && e < bi))) {
-        bv = v[m];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (j == 0) first = bv;
-    if (lane == j) {
-      myv = bv;
-      myi = bi;
-    }
-  }
-  const float ex = lane < k ? expf(myv - first) : 0.f;
-  float sum = ex;
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-  myw = ex / sum;
-}
 
 // Top-k and weights of each token of a chunk, and the chunk's per-expert
 // assignment counts. One warp per token.
@@ -458,6 +407,7 @@ __global__ void __launch_bounds__(kRouterSmallExperts * 32)
     if (blockIdx.x == 0) {  // first kernel of the call: start its status afresh
       hdr->status = 0;
       hdr->detail = 0;
+      hdr->counter = 0;  // the fused decode's grid barrier counts from here
     }
     *abort_flag = 0;
     mbar_init(bar, 1);
@@ -574,20 +524,28 @@ __global__ void __launch_bounds__(1024)
 
 }  // namespace
 
+cudaError_t route_logits_small(const Ctx& c) {
+  const moe_weights* w = c.w;
+  if (c.T > kSmallRouteTokens || c.D > 4096) return cudaErrorInvalidValue;
+  const int tt = c.T <= 2 ? 2 : c.T <= 8 ? 8 : 16;
+  void (*rk)(const uint16_t*, const float*, const float*, int, int, int, float*, WsHeader*) =
+      tt == 2 ? router_small_kernel<2> : tt == 8 ? router_small_kernel<8> : router_small_kernel<16>;
+  const size_t smem = router_small_smem(tt, c.D);
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(rk), int(smem))) return cudaErrorInvalidValue;
+  rk<<<(c.E + kRouterSmallExperts - 1) / kRouterSmallExperts, kRouterSmallExperts * 32, smem, c.stream>>>(
+      c.x, w->router_w, w->router_bias, c.T, c.D, c.E, c.logits, c.hdr);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  launch_done("router_small", c.stream);
+  return cudaSuccess;
+}
+
 cudaError_t route(const Ctx& c) {
   const moe_weights* w = c.w;
   cudaError_t err;
   // one CTA of 1024 threads does the small-T top-k: up to 16 logits per lane
   if (c.T <= kSmallRouteTokens && c.D <= 4096 && c.E <= 512) {
-    const int tt = c.T <= 2 ? 2 : c.T <= 8 ? 8 : 16;
-    void (*rk)(const uint16_t*, const float*, const float*, int, int, int, float*, WsHeader*) =
-        tt == 2 ? router_small_kernel<2> : tt == 8 ? router_small_kernel<8> : router_small_kernel<16>;
-    const size_t smem = router_small_smem(tt, c.D);
-    if (!ensure_smem_limit(reinterpret_cast<const void*>(rk), int(smem))) return cudaErrorInvalidValue;
-    rk<<<(c.E + kRouterSmallExperts - 1) / kRouterSmallExperts, kRouterSmallExperts * 32, smem, c.stream>>>(
-        c.x, w->router_w, w->router_bias, c.T, c.D, c.E, c.logits, c.hdr);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    launch_done("router_small", c.stream);
+    if ((err = route_logits_small(c)) != cudaSuccess) return err;
     const int mpl = (c.E + 31) / 32;
     void (*rs)(const float*, int, int, int, int, int, int32_t*, float*, int32_t*, int32_t*, int32_t*, int32_t*,
                int32_t*, int32_t*, WsHeader*) =

@@ -132,12 +132,17 @@ typedef enum {
                                 bounded-wait failure path (status
                                 MOE_ERR_DEVICE_TIMEOUT, drain, clean exit) runs;
                                 0 (the default) turns the hook off */
-  MOE_OPT_BLOCK_M = 6        /* rows per block-map entry (the grouped GEMMs' token
+  MOE_OPT_BLOCK_M = 6,       /* rows per block-map entry (the grouped GEMMs' token
                                 tile): 0 (default) uses the path's own size,
                                 192 on the tensor-memory path and 128 on the
                                 others; 16..192 in steps of 16 is clamped to
                                 the path's size. The workspace always has
                                 room for 16-row blocks. */
+  MOE_OPT_DECODE_FUSED = 7   /* 1 (default): one token on the GEMV path runs top-k,
+                                gate/up and down in one cooperative kernel after
+                                the router logits (when the device can hold all
+                                its CTAs at once); 0: the separate routing and
+                                GEMV kernels */
 } moe_option;
 
 /* Bytes of workspace one call with T tokens needs (pure host; 0 on bad

@@ -206,6 +206,34 @@ def test_layer_decode(path):
     check_output(y, O.forward(O.OracleLayer(layer), x), f"decode {path[0]}")
 
 
+@pytest.mark.parametrize("fused", [0, 1], ids=["separate", "fused"])
+def test_layer_decode_fused_and_separate(fused):
+    # one token on the GEMV path: the cooperative kernel (top-k, gate/up, grid
+    # barrier, down) and the separate routing + GEMV kernels, both against the oracle
+    layer, x = config("decode")
+    assert moe.moe_set_option(moe.MOE_OPT_DECODE_FUSED, fused) == moe.MOE_OK
+    try:
+        dl = dev_layer("decode", layer)
+        y, ws = run_forward(dl, x, moe.PATH_GEMV)
+        launches = moe.moe_last_launch_count()
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_DECODE_FUSED, 1)
+    ol = O.OracleLayer(layer)
+    check_output(y, O.forward(ol, x), f"decode fused={fused}")
+    assert launches == (2 if fused else 4)
+    # the routing tables in the workspace agree with the oracle either way
+    v = dl.view(1, ws)
+    g = lambda p_, shape, dt: moe.ws_tensor(ws, p_, shape, dt).cpu().numpy()
+    _, idx, w = O.route(ol, x)
+    tb = O.route_tables(idx, layer.E, v.block_m)
+    assert np.array_equal(g(v.topk_idx, (1, layer.k), torch.int32), idx)
+    assert np.abs(g(v.topk_w, (1, layer.k), torch.float32) - w).max() <= WEIGHT_ATOL
+    assert np.array_equal(g(v.perm, (layer.k,), torch.int32), tb["perm"])
+    assert np.array_equal(g(v.count, (layer.E,), torch.int32), tb["count"])
+    nb = int(g(v.n_blocks, (1,), torch.int32)[0])
+    assert np.array_equal(g(v.blocks, (v.max_blocks, 3), torch.int32)[:nb], tb["blocks"])
+
+
 @pytest.mark.parametrize("path", PATHS, ids=[p[0] for p in PATHS])
 @pytest.mark.parametrize("T", synth.SWEEP_T)
 def test_layer_crossover_sweep(path, T):
