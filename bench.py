@@ -418,12 +418,14 @@ def run_decode(args, moe, synth, torch, device, stream, peaks) -> dict:
     med = lambda m: m[len(m) // 2]
     us, us_g = 1e3 * med(ms), 1e3 * med(ms_g)
     kern = {nm: dict(ms_per_launch=t / c, launches=c) for nm, (t, c) in kt.items()}
-    gemv_ms = sum(kern[nm]["ms_per_launch"] for nm in ("gemv_gateup", "gemv_down") if nm in kern)
+    # the fused one-token kernel when it ran, else the two GEMV kernels
+    names = ("decode_fused",) if "decode_fused" in kern else ("gemv_gateup", "gemv_down")
+    gemv_ms = sum(kern[nm]["ms_per_launch"] for nm in names if nm in kern)
     ach = work["weight_bytes"] / (gemv_ms / 1e3) / 1e9 if gemv_ms else None
     return {"us_per_token": us_g, "us_per_token_stream": us, "us_p95_stream": 1e3 * ms[int(0.95 * (n - 1))],
             "us_p95": 1e3 * ms_g[int(0.95 * (n - 1))], "steps": n, "tokens_per_s": 1e6 / us_g,
             "launches_per_step": launches,
-            "roofline": dict(kernel="gemv_gateup+gemv_down", bound="hbm", achieved=ach, peak=peaks["hbm_gbs"],
+            "roofline": dict(kernel="+".join(names), bound="hbm", achieved=ach, peak=peaks["hbm_gbs"],
                              unit="GB/s", frac=(ach / peaks["hbm_gbs"]) if ach else None, traffic=None,
                              bytes_per_launch=work["weight_bytes"],
                              peak_source=f"{peaks['source']} copy"),

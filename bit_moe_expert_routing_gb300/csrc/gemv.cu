@@ -343,28 +343,36 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_down_kernel(GemvArgs a) 
 }
 
 // ---------------------------------------------------------------------------
-// Fused decode for one token: top-k, gate/up + SwiGLU and down + combine in
-// one cooperative kernel after the router logits. Every CTA takes the top-k
-// of the 256 logits itself (the same deterministic selection), so no grid-wide
-// step separates the routing from the weight reads: each CTA at once bulk-
-// copies its two gate/up items (expert slot x 16 intermediate rows) and the
-// down rows of its 16 output columns for all k+1 slots, computes its h rows,
-// waits at one grid barrier for the other CTAs' h, and finishes its columns.
+// Fused decode for one token: router logits, top-k, gate/up + SwiGLU and
+// down + combine in one cooperative kernel.
+//   1. At once: each CTA bulk-copies its router rows (experts blockIdx.x +
+//      m * gridDim.x) and every weight that does not depend on the routing
+//      (the shared expert's gate/up items and down rows), and stages x.
+//   2. Logits of its experts in the canonical order; grid barrier.
+//   3. Every CTA takes the top-k of all logits itself (the same deterministic
+//      selection), then copies the routed experts' rows of its two gate/up
+//      items (expert slot x 16 intermediate rows) and of its 16 output
+//      columns; computes its h rows; grid barrier.
+//   4. Its 16 columns of y from all k+1 slots.
 // Slot j < k is the token's j-th expert, slot k the shared expert.
 constexpr int kFdRows = 16;  // intermediate rows per gate/up item
 constexpr int kFdCols = 16;  // output columns per down group
-constexpr int kFdWarps = 8;
+constexpr int kFdWarps = 16;
+
+constexpr int kFdRouterRows = 2;  // router rows (experts) per CTA
 
 struct FusedSmem {
-  size_t xs4, xsum, item[2], down, dsc, dbi, hs4, hsum, red, total;
+  size_t xs4, xsum, xraw, wr, item[2], down, dsc, dbi, hs4, hsum, red, total;
   size_t item_codes, item_sb;  // bytes of one matrix's codes / scales of an item
   __host__ __device__ FusedSmem(int D, int I, int k) {
     const size_t S = size_t(k) + 1;
     item_codes = size_t(kFdRows) * D / 2;
     item_sb = size_t(kFdRows) * (D / 64) * 2;
-    xs4 = 64;  // bytes 0..63: three mbarriers, abort flag, grid-barrier result
+    xs4 = 64;  // bytes 0..63: four mbarriers, abort flag, grid-barrier result
     xsum = xs4 + size_t(D) * 4;
-    item[0] = (xsum + size_t(D / 32) * 4 + 127) & ~size_t(127);
+    xraw = (xsum + size_t(D / 32) * 4 + 15) & ~size_t(15);  // the token row as bf16
+    wr = (xraw + size_t(D) * 2 + 127) & ~size_t(127);       // router rows, fp32
+    item[0] = (wr + size_t(kFdRouterRows) * D * 4 + 127) & ~size_t(127);
     item[1] = item[0] + 2 * item_codes + 4 * item_sb;
     down = (item[1] + 2 * item_codes + 4 * item_sb + 127) & ~size_t(127);
     dsc = down + S * kFdCols * (I / 2);
@@ -372,14 +380,16 @@ struct FusedSmem {
     hs4 = (dbi + S * kFdCols * (I / 64) * 2 + 15) & ~size_t(15);
     hsum = hs4 + S * size_t(I) * 4;
     red = hsum + S * size_t(I / 32) * 4;
-    total = red + size_t(kFdWarps) * kFdCols * 4;
+    total = red + size_t(kFdWarps * kFdCols > 512 ? kFdWarps * kFdCols : 512) * 4;  // also the E <= 512 logits
   }
 };
 
 struct FusedArgs {
   const uint16_t* x;
   moe_qmatrix gate, up, down, s_gate, s_up, s_down;
-  const float* logits;
+  const float* router_w;
+  const float* router_bias;
+  float* logits;
   int32_t* topk_idx;
   float* topk_w;
   int32_t* count;
@@ -396,9 +406,9 @@ struct FusedArgs {
 };
 
 // Grid-wide barrier of a cooperative launch: every CTA arrives once on the
-// header's counter (zeroed by the router kernel before this launch) and waits,
-// for at most kWaitLimit cycles, until all have. Returns false on expiry
-// (MOE_ERR_DEVICE_TIMEOUT recorded).
+// header's counter (zeroed on the stream before the launch) and waits, for at
+// most kWaitLimit cycles, until `target` arrivals in all. Returns false on
+// expiry (MOE_ERR_DEVICE_TIMEOUT recorded).
 __device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned target, volatile int* result) {
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -423,6 +433,21 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned target, vol
   return *result != 0;
 }
 
+__device__ __forceinline__ void cp16(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// `bytes` (a multiple of 16) from global to shared memory, 16 bytes per
+// thread and step, by all threads of the CTA.
+__device__ __forceinline__ void cp_rows(uint8_t* dst, const void* src, uint32_t bytes) {
+  const uint8_t* s = static_cast<const uint8_t*>(src);
+  for (uint32_t o = threadIdx.x * 16u; o < bytes; o += blockDim.x * 16u) cp16(dst + o, s + o);
+}
+
 template <int MPL>
 __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArgs a) {
   extern __shared__ __align__(128) uint8_t fsm[];
@@ -431,23 +456,119 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
   const int D = a.D, I = a.I, k = a.k, E = a.E, S = k + 1, nch = D / 32, G = D / 64, Gi = I / 64;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const FusedSmem L(D, I, k);
-  const uint32_t bar0 = smem_u32(fsm);  // item 0, item 1, down
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(fsm + 24);
-  volatile int* gb_result = reinterpret_cast<volatile int*>(fsm + 28);
-  if (threadIdx.x == 0) {
-    *abort_flag = 0;
-    for (int i = 0; i < 3; ++i) mbar_init(bar0 + 8u * i, 1);
-    mbar_init_fence();
+  const uint32_t bar0 = smem_u32(fsm);  // mbarriers (bulk-copied codes): item 0, item 1, down, router rows
+  const uint32_t rbar = bar0 + 24u;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(fsm + 32);
+  volatile int* gb_result = reinterpret_cast<volatile int*>(fsm + 36);
+  const int RB = I / kFdRows;  // row blocks per slot
+  const bool has_down = blockIdx.x < a.n_groups;
+  const int d0 = blockIdx.x * kFdCols;
+  const uint32_t icb = uint32_t(L.item_codes), isb = uint32_t(L.item_sb);
+  const uint32_t dcb = kFdCols * (I / 2), dsb = kFdCols * Gi * 2;
+  int n_rt = 0;  // router rows (experts) of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
+  for (int m = 0; m < kFdRouterRows; ++m) n_rt += (blockIdx.x + m * int(gridDim.x) < E);
+  auto has_item = [&](int m) { return blockIdx.x + m * int(gridDim.x) < a.n_items; };
+  auto item_slot = [&](int m) { return (blockIdx.x + m * int(gridDim.x)) / RB; };
+
+  // Item m's gate/up rows and slot j's down rows of expert e. The codes, a
+  // few large contiguous blocks, go by bulk copy (one lane each); the small
+  // scale and bias rows by cp.async from every thread of the CTA.
+  auto item_codes = [&](int m, int e, int part) {  // part 0 gate, 1 up
+    const int item = blockIdx.x + m * gridDim.x, i0 = (item % RB) * kFdRows;
+    const bool sh = (e == E);
+    const moe_qmatrix mq = part == 0 ? (sh ? a.s_gate : a.gate) : (sh ? a.s_up : a.up);
+    const size_t row0 = size_t(sh ? 0 : e) * I + i0;
+    bulk_g2s(bar0 + uint32_t(m == 0 ? L.item[0] : L.item[1]) + part * icb, mq.codes + row0 * (D / 8), icb,
+             bar0 + 8u * m);
+  };
+  auto item_small = [&](int m, int e) {
+    const int item = blockIdx.x + m * gridDim.x, i0 = (item % RB) * kFdRows;
+    const bool sh = (e == E);
+    const moe_qmatrix mg = sh ? a.s_gate : a.gate, mu = sh ? a.s_up : a.up;
+    const size_t row0 = size_t(sh ? 0 : e) * I + i0;
+    uint8_t* dst = fsm + (m == 0 ? L.item[0] : L.item[1]) + 2 * icb;
+    cp_rows(dst, mg.scales + row0 * G, isb);
+    cp_rows(dst + isb, mg.biases + row0 * G, isb);
+    cp_rows(dst + 2 * isb, mu.scales + row0 * G, isb);
+    cp_rows(dst + 3 * isb, mu.biases + row0 * G, isb);
+  };
+  auto down_codes = [&](int j, int e) {
+    const bool sh = (e == E);
+    const moe_qmatrix mq = sh ? a.s_down : a.down;
+    const size_t row0 = size_t(sh ? 0 : e) * D + d0;
+    bulk_g2s(bar0 + uint32_t(L.down) + j * dcb, mq.codes + row0 * (I / 8), dcb, bar0 + 16u);
+  };
+  auto down_small = [&](int j, int e) {
+    const bool sh = (e == E);
+    const moe_qmatrix mq = sh ? a.s_down : a.down;
+    const size_t row0 = size_t(sh ? 0 : e) * D + d0;
+    cp_rows(fsm + L.dsc + j * dsb, mq.scales + row0 * Gi, dsb);
+    cp_rows(fsm + L.dbi + j * dsb, mq.biases + row0 * Gi, dsb);
+  };
+
+  // --- start: barriers and byte counts; bulk copies of the router rows and of
+  // the shared expert's (slot k) codes, which do not depend on the routing.
+  if (warp == 0) {
+    if (lane == 0) {
+      *abort_flag = 0;
+      for (int i = 0; i < 4; ++i) mbar_init(bar0 + 8u * i, 1);
+      mbar_init_fence();
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+        if (has_item(m)) mbar_arrive_tx(bar0 + 8u * m, 2 * icb);
+      if (has_down) mbar_arrive_tx(bar0 + 16u, uint32_t(S) * dcb);
+      if (n_rt) mbar_arrive_tx(rbar, uint32_t(n_rt) * D * 4);
+    }
+    __syncwarp();
+    if (lane < n_rt)
+      bulk_g2s(bar0 + uint32_t(L.wr) + lane * D * 4, a.router_w + size_t(blockIdx.x + lane * gridDim.x) * D, D * 4,
+               rbar);
+    if (lane >= 2 && lane < 6) {
+      const int m = (lane - 2) >> 1;
+      if (has_item(m) && item_slot(m) == k) item_codes(m, E, (lane - 2) & 1);
+    }
+    if (lane == 6 && has_down) down_codes(k, E);
   }
-  // the token row, chunk-major fp32, staged while the logits are read
+  // the token row: bf16 as is (router) and chunk-major fp32 (expert dot products)
   float4* xs4 = reinterpret_cast<float4*>(fsm + L.xs4);
   float* xsum = reinterpret_cast<float*>(fsm + L.xsum);
-  for (int q = threadIdx.x; q < D / 8; q += blockDim.x)
-    stage_bf16x8(xs4, nch, q, *reinterpret_cast<const uint4*>(a.x + size_t(q) * 8));
+  uint4* xraw4 = reinterpret_cast<uint4*>(fsm + L.xraw);
+  for (int q = threadIdx.x; q < D / 8; q += blockDim.x) {
+    const uint4 v = *reinterpret_cast<const uint4*>(a.x + size_t(q) * 8);
+    xraw4[q] = v;
+    stage_bf16x8(xs4, nch, q, v);
+  }
+  if (threadIdx.x == 0) {
+    s_exp[k] = E;  // slot k: the shared expert
+    s_w[k] = 1.f;
+  }
+  __syncthreads();
+  chunk_sums(xs4, xsum, 1, nch);
+
+  // --- router logits of this CTA's experts, in the canonical order (lane l: elements 32c + l, then the tree)
+  if (warp < n_rt && mbar_wait(rbar, 0, abort_flag, a.hdr, kWaitLimit, true)) {
+    const int e = blockIdx.x + warp * gridDim.x;
+    const float* wrow = reinterpret_cast<const float*>(fsm + L.wr) + size_t(warp) * D;
+    const uint16_t* xr = reinterpret_cast<const uint16_t*>(fsm + L.xraw);
+    float acc = 0.f;
+    for (int c = 0; c < nch; ++c) acc = fmaf(bf16_to_f32(xr[32 * c + lane]), wrow[32 * c + lane], acc);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_down_sync(0xffffffffu, acc, off));
+    if (lane == 0) a.logits[e] = a.router_bias ? __fadd_rn(acc, a.router_bias[e]) : acc;
+  }
+  if (n_rt && warp == kFdWarps - 1) mbar_wait(rbar, 0, abort_flag, a.hdr, kWaitLimit, true);  // landed before any exit
+  const bool gb1 = grid_barrier(a.hdr, gridDim.x, gb_result);
+
+  // --- top-k (every CTA, the same selection), then the routed experts' copies:
+  // group 2 item 0, group 3 item 1, group 4 the down rows
   if (warp == 0) {
-    int myi;
-    float myw;
-    select_topk<MPL>(a.logits, E, k, myi, myw);
+    int myi = 0;
+    float myw = 0.f;
+    if (gb1) select_topk<MPL, true>(a.logits, E, k, myi, myw);
+    if (lane < k && (myi < 0 || myi >= E)) {
+      report(a.hdr, MOE_ERR_DEVICE_CHECK, 111);
+      myi = 0;
+    }
     if (lane < k) {
       s_exp[lane] = myi;
       s_w[lane] = myw;
@@ -456,85 +577,41 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
         a.topk_w[lane] = myw;
       }
     }
-    if (lane == 0) {
-      s_exp[k] = E;
-      s_w[k] = 1.f;
+    __syncwarp();
+    // bulk copies of the routed codes: lanes 0..3 the two items' gate and up,
+    // lanes 4.. the down slots
+    if (lane < 4) {
+      const int m = lane >> 1;
+      if (has_item(m) && item_slot(m) < k) item_codes(m, s_exp[item_slot(m)], lane & 1);
+    } else if (lane < 4 + k && has_down) {
+      down_codes(lane - 4, s_exp[lane - 4]);
     }
   }
   __syncthreads();
-  if (blockIdx.x == 0)  // the routing tables of one token, for the workspace view
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int slot = -1, below = 0;
-    for (int j = 0; j < k; ++j) {
-      slot = (s_exp[j] == e) ? j : slot;
-      below += s_exp[j] < e;
-    }
-    a.count[e] = slot >= 0;
-    a.off[e] = below;
-    if (e == E - 1) a.off[E] = k;
-    if (slot >= 0) {
-      a.perm[below] = slot;
-      a.inv[slot] = below;
-      a.blocks[3 * below] = e;
-      a.blocks[3 * below + 1] = below;
-      a.blocks[3 * below + 2] = 1;
-    }
-    if (e == 0) {
-      a.blocks[3 * k] = E;
-      a.blocks[3 * k + 1] = k;
-      a.blocks[3 * k + 2] = 1;
-      *a.n_blocks = k + 1;
-    }
-  }
-  const int RB = I / kFdRows;  // row blocks per slot
-  const bool has_down = blockIdx.x < a.n_groups;
-  const int d0 = blockIdx.x * kFdCols;
-  if (threadIdx.x == 0) {  // every weight this CTA needs, at once
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      const int item = blockIdx.x + m * gridDim.x;
-      if (item >= a.n_items) continue;
-      const int slot = item / RB, i0 = (item % RB) * kFdRows, e = s_exp[slot];
-      const bool sh = (e == E);
-      const moe_qmatrix mg = sh ? a.s_gate : a.gate, mu = sh ? a.s_up : a.up;
-      const size_t row0 = size_t(sh ? 0 : e) * I + i0;
-      const uint32_t cb = uint32_t(L.item_codes), sbb = uint32_t(L.item_sb);
-      const uint32_t dst = bar0 + uint32_t(L.item[m]), bar = bar0 + 8u * m;
-      mbar_arrive_tx(bar, 2 * cb + 4 * sbb);
-      bulk_g2s(dst, mg.codes + row0 * (D / 8), cb, bar);
-      bulk_g2s(dst + cb, mu.codes + row0 * (D / 8), cb, bar);
-      bulk_g2s(dst + 2 * cb, mg.scales + row0 * G, sbb, bar);
-      bulk_g2s(dst + 2 * cb + sbb, mg.biases + row0 * G, sbb, bar);
-      bulk_g2s(dst + 2 * cb + 2 * sbb, mu.scales + row0 * G, sbb, bar);
-      bulk_g2s(dst + 2 * cb + 3 * sbb, mu.biases + row0 * G, sbb, bar);
-    }
-    if (has_down) {
-      const uint32_t cb = kFdCols * (I / 2), sbb = kFdCols * Gi * 2, bar = bar0 + 16u;
-      mbar_arrive_tx(bar, uint32_t(S) * (cb + 2 * sbb));
-      for (int j = 0; j < S; ++j) {
-        const int e = s_exp[j];
-        const bool sh = (e == E);
-        const moe_qmatrix m = sh ? a.s_down : a.down;
-        const size_t row0 = size_t(sh ? 0 : e) * D + d0;
-        bulk_g2s(bar0 + uint32_t(L.down) + j * cb, m.codes + row0 * (I / 8), cb, bar);
-        bulk_g2s(bar0 + uint32_t(L.dsc) + j * sbb, m.scales + row0 * Gi, sbb, bar);
-        bulk_g2s(bar0 + uint32_t(L.dbi) + j * sbb, m.biases + row0 * Gi, sbb, bar);
-      }
-    }
-  }
-  chunk_sums(xs4, xsum, 1, nch);
-  __syncthreads();
-
-  // gate/up: warp w takes rows w and w+8 of each item
-  bool ok = true;
+  // groups 0, 1, 2: the scales and biases (small rows, by cp.async) of item 0,
+  // item 1 and the down slots. Issued only now: cp.async requests still in
+  // flight hold up the top-k's reads of the logits behind them.
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
+    if (has_item(m)) item_small(m, s_exp[item_slot(m)]);
+    cp_commit();
+  }
+  if (has_down)
+    for (int j = 0; j < S; ++j) down_small(j, s_exp[j]);
+  cp_commit();
+
+  // --- gate/up: warp w takes row w of each item
+  const bool ok = gb1;
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    if (m == 0)
+      cp_wait<2>();  // group 0: item 0's scales and biases
+    else
+      cp_wait<1>();  // group 1: item 1's
+    __syncthreads();
+    if (!has_item(m)) continue;
+    if (!mbar_wait(bar0 + 8u * m, 0, abort_flag, a.hdr, kWaitLimit, true)) continue;
     const int item = blockIdx.x + m * gridDim.x;
-    if (item >= a.n_items) continue;
-    if (!mbar_wait(bar0 + 8u * m, 0, abort_flag, a.hdr, kWaitLimit, true)) {
-      ok = false;
-      continue;
-    }
     const int slot = item / RB, i0 = (item % RB) * kFdRows;
     const uint8_t* base = fsm + L.item[m];
     const uint8_t* cg = base;
@@ -574,13 +651,10 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
   }
 
   // every CTA's h rows are written: the down projection may read them
-  const bool gb_ok = grid_barrier(a.hdr, gridDim.x, gb_result);
+  const bool gb2 = grid_barrier(a.hdr, 2 * gridDim.x, gb_result);
+  cp_wait<0>();  // group 2: the down scales and biases; no cp.async is left in flight
   if (!has_down) return;
-  const uint32_t dbar = bar0 + 16u;
-  if (!ok || !gb_ok) {  // drain the down copies before leaving
-    mbar_wait(dbar, 0, abort_flag, a.hdr, kWaitLimit, true);
-    return;
-  }
+  if (!mbar_wait(bar0 + 16u, 0, abort_flag, a.hdr, kWaitLimit, true) || !ok || !gb2) return;
   float4* hs4 = reinterpret_cast<float4*>(fsm + L.hs4);
   float* hsum = reinterpret_cast<float*>(fsm + L.hsum);
   const int nchi = I / 32;
@@ -591,14 +665,15 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
   __syncthreads();
   chunk_sums(hs4, hsum, S, nchi);
   __syncthreads();
-  if (!mbar_wait(dbar, 0, abort_flag, a.hdr, kWaitLimit, true)) return;
   const uint8_t* codes = fsm + L.down;
   const uint16_t* sc = reinterpret_cast<const uint16_t*>(fsm + L.dsc);
   const uint16_t* bi = reinterpret_cast<const uint16_t*>(fsm + L.dbi);
-  float part[kFdCols];
-#pragma unroll
-  for (int cl = 0; cl < kFdCols; ++cl) part[cl] = 0.f;
-  for (int it = threadIdx.x; it < S * nchi; it += blockDim.x) {
+  // unit = (item it, column quarter q): 4 dot products. Lane l of warp w
+  // takes quarter q = l / 8 and items 8w + l % 8 (+ 8 * warps per round), so
+  // the 8 lanes of one quarter read 128 contiguous bytes of one row.
+  const int q = (lane >> 3) & 3;
+  float part[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int it = 8 * warp + (lane & 7); it < S * nchi; it += 8 * kFdWarps) {
     const int j = it / nchi, c = it % nchi;
     float4 xv[8];
     const float4* xr = hs4 + size_t(j) * 8 * nchi;
@@ -606,22 +681,22 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
     for (int jq = 0; jq < 8; ++jq) xv[jq] = xr[jq * nchi + c];
     const float sx = hsum[j * nchi + c], wj = s_w[j];
 #pragma unroll
-    for (int cl = 0; cl < kFdCols; ++cl) {
-      const int rowi = j * kFdCols + cl;
+    for (int cc = 0; cc < 4; ++cc) {
+      const int rowi = j * kFdCols + 4 * q + cc;
       const uint4 w4 = reinterpret_cast<const uint4*>(codes + size_t(rowi) * (I / 2))[c];
       const int gi = rowi * Gi + c / 2;
-      part[cl] += wj * chunk_dot_r(w4, xv, sx, sc[gi], bi[gi]);
+      part[cc] += wj * chunk_dot_r(w4, xv, sx, sc[gi], bi[gi]);
     }
   }
-  float* red = reinterpret_cast<float*>(fsm + L.red);
+  float* red = reinterpret_cast<float*>(fsm + L.red);  // [kFdWarps][kFdCols]
 #pragma unroll
-  for (int cl = 0; cl < kFdCols; ++cl) {
+  for (int cc = 0; cc < 4; ++cc) {
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) part[cl] += __shfl_xor_sync(0xffffffffu, part[cl], off);
+    for (int off = 4; off >= 1; off >>= 1) part[cc] += __shfl_xor_sync(0xffffffffu, part[cc], off);
   }
-  if (lane == 0) {
+  if ((lane & 7) == 0) {
 #pragma unroll
-    for (int cl = 0; cl < kFdCols; ++cl) red[warp * kFdCols + cl] = part[cl];
+    for (int cc = 0; cc < 4; ++cc) red[warp * kFdCols + 4 * q + cc] = part[cc];
   }
   __syncthreads();
   if (threadIdx.x < kFdCols) {
@@ -677,7 +752,7 @@ FusedPlan fused_plan_uncached(const Ctx& c) {
   if (p.smem > 227 * 1024) return p;
   p.n_items = (c.k + 1) * (c.I / kFdRows);
   p.n_groups = c.D / kFdCols;
-  const int grid = std::max(p.n_groups, (p.n_items + 1) / 2);
+  const int grid = std::max(std::max(p.n_groups, (p.n_items + 1) / 2), (c.E + kFdRouterRows - 1) / kFdRouterRows);
   int dev = 0, coop = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop ||
@@ -719,13 +794,17 @@ cudaError_t decode_fused(const Ctx& c) {
   const FusedPlan p = fused_plan(c);
   if (p.grid == 0) return cudaErrorInvalidValue;
   const moe_weights* w = c.w;
-  FusedArgs a{c.x,     w->gate, w->up,     w->down,  w->s_gate, w->s_up, w->s_down, c.logits, c.topk_idx,
-              c.topk_w, c.count, c.off,    c.perm,   c.inv,     c.blocks, c.n_blocks, c.h,     c.y,
-              c.hdr,   c.D,     c.E,       c.k,      c.I,       p.n_items, p.n_groups};
+  FusedArgs a{c.x,         w->gate,        w->up,    w->down,     w->s_gate, w->s_up, w->s_down,
+              w->router_w,  w->router_bias, c.logits, c.topk_idx,  c.topk_w,  c.count, c.off,
+              c.perm,       c.inv,          c.blocks, c.n_blocks,  c.h,       c.y,     c.hdr,
+              c.D,          c.E,            c.k,      c.I,         p.n_items, p.n_groups};
+  // status and grid-barrier counter start at zero for this call
+  cudaError_t err = cudaMemsetAsync(c.hdr, 0, 16, c.stream);
+  if (err != cudaSuccess) return err;
   void* args[] = {&a};
   const void* f = p.mpl == 8 ? reinterpret_cast<const void*>(decode_fused_kernel<8>)
                              : reinterpret_cast<const void*>(decode_fused_kernel<16>);
-  cudaError_t err = cudaLaunchCooperativeKernel(f, dim3(p.grid), dim3(kFdWarps * 32), args, p.smem, c.stream);
+  err = cudaLaunchCooperativeKernel(f, dim3(p.grid), dim3(kFdWarps * 32), args, p.smem, c.stream);
   if (err != cudaSuccess) return err;
   launch_done("decode_fused", c.stream);
   return cudaSuccess;

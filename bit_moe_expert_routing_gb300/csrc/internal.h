@@ -77,8 +77,8 @@ bool tmap_encoder_available();
 // Decode GEMV path (a few rows).
 cudaError_t gemv(const Ctx& c);
 bool gemv_supported(const Ctx& c);
-// One token: top-k, gate/up and down in one cooperative kernel after the
-// router logits (route_logits_small).
+// One token: router logits, top-k, gate/up and down in one cooperative kernel
+// (with the header zeroed on the stream first).
 cudaError_t decode_fused(const Ctx& c);
 bool decode_fused_supported(const Ctx& c);
 // Router logits only, for up to 16 tokens; also zeroes the header counter.

@@ -269,10 +269,10 @@ moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uin
   if (!x || !y || !aligned16(x) || !aligned16(y) || x == y) return MOE_ERR_ARG;
   const Path path = plan(c);
   timing_begin(c.stream);
-  cudaError_t err = (path == Path::DecodeFused) ? route_logits_small(c) : route(c);
+  if (path == Path::DecodeFused) return cuda_status(decode_fused(c));  // routing included
+  cudaError_t err = route(c);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (path == Path::Gemv) return cuda_status(gemv(c));
-  if (path == Path::DecodeFused) return cuda_status(decode_fused(c));
   if (path == Path::GemmWt) return cuda_status(gemm_wt(c));
   if (path == Path::GemmTc) return cuda_status(gemm_tc(c));
   return cuda_status(gemm_simt(c));

@@ -2,56 +2,63 @@
 // routing kernels and the fused decode kernel.
 #pragma once
 
-#include <climits>
-
 #include "common.cuh"
 
 namespace moe {
+
+// Order-preserving map of a logit onto an unsigned key: a larger float gives
+// a larger key. NaN is taken as -inf and -0 as +0, so floats that compare
+// equal give equal keys; every real logit's key is above 0, the key of an
+// empty or taken place.
+__device__ __forceinline__ unsigned logit_key(float v) {
+  if (v != v) v = -INFINITY;
+  if (v == 0.f) v = 0.f;
+  const unsigned b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(unsigned key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
 
 // Top-k of one token's logits (larger logit first, lower expert index on
 // ties) by one warp; lane l holds logits l, l+32, ... On return lane j < k
 // holds slot j: its expert and its weight, the softmax renormalised over the
 // k kept, exp(l_j - l_max) / sum.
-// MPL >= ceil(E / 32) logits per lane (E <= 1024).
-template <int MPL>
+// MPL >= ceil(E / 32) logits per lane (E <= 1024). L2 = true reads the
+// logits through L2 only (they were written by other CTAs of the same grid).
+// Each of the k rounds takes the warp's largest key with one max reduction
+// and, among the places holding it, the lowest expert index with one min
+// reduction (redux.sync), then clears that place.
+template <int MPL, bool L2 = false>
 __device__ __forceinline__ void select_topk(const float* __restrict__ lg, int E, int k, int& myi, float& myw) {
   const int lane = threadIdx.x & 31;
-  const int M = (E + 31) / 32;
-  float v[MPL];
-  unsigned taken = 0;
+  unsigned key[MPL];
 #pragma unroll
   for (int m = 0; m < MPL; ++m) {
     const int e = lane + 32 * m;
-    v[m] = (m < M && e < E) ? lg[e] : 0.f;
-    if (!(m < M && e < E)) taken |= 1u << m;
+    key[m] = e < E ? logit_key(L2 ? __ldcg(lg + e) : lg[e]) : 0u;
   }
   float first = 0.f, myv = 0.f;
   myi = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = INT_MAX;
+    unsigned lb = key[0];
+    int lm = 0;
 #pragma unroll
-    for (int m = 0; m < MPL; ++m) {
-      const int e = lane + 32 * m;
-      if (!((taken >> m) & 1u) && (v[m] > bv || (v[m] == bv && e < bi))) {
-        bv = v[m];
-        bi = e;
+    for (int m = 1; m < MPL; ++m)
+      if (key[m] > lb) {  // strict: the lowest place of equal keys stays
+        lb = key[m];
+        lm = m;
       }
-    }
+    const unsigned top = __reduce_max_sync(0xffffffffu, lb);
+    const unsigned bi = __reduce_min_sync(0xffffffffu, lb == top ? unsigned(lane + 32 * lm) : 0xffffffffu);
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    for (int m = 0; m < MPL; ++m)
+      if (unsigned(lane + 32 * m) == bi) key[m] = 0u;
+    const float bv = key_logit(top);
     if (j == 0) first = bv;
     if (lane == j) {
       myv = bv;
-      myi = bi;
+      myi = int(bi);
     }
   }
   const float ex = lane < k ? expf(myv - first) : 0.f;

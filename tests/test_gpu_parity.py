@@ -208,8 +208,9 @@ def test_layer_decode(path):
 
 @pytest.mark.parametrize("fused", [0, 1], ids=["separate", "fused"])
 def test_layer_decode_fused_and_separate(fused):
-    # one token on the GEMV path: the cooperative kernel (top-k, gate/up, grid
-    # barrier, down) and the separate routing + GEMV kernels, both against the oracle
+    # one token on the GEMV path: the cooperative kernel (router, grid barrier,
+    # top-k, gate/up, grid barrier, down) and the separate routing + GEMV
+    # kernels, both against the oracle
     layer, x = config("decode")
     assert moe.moe_set_option(moe.MOE_OPT_DECODE_FUSED, fused) == moe.MOE_OK
     try:
@@ -220,7 +221,7 @@ def test_layer_decode_fused_and_separate(fused):
         moe.moe_set_option(moe.MOE_OPT_DECODE_FUSED, 1)
     ol = O.OracleLayer(layer)
     check_output(y, O.forward(ol, x), f"decode fused={fused}")
-    assert launches == (2 if fused else 4)
+    assert launches == (1 if fused else 4)
     # the routing tables in the workspace agree with the oracle either way
     v = dl.view(1, ws)
     g = lambda p_, shape, dt: moe.ws_tensor(ws, p_, shape, dt).cpu().numpy()
