@@ -608,20 +608,23 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
             }
           }
         } else {
-          // transpose the warp's 32 columns x 16 tokens so that each lane adds
-          // four consecutive output columns of one token (16-byte reductions)
+          // transpose the warp's 32 columns x 16 tokens, then add them as
+          // 16-byte reductions, eight lanes covering one token's 128-byte
+          // line: each instruction touches four whole lines. Token c's index
+          // and weight sit in lanes 2c and 2c+1.
 #pragma unroll
           for (int c = 0; c < 16; ++c) xb[c * kXposeStride + lane] = __uint_as_float(v[c]);
           __syncwarp();
-          const int c = lane >> 1, nn = n0 + c;
-          if (nn < R) {
-            const float w = wgt[m];
-            float* dst = a.y_acc + size_t(tok[m]) * a.D + j * WM + q * 32;
+          const int quad = lane & 7;
 #pragma unroll
-            for (int kq = 0; kq < 4; ++kq) {
-              const int quad = (lane & 1) * 4 + kq;
+          for (int kq = 0; kq < 4; ++kq) {
+            const int c = (lane >> 3) + 4 * kq;
+            const int tc_ = __shfl_sync(0xffffffffu, tok[m], 2 * c);
+            const float w = __shfl_sync(0xffffffffu, wgt[m], 2 * c);
+            if (n0 + c < R) {
               const float4 val = *reinterpret_cast<const float4*>(xb + c * kXposeStride + quad * 4);
-              red_add_v4(dst + quad * 4, w * val.x, w * val.y, w * val.z, w * val.w);
+              red_add_v4(a.y_acc + size_t(tc_) * a.D + j * WM + q * 32 + quad * 4, w * val.x, w * val.y, w * val.z,
+                         w * val.w);
             }
           }
           __syncwarp();
