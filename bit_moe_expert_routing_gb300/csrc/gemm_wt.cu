@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
       mbar_init(bempty(s), 1);
     }
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(afull(s), kNumDqWarps);  // both groups of the stage, four warps each
+      mbar_init(afull(s), kNumDqWarps / 2);  // the four warps (one per lane quarter) of the stage's parity
       mbar_init(aempty(s), 1);
     }
     for (int s = 0; s < kCStages; ++s) {
@@ -447,11 +447,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
     }
   } else if (warp >= kWarpDq0 && warp < kWarpDq0 + kNumDqWarps) {
     // ---------------- dequantisation into the tensor-memory A stage ----------------
-    // Four warps (one per TMEM lane quarter) take the even groups of K, four the
-    // odd ones: each stage's two groups are converted side by side, a warp
-    // converting all 64 codes of its row in a group.
+    // Four warps (one per TMEM lane quarter) fill the even stages, four the odd
+    // ones: a warp converts both groups of its stage (all 128 codes of its
+    // row), so each barrier wait, tensor-memory store wait and arrival is paid
+    // once per stage, and consecutive stages are converted side by side.
     const int q = warp & 3;                          // TMEM lane quarter of this warp
-    const int par = (warp - kWarpDq0) >> 2;          // group parity = position in the stage
+    const int par = (warp - kWarpDq0) >> 2;          // stage parity this warp fills
     const int L = q * 32 + lane;                     // TMEM lane = weight row of the tile
     const int srow_stage = GATEUP ? ((L & 1) ? 64 + (L >> 1) : (L >> 1)) : L;  // row in the code stage
     const bool vec_sb = (K / 64) % 8 == 0;
@@ -480,49 +481,56 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
         }
       }
       int win = 0;
-      for (int ks = par; ks < KS; ks += 2) {
-        const uint32_t ig = g0 + ks, is = t0 + ks / kGroupsPerStage;
-        const int s = is % kAStages, cs = ig % kCStages;
-        const uint32_t ph = (is / kAStages) & 1u, cph = (ig / kCStages) & 1u;
-        uint16_t sc, bi;
-        if (vec_sb) {
-          if ((ks >> 3) != win) {  // next window of 8 groups
-            win = ks >> 3;
-            s_cur = s_nxt;
-            b_cur = b_nxt;
-            if (8 * (win + 1) < KS) {
-              s_nxt = *reinterpret_cast<const uint4*>(srow + 8 * (win + 1));
-              b_nxt = *reinterpret_cast<const uint4*>(brow + 8 * (win + 1));
+      for (int t = par; t < KT && ok; t += 2) {
+        const uint32_t is = t0 + t;
+        const int s = is % kAStages;
+        const uint32_t ph = (is / kAStages) & 1u;
+#pragma unroll 1
+        for (int hb = 0; hb < kGroupsPerStage; ++hb) {
+          const int ks = t * kGroupsPerStage + hb;
+          const uint32_t ig = g0 + ks;
+          const int cs = ig % kCStages;
+          const uint32_t cph = (ig / kCStages) & 1u;
+          uint16_t sc, bi;
+          if (vec_sb) {
+            if ((ks >> 3) != win) {  // next window of 8 groups
+              win = ks >> 3;
+              s_cur = s_nxt;
+              b_cur = b_nxt;
+              if (8 * (win + 1) < KS) {
+                s_nxt = *reinterpret_cast<const uint4*>(srow + 8 * (win + 1));
+                b_nxt = *reinterpret_cast<const uint4*>(brow + 8 * (win + 1));
+              }
             }
+            sc = pick_bf16(s_cur, ks & 7);
+            bi = pick_bf16(b_cur, ks & 7);
+          } else {
+            sc = srow[ks];
+            bi = brow[ks];
           }
-          sc = pick_bf16(s_cur, ks & 7);
-          bi = pick_bf16(b_cur, ks & 7);
-        } else {
-          sc = srow[ks];
-          bi = brow[ks];
+          if (!(ok = mbar_wait(cfull(cs), cph, abort_flag, a.hdr))) break;
+          const uint8_t* crow = gbase + kOffC + cs * kCBytes + srow_stage * 32;
+          const uint4 w0 = *reinterpret_cast<const uint4*>(crow);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(crow + 16);
+          const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16(sc), __ushort_as_bfloat16(sc));
+          const __nv_bfloat162 b2 = __halves2bfloat162(__ushort_as_bfloat16(bi), __ushort_as_bfloat16(bi));
+          uint32_t o[32];
+          dq8_bf16(w0.x, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 0));
+          dq8_bf16(w0.y, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 4));
+          dq8_bf16(w0.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 8));
+          dq8_bf16(w0.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 12));
+          dq8_bf16(w1.x, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 16));
+          dq8_bf16(w1.y, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 20));
+          dq8_bf16(w1.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 24));
+          dq8_bf16(w1.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 28));
+          // the code stage goes back to the TMA: the arrival releases this
+          // warp's reads of it (they have returned: the values above use them)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(cempty(cs));
+          if (hb == 0 && !(ok = mbar_wait(aempty(s), ph ^ 1u, abort_flag, a.hdr))) break;
+          tmem_st32(tmem + (uint32_t(q * 32) << 16) + kAColBase + s * kAStageCols + hb * kAGroupCols, o);
         }
-        if (!(ok = mbar_wait(cfull(cs), cph, abort_flag, a.hdr))) break;
-        const uint8_t* crow = gbase + kOffC + cs * kCBytes + srow_stage * 32;
-        const uint4 w0 = *reinterpret_cast<const uint4*>(crow);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(crow + 16);
-        const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16(sc), __ushort_as_bfloat16(sc));
-        const __nv_bfloat162 b2 = __halves2bfloat162(__ushort_as_bfloat16(bi), __ushort_as_bfloat16(bi));
-        uint32_t o[32];
-        dq8_bf16(w0.x, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 0));
-        dq8_bf16(w0.y, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 4));
-        dq8_bf16(w0.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 8));
-        dq8_bf16(w0.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 12));
-        dq8_bf16(w1.x, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 16));
-        dq8_bf16(w1.y, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 20));
-        dq8_bf16(w1.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 24));
-        dq8_bf16(w1.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 28));
-        // the code stage goes back to the TMA only after the reads above have
-        // returned (the dequantised values depend on them)
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cempty(cs));
-        if (!(ok = mbar_wait(aempty(s), ph ^ 1u, abort_flag, a.hdr))) break;
-        tmem_st32(tmem + (uint32_t(q * 32) << 16) + kAColBase + s * kAStageCols + par * kAGroupCols, o);
+        if (!ok) break;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
