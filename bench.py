@@ -426,7 +426,8 @@ def run_decode(args, moe, synth, torch, device, stream, peaks) -> dict:
             "us_p95": 1e3 * ms_g[int(0.95 * (n - 1))], "steps": n, "tokens_per_s": 1e6 / us_g,
             "launches_per_step": launches,
             "roofline": dict(kernel="+".join(names), bound="hbm", achieved=ach, peak=peaks["hbm_gbs"],
-                             unit="GB/s", frac=(ach / peaks["hbm_gbs"]) if ach else None, traffic=None,
+                             unit="GB/s", frac=(ach / peaks["hbm_gbs"]) if ach else None,
+                             traffic=profiled_traffic(names[0]) if len(names) == 1 else None,
                              bytes_per_launch=work["weight_bytes"],
                              peak_source=f"{peaks['source']} copy"),
             "layer_GBps_on_expert_bytes": work["weight_bytes"] / (us_g / 1e6) / 1e9,
