@@ -336,7 +336,9 @@ def run_ours(args) -> dict:
                    "l2": "flushed between steps (512 MiB write outside the timed events)",
                    "parallelism": f"replicas x{world}", "gemm_impl": "tcgen05" if moe.moe_get_option(
                        moe.MOE_OPT_GEMM_IMPL) == 0 else "cuda-core",
-                   "experts_touched": work["experts_touched"]},
+                   "experts_touched": work["experts_touched"],
+                   "workspace_bytes": dl.workspace_bytes(T),
+                   "chunk_tokens": moe.moe_get_option(moe.MOE_OPT_CHUNK_TOKENS)},
         "roofline": roof,
         "layer_tflops": whole,
         "kernels": kernels,

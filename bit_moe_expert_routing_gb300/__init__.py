@@ -32,6 +32,7 @@ MOE_OPT_GEMM_IMPL = 4
 MOE_OPT_TEST_WAIT_CYCLES = 5
 MOE_OPT_BLOCK_M = 6
 MOE_OPT_DECODE_FUSED = 7
+MOE_OPT_CHUNK_TOKENS = 8
 
 PATH_AUTO, PATH_GEMV, PATH_GEMM = 0, 1, 2
 GEMM_TENSOR_CORE, GEMM_CUDA_CORE, GEMM_TENSOR_CORE_SMEM = 0, 1, 2
@@ -210,14 +211,16 @@ class DeviceLayer:
                              qm(layer.gate), qm(layer.up), qm(layer.down),
                              qm(layer.s_gate), qm(layer.s_up), qm(layer.s_down))
 
-    def workspace(self, T: int, host_staging: bool = False):
-        import torch
+    def workspace_bytes(self, T: int, host_staging: bool = False) -> int:
+        """Device bytes of the workspace for T tokens (one pass of at most the chunk size)."""
         n = moe_workspace_size(self.w, T)
         if n == 0:
             raise MoEError(MOE_ERR_ARG, "moe_workspace_size")
-        if host_staging:
-            n += moe_host_staging_size(self.w, T)
-        return torch.empty(n, dtype=torch.uint8, device=self._t[0].device)
+        return n + (moe_host_staging_size(self.w, T) if host_staging else 0)
+
+    def workspace(self, T: int, host_staging: bool = False):
+        import torch
+        return torch.empty(self.workspace_bytes(T, host_staging), dtype=torch.uint8, device=self._t[0].device)
 
     def forward(self, x, y=None, workspace=None, stream=None):
         """x: bf16 [T, D] on the device. Returns y: bf16 [T, D]."""

@@ -24,6 +24,7 @@ struct Options {
   int test_wait_cycles = 0;
   int block_m = 0;  // 0: the path's own block size
   int decode_fused = 1;
+  int chunk_tokens = 8192;  // 0: one pass over all T
 };
 Options g_opt;
 std::mutex g_mu;
@@ -114,6 +115,9 @@ moe_status check_weights(const moe_weights* w) {
 }
 
 constexpr int kMaxT = 1 << 20;
+
+// Tokens of one pass: T, or the chunk size when chunking is on and T is larger.
+int pass_tokens(int T) { return (g_opt.chunk_tokens > 0 && T > g_opt.chunk_tokens) ? g_opt.chunk_tokens : T; }
 
 moe_status make_ctx(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* ws, size_t ws_bytes,
                     void* stream, Ctx* c) {
@@ -229,12 +233,12 @@ extern "C" {
 
 size_t moe_workspace_size(const moe_weights* w, int T) {
   if (check_weights(w) != MOE_OK || T < 0 || T > kMaxT) return 0;
-  return layout(w, T).total;
+  return layout(w, pass_tokens(T)).total;
 }
 
 size_t moe_host_staging_size(const moe_weights* w, int T) {
   if (check_weights(w) != MOE_OK || T < 0 || T > kMaxT) return 0;
-  return 2 * al256(size_t(T) * w->D * 2);
+  return 2 * al256(size_t(pass_tokens(T)) * w->D * 2);
 }
 
 moe_status moe_route(const moe_weights* w, const uint16_t* x, int T, void* workspace, size_t workspace_bytes,
@@ -260,13 +264,13 @@ moe_status moe_workspace_view(const moe_weights* w, int T, void* workspace, size
   return MOE_OK;
 }
 
-moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+// One pass of the layer over T tokens (T no larger than the workspace was
+// laid out for). Adds its launches to the thread's count.
+static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   Ctx c;
   if (moe_status s = make_ctx(w, x, T, y, workspace, workspace_bytes, stream, &c)) return s;
-  t_launches = 0;
   if (T == 0) return MOE_OK;
-  if (!x || !y || !aligned16(x) || !aligned16(y) || x == y) return MOE_ERR_ARG;
   const Path path = plan(c);
   timing_begin(c.stream);
   if (path == Path::DecodeFused) return cuda_status(decode_fused(c));  // routing included
@@ -278,23 +282,52 @@ moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uin
   return cuda_status(gemm_simt(c));
 }
 
+// Prompt chunking ("Optimizing on-device inference for Apple Silicon",
+// section "Bound temporary memory with prompt chunking"): T above the chunk
+// size runs as consecutive passes over bounded token ranges on the caller's
+// stream, all reusing one workspace sized for a single pass. Tokens are
+// independent in this layer, so the output is the one pass's output.
+moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (moe_status s = check_weights(w)) return s;
+  if (T < 0 || T > kMaxT) return MOE_ERR_ARG;
+  t_launches = 0;
+  if (T == 0) return forward_pass(w, x, 0, y, workspace, workspace_bytes, stream);  // checks the workspace
+  if (!x || !y || !aligned16(x) || !aligned16(y) || x == y) return MOE_ERR_ARG;
+  const int step = pass_tokens(T);
+  for (int t0 = 0; t0 < T; t0 += step) {
+    const int n = std::min(step, T - t0);
+    const size_t at = size_t(t0) * w->D;
+    if (moe_status s = forward_pass(w, x + at, n, y + at, workspace, workspace_bytes, stream)) return s;
+  }
+  return MOE_OK;
+}
+
 moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, int T, uint16_t* y_host,
                                   void* workspace, size_t workspace_bytes, void* stream) {
   if (check_weights(w) != MOE_OK) return check_weights(w);
   if (T < 0 || T > kMaxT) return MOE_ERR_ARG;
   if (T == 0) return MOE_OK;
   if (!x_host || !y_host) return MOE_ERR_ARG;
-  const size_t need = moe_workspace_size(w, T), stage = al256(size_t(T) * w->D * 2);
+  // one pass's tokens are staged at a time: x in, the layer, y out
+  const int step = pass_tokens(T);
+  const size_t need = moe_workspace_size(w, T), stage = al256(size_t(step) * w->D * 2);
   if (!workspace || workspace_bytes < need + 2 * stage) return MOE_ERR_WORKSPACE;
   char* base = static_cast<char*>(workspace);
   uint16_t* xd = reinterpret_cast<uint16_t*>(base + need);
   uint16_t* yd = reinterpret_cast<uint16_t*>(base + need + stage);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t bytes = size_t(T) * w->D * 2;
-  if (cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
-  moe_status st = moe_layer_forward(w, xd, T, yd, workspace, need, stream);
-  if (st != MOE_OK) return st;
-  if (cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  int launches = 0;
+  for (int t0 = 0; t0 < T; t0 += step) {
+    const int n = std::min(step, T - t0);
+    const size_t at = size_t(t0) * w->D, bytes = size_t(n) * w->D * 2;
+    if (cudaMemcpyAsync(xd, x_host + at, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+    moe_status st = moe_layer_forward(w, xd, n, yd, workspace, need, stream);
+    if (st != MOE_OK) return st;
+    launches += t_launches;
+    if (cudaMemcpyAsync(y_host + at, yd, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  t_launches = launches;
   return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -337,6 +370,10 @@ moe_status moe_set_option(int option, int value) {
       if (value != 0 && (value < kMinBlockM || value > kWtBlockRows || value % 16 != 0)) return MOE_ERR_ARG;
       g_opt.block_m = value;
       return MOE_OK;
+    case MOE_OPT_CHUNK_TOKENS:
+      if (value < 0 || value > kMaxT) return MOE_ERR_ARG;
+      g_opt.chunk_tokens = value;
+      return MOE_OK;
     case MOE_OPT_TEST_WAIT_CYCLES:
       if (value < 0) return MOE_ERR_ARG;
       g_opt.test_wait_cycles = value;
@@ -356,6 +393,7 @@ int moe_get_option(int option) {
     case MOE_OPT_TEST_WAIT_CYCLES: return g_opt.test_wait_cycles;
     case MOE_OPT_BLOCK_M: return g_opt.block_m;
     case MOE_OPT_DECODE_FUSED: return g_opt.decode_fused;
+    case MOE_OPT_CHUNK_TOKENS: return g_opt.chunk_tokens;
     default: return -1;
   }
 }

@@ -44,14 +44,37 @@ void* static_scratch_on_current_device() {
   return ptrs[dev];
 }
 
+// Largest token count, at most T, whose workspace fits the array (0 if even
+// one token does not). The size grows with the token count up to the chunk
+// size and is flat beyond it, so a bisection finds it.
+int tokens_fitting(const moe_weights* w, int T) {
+  if (moe_workspace_size(w, T) <= kStaticScratchBytes) return T;
+  int lo = 0, hi = T;  // size(lo) fits (or lo = 0), size(hi) does not
+  while (hi - lo > 1) {
+    const int mid = lo + (hi - lo) / 2;
+    if (moe_workspace_size(w, mid) <= kStaticScratchBytes)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
 }  // namespace
 
 extern "C" moe_status moe_layer_forward_static(const moe_weights* w, const uint16_t* x, int T, uint16_t* y,
                                                void* stream) {
   const size_t need = moe_workspace_size(w, T);
-  if (need == 0) return moe_layer_forward(w, x, T, y, nullptr, 0, stream);  // names the argument or shape error
-  if (need > kStaticScratchBytes) return MOE_ERR_WORKSPACE;
+  if (need == 0 || T == 0) return moe_layer_forward(w, x, T, y, nullptr, 0, stream);  // names the error, or T = 0
+  const int step = tokens_fitting(w, T);
+  if (step == 0) return MOE_ERR_WORKSPACE;
   void* scratch = static_scratch_on_current_device();
   if (!scratch) return MOE_ERR_CUDA;
-  return moe_layer_forward(w, x, T, y, scratch, kStaticScratchBytes, stream);
+  if (!x || !y) return MOE_ERR_ARG;
+  for (int t0 = 0; t0 < T; t0 += step) {
+    const int n = T - t0 < step ? T - t0 : step;
+    const size_t at = size_t(t0) * w->D;
+    if (moe_status s = moe_layer_forward(w, x + at, n, y + at, scratch, kStaticScratchBytes, stream)) return s;
+  }
+  return MOE_OK;
 }

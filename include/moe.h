@@ -138,15 +138,27 @@ typedef enum {
                                 others; 16..192 in steps of 16 is clamped to
                                 the path's size. The workspace always has
                                 room for 16-row blocks. */
-  MOE_OPT_DECODE_FUSED = 7   /* 1 (default): one token on the GEMV path runs top-k,
-                                gate/up and down in one cooperative kernel after
-                                the router logits (when the device can hold all
+  MOE_OPT_DECODE_FUSED = 7,  /* 1 (default): one token on the GEMV path runs the
+                                router logits, top-k, gate/up and down in one
+                                cooperative kernel (when the device can hold all
                                 its CTAs at once); 0: the separate routing and
                                 GEMV kernels */
+  MOE_OPT_CHUNK_TOKENS = 8   /* prompt chunking ("Optimizing on-device inference
+                                for Apple Silicon", "Bound temporary memory with
+                                prompt chunking"): a forward with more tokens
+                                than this runs as consecutive passes of at most
+                                this many tokens that reuse one workspace, so
+                                the workspace (and the host-entry staging) is
+                                sized for one pass. Default 8192; 0 turns it
+                                off (one pass over all T). Tokens are
+                                independent, so the output does not change. Set
+                                it before sizing the workspace. */
 } moe_option;
 
 /* Bytes of workspace one call with T tokens needs (pure host; 0 on bad
- * arguments). The workspace also holds the device status word. */
+ * arguments): the tables and buffers of one pass of min(T, chunk tokens)
+ * tokens (MOE_OPT_CHUNK_TOKENS), so it stops growing at the chunk size. The
+ * workspace also holds the device status word. */
 size_t moe_workspace_size(const moe_weights* w, int T);
 
 /* The whole layer on the GPU: routing (logits, top-k, weights, histogram,
@@ -158,10 +170,11 @@ size_t moe_workspace_size(const moe_weights* w, int T);
 moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uint16_t* y,
                              void* workspace, size_t workspace_bytes, void* stream);
 
-/* Same layer with HOST x and y: copies x into the workspace, runs
- * moe_layer_forward, copies y back and synchronises `stream` before it
- * returns. Page-locked host buffers make the copies asynchronous DMA. The
- * workspace must hold moe_workspace_size(w, T) + moe_host_staging_size(w, T). */
+/* Same layer with HOST x and y: for each pass (chunk) copies its x rows into
+ * the workspace, runs the layer, copies its y rows back; synchronises
+ * `stream` before it returns. Page-locked host buffers make the copies
+ * asynchronous DMA. The workspace must hold moe_workspace_size(w, T) +
+ * moe_host_staging_size(w, T) (x and y staging for one pass). */
 size_t moe_host_staging_size(const moe_weights* w, int T);
 moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, int T,
                                   uint16_t* y_host, void* workspace, size_t workspace_bytes,
@@ -169,7 +182,10 @@ moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, 
 
 /* Routing only (the first five steps of the layer), on `stream`, no host
  * sync; fills `view` with device pointers into the workspace. The tables are
- * the ones moe_layer_forward builds for the same T (same block_m). */
+ * the ones moe_layer_forward builds for the same T (same block_m). All T
+ * tokens are routed in one pass: for T above the chunk size the workspace
+ * must be sized with chunking off (MOE_OPT_CHUNK_TOKENS = 0), else the call
+ * returns MOE_ERR_WORKSPACE. */
 moe_status moe_route(const moe_weights* w, const uint16_t* x, int T, void* workspace,
                      size_t workspace_bytes, void* stream, moe_route_view* view);
 
@@ -211,9 +227,11 @@ moe_status moe_debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, 
  * it can synchronise the device or fail on fragmentation, and hosts that hand
  * their plug-ins only input and output buffers.)
  *   x, y, stream: as for moe_layer_forward(); the caller still owns them.
- *   Limit: T is accepted only while moe_workspace_size(w, T) <=
- *   MOE_STATIC_SCRATCH_BYTES (for the D=2048, E=256, k=8, I=512 layer that is
- *   T <= 451); larger T returns MOE_ERR_WORKSPACE and enqueues nothing.
+ *   Any T: the tokens run in consecutive passes of the largest count whose
+ *   workspace fits MOE_STATIC_SCRATCH_BYTES (and no larger than the chunk
+ *   size; for the D=2048, E=256, k=8, I=512 layer, 451 tokens). A layer whose
+ *   single-token workspace does not fit returns MOE_ERR_WORKSPACE and
+ *   enqueues nothing.
  *   The first call on each device looks up the array's device address (with
  *   that device current), so make that first call before any stream capture.
  *   Every call on a device shares the one array and leaves its contents

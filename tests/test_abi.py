@@ -114,6 +114,33 @@ def test_block_m_option(lib):
     moe.moe_set_option(moe.MOE_OPT_BLOCK_M, old)
 
 
+def test_chunk_option_bounds_the_workspace(lib):
+    old = moe.moe_get_option(moe.MOE_OPT_CHUNK_TOKENS)
+    assert old == 8192  # the default
+    for bad in (-1, (1 << 20) + 1):
+        assert moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, bad) == moe.MOE_ERR_ARG, bad
+    w = _weights()
+    try:
+        assert moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, 1000) == moe.MOE_OK
+        assert moe.moe_get_option(moe.MOE_OPT_CHUNK_TOKENS) == 1000
+        # one pass's tables: the size stops growing at the chunk size
+        n1000 = moe.moe_workspace_size(w, 1000)
+        assert moe.moe_workspace_size(w, 999) < n1000
+        assert moe.moe_workspace_size(w, 1001) == n1000 == moe.moe_workspace_size(w, 50000)
+        assert moe.moe_host_staging_size(w, 50000) == moe.moe_host_staging_size(w, 1000)
+        # chunking off: the size keeps growing with T
+        assert moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, 0) == moe.MOE_OK
+        assert moe.moe_workspace_size(w, 50000) > 40 * n1000
+        assert moe.moe_host_staging_size(w, 50000) > moe.moe_host_staging_size(w, 1000)
+        # a workspace one byte short of one pass is still rejected before anything runs
+        assert moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, 1000) == moe.MOE_OK
+        ws = 1 << 30
+        assert moe.moe_layer_forward(w, 0x2000, 5000, 0x9000000, ws, n1000 - 1, None) == moe.MOE_ERR_WORKSPACE
+        assert moe.moe_last_launch_count() == 0
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, old)
+
+
 def test_status_strings(lib):
     for s in range(7):
         assert moe.moe_status_string(s)

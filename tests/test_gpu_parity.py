@@ -251,6 +251,35 @@ def test_layer_prefill512_all_tokens(impl):
     check_output(y, O.forward(O.OracleLayer(layer), x), "prefill512")
 
 
+@pytest.mark.parametrize("chunk,extra", [(200, 0), (256, 3)], ids=["3-passes", "ragged-gemv-tail"])
+def test_layer_chunked_prefill(chunk, extra):
+    # Prompt chunking: 512 (+3) tokens in passes of `chunk` tokens reusing one
+    # workspace sized for a single pass. Passes 200, 200, 112; or 256, 256, 3,
+    # whose last pass takes the decode GEMV path. Each token's output matches
+    # the oracle, and the one-pass output up to the combine's summation order.
+    layer, x = config("prefill512")
+    if extra:
+        x = np.concatenate([x, x[:extra]])
+    T = x.shape[0]
+    dl = dev_layer("prefill512", layer)
+    y_one, _ = run_forward(dl, x)
+    old = moe.moe_get_option(moe.MOE_OPT_CHUNK_TOKENS)
+    try:
+        assert moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, chunk) == moe.MOE_OK
+        assert moe.moe_workspace_size(dl.w, T) == moe.moe_workspace_size(dl.w, chunk)
+        y, _ = run_forward(dl, x)
+        launches = moe.moe_last_launch_count()
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, old)
+    assert launches > 8  # more than one pass ran
+    # rows that took the same (GEMM) path in both runs agree up to summation
+    # order; a GEMV tail pass rounds differently (fp32 weights) and is held to
+    # the oracle only
+    same = T - extra
+    assert np.allclose(y[:same], y_one[:same], rtol=2 ** -7, atol=1e-6)
+    check_output(y, O.forward(O.OracleLayer(layer), x), f"chunked prefill, {chunk}-token passes")
+
+
 def _sample_tokens(idx, count, T):
     heavy = int(np.argmax(count))
     light = int(np.argmin(np.where(count > 0, count, 1 << 30)))
