@@ -495,6 +495,141 @@ def run_reference(args) -> dict | None:
     }
 
 
+# --- ablations of the source pages' design claims (--ablations) ----------------------------
+
+def run_ablations(args) -> dict:
+    """GB300 measurements of the design choices the pages ablate ("Optimizing
+    on-device inference for Apple Silicon": "Keep expert routing on the GPU",
+    "Match tile size to expert load", "Dequantise weights during matrix
+    multiplication"), each against this build's default on the same seeded
+    workloads. Every figure is a median over steps with L2 flushed between
+    them; one GPU, rank 0 only."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    import bit_moe_expert_routing_gb300 as moe
+    from bit_moe_expert_routing_gb300 import build as moe_build, synth
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return None
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    moe_build.build()
+    moe.lib()
+    stream = torch.cuda.current_stream(device)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    steps = max(args.steps, 10)
+    layers = {}
+
+    def layer_of(name):
+        if name not in layers:
+            layer, x_np = synth.make_config(name)
+            dl = moe.DeviceLayer(layer, device=device)
+            x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).to(device)
+            layers[name] = (layer, x_np, dl, x, torch.empty_like(x))
+        return layers[name]
+
+    def layer_ms(name, opts=None):
+        """Median ms of one forward of workload `name` with library options {option: value} set."""
+        opts = opts or {}
+        layer, x_np, dl, x, y = layer_of(name)
+        old = {k: moe.moe_get_option(k) for k in opts}
+        try:
+            for k, v in opts.items():
+                if moe.moe_set_option(k, v) != moe.MOE_OK:
+                    raise moe.MoEError(moe.MOE_ERR_ARG, f"option {k}={v}")
+            T = x.shape[0]
+            ws = dl.workspace(T)
+            ms = []
+            for i in range(3 + steps):
+                flush.zero_()
+                torch.cuda._sleep(HOST_LEAD_CYCLES)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                st = moe.moe_layer_forward(dl.w, x.data_ptr(), T, y.data_ptr(), ws.data_ptr(), ws.numel(), sp)
+                if st != moe.MOE_OK:
+                    raise moe.MoEError(st, "moe_layer_forward")
+                b.record(stream)
+                b.synchronize()
+                if i >= 3:
+                    ms.append(a.elapsed_time(b))
+            st = moe.moe_get_device_status(ctypes.c_void_p(ws.data_ptr()), sp)
+            if st != moe.MOE_OK:
+                raise moe.MoEError(st, "device status")
+            return sorted(ms)[len(ms) // 2]
+        finally:
+            for k, v in old.items():
+                moe.moe_set_option(k, v)
+
+    moe.moe_set_option(moe.MOE_OPT_FORCE_PATH, moe.PATH_AUTO)
+    out = {}
+    # 1. routing tables built on the GPU in stream order vs a host round trip
+    #    (block count copied back, stream synchronised) before the expert kernels
+    out["routing"] = {}
+    for name in ("prefill512", "prefill4096_zipf"):
+        g = layer_ms(name)
+        h = layer_ms(name, {moe.MOE_OPT_HOST_SYNC_ROUTING: 1})
+        out["routing"][name] = dict(gpu_resident_ms=g, host_sync_ms=h, speedup=h / g)
+    # 2. rows per block-map entry (the GEMM's token tile)
+    out["block_rows"] = {}
+    for name in ("prefill512", "prefill4096_zipf"):
+        out["block_rows"][name] = {str(bm): layer_ms(name, {moe.MOE_OPT_BLOCK_M: bm})
+                                   for bm in (16, 32, 64, 128, 192)}
+    # 3. operand roles: dequantised weights as the MMA's M (tensor memory, the
+    #    default) vs tokens as M (weights in shared memory), and CUDA cores
+    out["gemm_impl"] = {}
+    for name in ("prefill512", "prefill4096_zipf"):
+        out["gemm_impl"][name] = {
+            "weights_as_M_tcgen05": layer_ms(name, {moe.MOE_OPT_GEMM_IMPL: moe.GEMM_TENSOR_CORE}),
+            "tokens_as_M_tcgen05": layer_ms(name, {moe.MOE_OPT_GEMM_IMPL: moe.GEMM_TENSOR_CORE_SMEM}),
+            "cuda_cores": layer_ms(name, {moe.MOE_OPT_GEMM_IMPL: moe.GEMM_CUDA_CORE})}
+    # 4. separate dequantisation: expanding every touched expert matrix to bf16
+    #    in HBM, the pass a separate-dequant design runs before its GEMMs (its
+    #    GEMMs then read 3.6x the weight bytes), against the fused layer
+    layer, x_np, dl, x, y = layer_of("prefill4096_zipf")
+    ws = dl.workspace(x.shape[0])
+    st = moe.moe_route(dl.w, x.data_ptr(), x.shape[0], ws.data_ptr(), ws.numel(), sp, None)
+    if st != moe.MOE_OK:
+        raise moe.MoEError(st, "moe_route")
+    v = dl.view(x.shape[0], ws)
+    count = moe.ws_tensor(ws, v.count, (layer.E,), torch.int32).cpu().numpy()
+    touched = [int(e) for e in np.nonzero(count)[0]]
+    rows_k = {"gate": (layer.I, layer.D), "up": (layer.I, layer.D), "down": (layer.D, layer.I)}
+    outbuf = torch.empty(max(r * k for r, k in rows_k.values()), dtype=torch.int16, device=device)
+    ms = []
+    for i in range(3 + steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for e in touched + [None]:
+            for mname, (rows, K) in rows_k.items():
+                qm = getattr(dl.w, ("s_" + mname) if e is None else mname)
+                r = moe.moe_debug_dequant(qm, 0 if e is None else e, rows, K, outbuf.data_ptr(), sp)
+                if r != moe.MOE_OK:
+                    raise moe.MoEError(r, "moe_debug_dequant")
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            ms.append(a.elapsed_time(b))
+    n_exp = len(touched) + 1
+    written = n_exp * 3 * layer.D * layer.I * 2
+    read = n_exp * expert_bytes(layer.D, layer.I)
+    out["separate_dequant"] = dict(
+        workload="prefill4096_zipf", experts=n_exp, dequant_pass_ms=sorted(ms)[len(ms) // 2],
+        bf16_bytes_written=written, packed_bytes_read=read,
+        hbm_floor_ms=(written + read) / (measured_peaks()["hbm_gbs"] * 1e9) * 1e3,
+        fused_layer_ms=layer_ms("prefill4096_zipf"))
+    # 5. one token: the single fused kernel vs routing + two GEMV kernels
+    out["decode"] = dict(fused_ms=layer_ms("decode", {moe.MOE_OPT_DECODE_FUSED: 1}),
+                         separate_ms=layer_ms("decode", {moe.MOE_OPT_DECODE_FUSED: 0}))
+    return {"ablations": out, "steps": steps, "l2": "flushed between steps",
+            "timing": "median of CUDA-event step times, stream-launched"}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -505,10 +640,15 @@ def main(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ablations", action="store_true",
+                    help="print GB300 measurements of the pages' ablated design choices instead")
     args = ap.parse_args(argv)
     if args.impl == "ours":
         args.warmup = max(args.warmup, 3)  # at least three untimed steps
-    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.ablations:
+        out = run_ablations(args)
+    else:
+        out = run_reference(args) if args.impl == "reference" else run_ours(args)
     if out is not None:
         print(json.dumps(out), flush=True)
 

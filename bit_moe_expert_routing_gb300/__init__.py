@@ -33,6 +33,7 @@ MOE_OPT_TEST_WAIT_CYCLES = 5
 MOE_OPT_BLOCK_M = 6
 MOE_OPT_DECODE_FUSED = 7
 MOE_OPT_CHUNK_TOKENS = 8
+MOE_OPT_HOST_SYNC_ROUTING = 9
 
 PATH_AUTO, PATH_GEMV, PATH_GEMM = 0, 1, 2
 GEMM_TENSOR_CORE, GEMM_CUDA_CORE, GEMM_TENSOR_CORE_SMEM = 0, 1, 2

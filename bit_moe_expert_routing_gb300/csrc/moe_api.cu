@@ -25,6 +25,7 @@ struct Options {
   int block_m = 0;  // 0: the path's own block size
   int decode_fused = 1;
   int chunk_tokens = 8192;  // 0: one pass over all T
+  int host_sync_routing = 0;
 };
 Options g_opt;
 std::mutex g_mu;
@@ -276,6 +277,16 @@ static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, u
   if (path == Path::DecodeFused) return cuda_status(decode_fused(c));  // routing included
   cudaError_t err = route(c);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
+  if (g_opt.host_sync_routing) {
+    // the host-scheduled variant: the block count comes back to the host
+    // before the expert kernels are launched (a stream synchronisation)
+    static thread_local int* nb_host = nullptr;
+    if (!nb_host && cudaMallocHost(&nb_host, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpyAsync(nb_host, c.n_blocks, sizeof(int), cudaMemcpyDeviceToHost, c.stream) != cudaSuccess ||
+        cudaStreamSynchronize(c.stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (*nb_host < 0 || *nb_host > c.max_blocks) return MOE_ERR_CUDA;
+  }
   if (path == Path::Gemv) return cuda_status(gemv(c));
   if (path == Path::GemmWt) return cuda_status(gemm_wt(c));
   if (path == Path::GemmTc) return cuda_status(gemm_tc(c));
@@ -374,6 +385,10 @@ moe_status moe_set_option(int option, int value) {
       if (value < 0 || value > kMaxT) return MOE_ERR_ARG;
       g_opt.chunk_tokens = value;
       return MOE_OK;
+    case MOE_OPT_HOST_SYNC_ROUTING:
+      if (value < 0 || value > 1) return MOE_ERR_ARG;
+      g_opt.host_sync_routing = value;
+      return MOE_OK;
     case MOE_OPT_TEST_WAIT_CYCLES:
       if (value < 0) return MOE_ERR_ARG;
       g_opt.test_wait_cycles = value;
@@ -394,6 +409,7 @@ int moe_get_option(int option) {
     case MOE_OPT_BLOCK_M: return g_opt.block_m;
     case MOE_OPT_DECODE_FUSED: return g_opt.decode_fused;
     case MOE_OPT_CHUNK_TOKENS: return g_opt.chunk_tokens;
+    case MOE_OPT_HOST_SYNC_ROUTING: return g_opt.host_sync_routing;
     default: return -1;
   }
 }

@@ -143,7 +143,7 @@ typedef enum {
                                 cooperative kernel (when the device can hold all
                                 its CTAs at once); 0: the separate routing and
                                 GEMV kernels */
-  MOE_OPT_CHUNK_TOKENS = 8   /* prompt chunking ("Optimizing on-device inference
+  MOE_OPT_CHUNK_TOKENS = 8,  /* prompt chunking ("Optimizing on-device inference
                                 for Apple Silicon", "Bound temporary memory with
                                 prompt chunking"): a forward with more tokens
                                 than this runs as consecutive passes of at most
@@ -153,6 +153,14 @@ typedef enum {
                                 off (one pass over all T). Tokens are
                                 independent, so the output does not change. Set
                                 it before sizing the workspace. */
+  MOE_OPT_HOST_SYNC_ROUTING = 9 /* 1: the host-scheduled routing variant ("Keep
+                                expert routing on the GPU" describes it as the
+                                design that section replaces): after routing,
+                                each pass copies the expert block count to the
+                                host and synchronises the stream before the
+                                expert kernels are launched. The output is
+                                unchanged; the call blocks. For measurement.
+                                0 (default): no host synchronisation. */
 } moe_option;
 
 /* Bytes of workspace one call with T tokens needs (pure host; 0 on bad
