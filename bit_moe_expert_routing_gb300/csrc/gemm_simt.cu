@@ -213,7 +213,7 @@ cudaError_t gemm_simt(const Ctx& c) {
     return cudaErrorInvalidValue;
   SimtArgs a{c.x, c.h, w->gate, w->up, w->s_gate, w->s_up, c.blocks, c.n_blocks, c.perm, c.topk_w,
              c.h, c.y_acc, c.hdr, c.T, c.D, c.E, c.k, c.I};
-  cudaError_t err = zero_yacc(c);
+  cudaError_t err = c.yacc_zeroed ? cudaSuccess : zero_yacc(c);
   if (err != cudaSuccess) return err;
   gemm_simt_kernel<true><<<dim3(c.max_blocks, c.I / SBN), 256, simt_smem_bytes(2), c.stream>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;

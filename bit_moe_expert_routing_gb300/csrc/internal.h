@@ -43,6 +43,7 @@ struct Ctx {
   uint16_t* h;
   float* y_acc;
   cudaStream_t stream;
+  bool yacc_zeroed = false;  // set when routing already cleared y_acc
 };
 
 // Bookkeeping of launches: counts this library's kernels and, when kernel
@@ -51,8 +52,10 @@ void launch_done(const char* name, cudaStream_t s);
 void timing_begin(cudaStream_t s);
 
 // Routing: logits, top-k + weights + per-chunk histogram, scan + block map,
-// scatter. Returns the first CUDA error.
-cudaError_t route(const Ctx& c);
+// scatter. Returns the first CUDA error. With yacc_zeroed given, the router
+// kernel may also clear y_acc for the grouped GEMM that follows; then it sets
+// *yacc_zeroed.
+cudaError_t route(const Ctx& c, bool* yacc_zeroed = nullptr);
 
 // Combine accumulator: zero before, bf16 cast after the down projection.
 cudaError_t zero_yacc(const Ctx& c);

@@ -275,7 +275,7 @@ static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, u
   const Path path = plan(c);
   timing_begin(c.stream);
   if (path == Path::DecodeFused) return cuda_status(decode_fused(c));  // routing included
-  cudaError_t err = route(c);
+  cudaError_t err = route(c, path == Path::Gemv ? nullptr : &c.yacc_zeroed);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (g_opt.host_sync_routing) {
     // the host-scheduled variant: the block count comes back to the host

@@ -49,13 +49,21 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 template <bool WDUP, bool XF>
 __global__ void __launch_bounds__(kRtWarps * 32, 1)
     router_tree_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
-                       int T, int D, int E, float* __restrict__ logits, WsHeader* hdr) {
+                       int T, int D, int E, float* __restrict__ logits, WsHeader* hdr,
+                       float4* __restrict__ yacc, size_t yacc_n4) {
   // First kernel of every call: start the call's device status afresh. No
   // other CTA of this kernel reports, so nothing races with the clear.
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     hdr->status = 0;
     hdr->detail = 0;
     hdr->counter = 0;
+  }
+  // When the grouped GEMM follows, its combine accumulator is cleared here,
+  // a slice per CTA (the stores overlap this kernel's arithmetic)
+  if (yacc) {
+    const size_t cta = size_t(blockIdx.y) * gridDim.x + blockIdx.x, n_cta = size_t(gridDim.x) * gridDim.y;
+    for (size_t i = cta * blockDim.x + threadIdx.x; i < yacc_n4; i += n_cta * blockDim.x)
+      yacc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   extern __shared__ __align__(16) uint8_t rt_smem_raw[];
   uint8_t* wsb = rt_smem_raw;                            // [2][kRtExp][kRtDC] of float or float2
@@ -228,16 +236,30 @@ __global__ void __launch_bounds__(kTopkThreads)
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int tt = warp; tt < kChunkTokens; tt += blockDim.x / 32) {
-    const int t = blockIdx.x * kChunkTokens + tt;
-    if (t >= T) break;
-    int myi;
-    float myw;
-    select_topk<MPL>(logits + size_t(t) * E, E, k, myi, myw);
-    if (lane < k) {
-      topk_idx[size_t(t) * k + lane] = myi;
-      topk_w[size_t(t) * k + lane] = myw;
-      atomicAdd(&hist[myi], 1);
+  // a warp's tokens: their logits are all loaded first (the loads overlap),
+  // then selected one after another
+  constexpr int kPerWarp = kChunkTokens / (kTopkThreads / 32);
+  constexpr int kAhead = MPL <= 8 ? kPerWarp : 1;  // keys held at once
+  static_assert(kPerWarp * (kTopkThreads / 32) == kChunkTokens && kPerWarp % kAhead == 0, "tokens per warp");
+  for (int g0 = 0; g0 < kPerWarp; g0 += kAhead) {
+    unsigned key[kAhead][MPL];
+#pragma unroll
+    for (int i = 0; i < kAhead; ++i) {
+      const int t = blockIdx.x * kChunkTokens + warp + (g0 + i) * (kTopkThreads / 32);
+      if (t < T) load_logit_keys<MPL>(logits + size_t(t) * E, E, key[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < kAhead; ++i) {
+      const int t = blockIdx.x * kChunkTokens + warp + (g0 + i) * (kTopkThreads / 32);
+      if (t >= T) break;
+      int myi;
+      float myw;
+      select_topk_keys<MPL>(key[i], k, myi, myw);
+      if (lane < k) {
+        topk_idx[size_t(t) * k + lane] = myi;
+        topk_w[size_t(t) * k + lane] = myw;
+        atomicAdd(&hist[myi], 1);
+      }
     }
   }
   __syncthreads();
@@ -283,12 +305,18 @@ __global__ void __launch_bounds__(1024)
   __shared__ int s_warp[32];
   __shared__ int s_tot_rows, s_tot_blocks;
   const int e = threadIdx.x;
+  // the per-chunk counts of expert e are read kScanBatch at a time (independent
+  // loads in flight together): first for the total, then again to replace
+  // each by its base (the expert's offset plus the counts of earlier chunks)
+  constexpr int kScanBatch = 8;
   int total = 0;
   if (e < E) {
-    for (int c = 0; c < n_chunks; ++c) {
-      const int v = chunk[size_t(c) * E + e];
-      chunk[size_t(c) * E + e] = total;
-      total += v;
+    for (int c0 = 0; c0 < n_chunks; c0 += kScanBatch) {
+      int v[kScanBatch];
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j) v[j] = c0 + j < n_chunks ? chunk[size_t(c0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j) total += v[j];
     }
   }
   const int nb = (total + BM - 1) / BM;
@@ -297,7 +325,17 @@ __global__ void __launch_bounds__(1024)
   if (e < E) {
     count[e] = total;
     off[e] = ex_off;
-    for (int c = 0; c < n_chunks; ++c) chunk[size_t(c) * E + e] += ex_off;
+    int run = ex_off;
+    for (int c0 = 0; c0 < n_chunks; c0 += kScanBatch) {
+      int v[kScanBatch];
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j) v[j] = c0 + j < n_chunks ? chunk[size_t(c0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j) {
+        if (c0 + j < n_chunks) chunk[size_t(c0 + j) * E + e] = run;
+        run += v[j];
+      }
+    }
     for (int b = 0; b < nb; ++b) {
       const int idx = ex_nb + b;
       if (idx < max_blocks) {
@@ -540,7 +578,7 @@ cudaError_t route_logits_small(const Ctx& c) {
   return cudaSuccess;
 }
 
-cudaError_t route(const Ctx& c) {
+cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
   const moe_weights* w = c.w;
   cudaError_t err;
   // one CTA of 1024 threads does the small-T top-k: up to 16 logits per lane
@@ -561,8 +599,11 @@ cudaError_t route(const Ctx& c) {
     auto* rk = router_tree_kernel<kRtWdup, kRtXf>;
     const size_t smem = rt_smem<kRtWdup, kRtXf>();
     if (!ensure_smem_limit(reinterpret_cast<const void*>(rk), int(smem))) return cudaErrorInvalidValue;
+    const bool zero = yacc_zeroed != nullptr;
     rk<<<dim3((c.T + kRtTok - 1) / kRtTok, (c.E + kRtExp - 1) / kRtExp), kRtWarps * 32, smem, c.stream>>>(
-        c.x, w->router_w, w->router_bias, c.T, c.D, c.E, c.logits, c.hdr);
+        c.x, w->router_w, w->router_bias, c.T, c.D, c.E, c.logits, c.hdr,
+        zero ? reinterpret_cast<float4*>(c.y_acc) : nullptr, zero ? size_t(c.T) * c.D / 4 : 0);
+    if (zero) *yacc_zeroed = true;
   }
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done("router_logits", c.stream);

@@ -141,6 +141,15 @@ def test_chunk_option_bounds_the_workspace(lib):
         moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, old)
 
 
+def test_host_sync_routing_option(lib):
+    assert moe.moe_get_option(moe.MOE_OPT_HOST_SYNC_ROUTING) == 0  # off by default
+    for bad in (-1, 2):
+        assert moe.moe_set_option(moe.MOE_OPT_HOST_SYNC_ROUTING, bad) == moe.MOE_ERR_ARG
+    assert moe.moe_set_option(moe.MOE_OPT_HOST_SYNC_ROUTING, 1) == moe.MOE_OK
+    assert moe.moe_get_option(moe.MOE_OPT_HOST_SYNC_ROUTING) == 1
+    assert moe.moe_set_option(moe.MOE_OPT_HOST_SYNC_ROUTING, 0) == moe.MOE_OK
+
+
 def test_status_strings(lib):
     for s in range(7):
         assert moe.moe_status_string(s)

@@ -280,6 +280,22 @@ def test_layer_chunked_prefill(chunk, extra):
     check_output(y, O.forward(O.OracleLayer(layer), x), f"chunked prefill, {chunk}-token passes")
 
 
+@pytest.mark.parametrize("path", [moe.PATH_GEMV, moe.PATH_GEMM], ids=["gemv", "gemm"])
+def test_layer_host_synchronised_routing(path):
+    # the host round trip after routing changes nothing in the result
+    layer, x = config("prefill512")
+    x = x[:3] if path == moe.PATH_GEMV else x
+    dl = dev_layer("prefill512", layer)
+    y_ref, _ = run_forward(dl, x, path)
+    assert moe.moe_set_option(moe.MOE_OPT_HOST_SYNC_ROUTING, 1) == moe.MOE_OK
+    try:
+        y, _ = run_forward(dl, x, path)
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_HOST_SYNC_ROUTING, 0)
+    assert np.allclose(y, y_ref, rtol=2 ** -7, atol=1e-6)
+    check_output(y, O.forward(O.OracleLayer(layer), x), "host-synchronised routing")
+
+
 def _sample_tokens(idx, count, T):
     heavy = int(np.argmax(count))
     light = int(np.argmin(np.where(count > 0, count, 1 << 30)))
