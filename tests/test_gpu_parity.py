@@ -352,6 +352,30 @@ def test_layer_shapes(shape, T):
         check_output(y, ref, f"{shape} T={T} path={p} impl={impl}")
 
 
+# Largest sizes the boundary accepts along each axis (E = 1024 with k = 32,
+# D = 16384, I = 4096), and E = 512, the largest the one-token fused kernel
+# takes (16 logits per lane). Where a path's limits exclude a shape, the call
+# falls back to the path that takes it; every result is held to the oracle.
+@pytest.mark.parametrize("shape", [dict(D=128, E=1024, k=32, I=128), dict(D=16384, E=4, k=2, I=128),
+                                   dict(D=128, E=4, k=2, I=4096), dict(D=256, E=512, k=8, I=128)],
+                         ids=["E1024k32", "D16384", "I4096", "E512"])
+@pytest.mark.parametrize("T", [1, 7, 130])
+def test_layer_max_shapes(shape, T):
+    layer = synth.make_layer(41, **shape)
+    x = synth.make_x(41, T, shape["D"])
+    dl = moe.DeviceLayer(layer)
+    ref = O.forward(O.OracleLayer(layer), x)
+    for p in (moe.PATH_GEMM, moe.PATH_GEMV):
+        if p == moe.PATH_GEMV and T > 8:
+            continue
+        y, ws = run_forward(dl, x, p)
+        check_output(y, ref, f"{shape} T={T} path={p}")
+        v = dl.view(T, ws)
+        idx = moe.ws_tensor(ws, v.topk_idx, (T, layer.k), torch.int32).cpu().numpy()
+        _, ridx, _ = O.route(O.OracleLayer(layer), x)
+        assert np.array_equal(idx, ridx)
+
+
 def test_zero_tokens_is_noop():
     layer, _ = config("tiny")
     dl = dev_layer("tiny", layer)
