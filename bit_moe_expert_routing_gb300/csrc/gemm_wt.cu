@@ -523,11 +523,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
           dq8_bf16(w1.y, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 20));
           dq8_bf16(w1.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 24));
           dq8_bf16(w1.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 28));
-          // the code stage goes back to the TMA: the arrival releases this
-          // warp's reads of it (they have returned: the values above use them)
+          // the code stage goes back to the TMA only after every lane's reads
+          // of it have completed: the proxy fence orders them before the
+          // TMA's (async proxy) next write to the stage
+          fence_proxy_async();
           __syncwarp();
           if (lane == 0) mbar_arrive(cempty(cs));
-          if (hb == 0 && !(ok = mbar_wait(aempty(s), ph ^ 1u, abort_flag, a.hdr))) break;
+          if (hb == 0) {
+            if (!(ok = mbar_wait(aempty(s), ph ^ 1u, abort_flag, a.hdr))) break;
+            tc_fence_after();  // the MMAs that read this A stage have completed
+          }
           tmem_st32(tmem + (uint32_t(q * 32) << 16) + kAColBase + s * kAStageCols + hb * kAGroupCols, o);
         }
         if (!ok) break;

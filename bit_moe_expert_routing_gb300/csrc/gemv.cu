@@ -506,8 +506,7 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
     cp_rows(fsm + L.dbi + j * dsb, mq.biases + row0 * Gi, dsb);
   };
 
-  // --- start: barriers and byte counts; bulk copies of the router rows and of
-  // the shared expert's (slot k) codes, which do not depend on the routing.
+  // --- start: barriers and byte counts; bulk copies of the router rows.
   if (warp == 0) {
     if (lane == 0) {
       *abort_flag = 0;
@@ -523,11 +522,6 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
     if (lane < n_rt)
       bulk_g2s(bar0 + uint32_t(L.wr) + lane * D * 4, a.router_w + size_t(blockIdx.x + lane * gridDim.x) * D, D * 4,
                rbar);
-    if (lane >= 2 && lane < 6) {
-      const int m = (lane - 2) >> 1;
-      if (has_item(m) && item_slot(m) == k) item_codes(m, E, (lane - 2) & 1);
-    }
-    if (lane == 6 && has_down) down_codes(k, E);
   }
   // the token row: bf16 as is (router) and chunk-major fp32 (expert dot products)
   float4* xs4 = reinterpret_cast<float4*>(fsm + L.xs4);
@@ -578,13 +572,14 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
       }
     }
     __syncwarp();
-    // bulk copies of the routed codes: lanes 0..3 the two items' gate and up,
-    // lanes 4.. the down slots
+    // bulk copies of the codes, the shared expert's (slot k) included: they
+    // are issued only now, since copies landing during the top-k slow it down.
+    // Lanes 0..3 take the two items' gate and up, lanes 4..31 the down slots.
     if (lane < 4) {
       const int m = lane >> 1;
-      if (has_item(m) && item_slot(m) < k) item_codes(m, s_exp[item_slot(m)], lane & 1);
-    } else if (lane < 4 + k && has_down) {
-      down_codes(lane - 4, s_exp[lane - 4]);
+      if (has_item(m)) item_codes(m, s_exp[item_slot(m)], lane & 1);
+    } else if (has_down) {
+      for (int j = lane - 4; j < S; j += 28) down_codes(j, s_exp[j]);
     }
   }
   __syncthreads();

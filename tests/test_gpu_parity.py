@@ -376,6 +376,27 @@ def test_layer_max_shapes(shape, T):
         assert np.array_equal(idx, ridx)
 
 
+def test_long_k_gemm_is_stable_over_repeats():
+    # 128 pipeline stages per gate/up tile (D = 16384): a stage of packed
+    # codes handed back to the TMA before every lane's reads of it completed
+    # was overwritten now and then (scattered errors in about half the runs).
+    # Ten runs on workspaces holding stale bytes must all match the oracle.
+    shape = dict(D=16384, E=4, k=2, I=128)
+    layer = synth.make_layer(41, **shape)
+    x = synth.make_x(41, 130, shape["D"])
+    dl = moe.DeviceLayer(layer)
+    ref = O.forward(O.OracleLayer(layer), x)
+    assert moe.moe_set_option(moe.MOE_OPT_FORCE_PATH, moe.PATH_GEMM) == moe.MOE_OK
+    assert moe.moe_set_option(moe.MOE_OPT_GEMM_IMPL, moe.GEMM_TENSOR_CORE) == moe.MOE_OK
+    xd = x_to_device(x)
+    for r in range(10):
+        ws = dl.workspace(130)
+        ws.fill_(0x3F)
+        y = bf16_to_np(dl.forward(xd, workspace=ws))
+        torch.cuda.synchronize()
+        check_output(y, ref, f"long-K GEMM, repeat {r}")
+
+
 def test_zero_tokens_is_noop():
     layer, _ = config("tiny")
     dl = dev_layer("tiny", layer)
