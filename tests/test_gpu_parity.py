@@ -353,12 +353,14 @@ def test_layer_shapes(shape, T):
 
 
 # Largest sizes the boundary accepts along each axis (E = 1024 with k = 32,
-# D = 16384, I = 4096), and E = 512, the largest the one-token fused kernel
-# takes (16 logits per lane). Where a path's limits exclude a shape, the call
+# D = 16384, I = 4096), E = 512, the largest the one-token fused kernel takes
+# (16 logits per lane), and k = 30 on the fused kernel (more down slots than
+# the 28 lanes that issue their copies in one pass). Where a path's limits exclude a shape, the call
 # falls back to the path that takes it; every result is held to the oracle.
 @pytest.mark.parametrize("shape", [dict(D=128, E=1024, k=32, I=128), dict(D=16384, E=4, k=2, I=128),
-                                   dict(D=128, E=4, k=2, I=4096), dict(D=256, E=512, k=8, I=128)],
-                         ids=["E1024k32", "D16384", "I4096", "E512"])
+                                   dict(D=128, E=4, k=2, I=4096), dict(D=256, E=512, k=8, I=128),
+                                   dict(D=128, E=64, k=30, I=128)],
+                         ids=["E1024k32", "D16384", "I4096", "E512", "k30-fused"])
 @pytest.mark.parametrize("T", [1, 7, 130])
 def test_layer_max_shapes(shape, T):
     layer = synth.make_layer(41, **shape)
