@@ -524,19 +524,24 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
           dq8_bf16(w1.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 24));
           dq8_bf16(w1.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 28));
           // the code stage goes back to the TMA only after every lane's reads
-          // of it have completed: the proxy fence orders them before the
-          // TMA's (async proxy) next write to the stage
-          fence_proxy_async();
+          // of it have returned: one instruction consumes all the words read
+          // (a warp issues in order, so it waits for every lane's loads), and
+          // the arrival depends on its result
+          const uint32_t got = w0.x ^ w0.y ^ w0.z ^ w0.w ^ w1.x ^ w1.y ^ w1.z ^ w1.w;
+          uint32_t zero;
+          asm volatile("and.b32 %0, %1, 0;" : "=r"(zero) : "r"(got));
           __syncwarp();
-          if (lane == 0) mbar_arrive(cempty(cs));
+          if (lane == int(zero)) mbar_arrive(cempty(cs));
           if (hb == 0) {
             if (!(ok = mbar_wait(aempty(s), ph ^ 1u, abort_flag, a.hdr))) break;
             tc_fence_after();  // the MMAs that read this A stage have completed
           }
           tmem_st32(tmem + (uint32_t(q * 32) << 16) + kAColBase + s * kAStageCols + hb * kAGroupCols, o);
+          // tcgen05.st reads its source registers asynchronously: wait before
+          // the next group's values overwrite them
+          tmem_wait_st();
         }
         if (!ok) break;
-        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(afull(s));

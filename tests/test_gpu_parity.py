@@ -379,10 +379,12 @@ def test_layer_max_shapes(shape, T):
 
 
 def test_long_k_gemm_is_stable_over_repeats():
-    # 128 pipeline stages per gate/up tile (D = 16384): a stage of packed
-    # codes handed back to the TMA before every lane's reads of it completed
-    # was overwritten now and then (scattered errors in about half the runs).
-    # Ten runs on workspaces holding stale bytes must all match the oracle.
+    # 128 pipeline stages per gate/up tile (D = 16384). A dequantising warp
+    # once reused the registers of a tensor-memory store for the next group
+    # before the store had read them (tcgen05.st reads its sources
+    # asynchronously), which corrupted a group now and then: scattered errors
+    # in about half the runs. Ten runs on workspaces holding stale bytes must
+    # all match the oracle.
     shape = dict(D=16384, E=4, k=2, I=128)
     layer = synth.make_layer(41, **shape)
     x = synth.make_x(41, 130, shape["D"])
