@@ -441,12 +441,6 @@ template <int N>
 __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-// `bytes` (a multiple of 16) from global to shared memory, 16 bytes per
-// thread and step, by all threads of the CTA.
-__device__ __forceinline__ void cp_rows(uint8_t* dst, const void* src, uint32_t bytes) {
-  const uint8_t* s = static_cast<const uint8_t*>(src);
-  for (uint32_t o = threadIdx.x * 16u; o < bytes; o += blockDim.x * 16u) cp16(dst + o, s + o);
-}
 
 template <int MPL>
 __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArgs a) {
@@ -481,16 +475,22 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
     bulk_g2s(bar0 + uint32_t(m == 0 ? L.item[0] : L.item[1]) + part * icb, mq.codes + row0 * (D / 8), icb,
              bar0 + 8u * m);
   };
-  auto item_small = [&](int m, int e) {
+  // Item m's four small rows (gate scales, gate biases, up scales, up
+  // biases), isb bytes each, as 16-byte pieces p = 0 .. 4 * isb / 16 - 1:
+  // each thread issues the pieces p = first, first + blockDim.x, ...
+  auto item_small = [&](int m, int e, int first) {
     const int item = blockIdx.x + m * gridDim.x, i0 = (item % RB) * kFdRows;
     const bool sh = (e == E);
     const moe_qmatrix mg = sh ? a.s_gate : a.gate, mu = sh ? a.s_up : a.up;
     const size_t row0 = size_t(sh ? 0 : e) * I + i0;
     uint8_t* dst = fsm + (m == 0 ? L.item[0] : L.item[1]) + 2 * icb;
-    cp_rows(dst, mg.scales + row0 * G, isb);
-    cp_rows(dst + isb, mg.biases + row0 * G, isb);
-    cp_rows(dst + 2 * isb, mu.scales + row0 * G, isb);
-    cp_rows(dst + 3 * isb, mu.biases + row0 * G, isb);
+    const int per = int(isb / 16);
+    for (int p = first; p < 4 * per; p += blockDim.x) {
+      const int r = p / per, o = (p % per) * 16;
+      const moe_qmatrix& mq = r < 2 ? mg : mu;
+      const uint16_t* src = ((r & 1) ? mq.biases : mq.scales) + row0 * G;
+      cp16(dst + r * isb + o, reinterpret_cast<const uint8_t*>(src) + o);
+    }
   };
   auto down_codes = [&](int j, int e) {
     const bool sh = (e == E);
@@ -498,12 +498,20 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
     const size_t row0 = size_t(sh ? 0 : e) * D + d0;
     bulk_g2s(bar0 + uint32_t(L.down) + j * dcb, mq.codes + row0 * (I / 8), dcb, bar0 + 16u);
   };
-  auto down_small = [&](int j, int e) {
-    const bool sh = (e == E);
-    const moe_qmatrix mq = sh ? a.s_down : a.down;
-    const size_t row0 = size_t(sh ? 0 : e) * D + d0;
-    cp_rows(fsm + L.dsc + j * dsb, mq.scales + row0 * Gi, dsb);
-    cp_rows(fsm + L.dbi + j * dsb, mq.biases + row0 * Gi, dsb);
+  // The down slots' scale and bias rows, dsb bytes each, as 16-byte pieces
+  // q = 0 .. S * 2 * dsb / 16 - 1 (slot, then scales / biases), spread over
+  // all threads like the items' pieces
+  auto down_small = [&](int first) {
+    const int per = int(dsb / 16);
+    for (int q = first; q < S * 2 * per; q += blockDim.x) {
+      const int j = q / (2 * per), r = (q / per) & 1, o = (q % per) * 16;
+      const int e = s_exp[j];
+      const bool sh = (e == E);
+      const moe_qmatrix mq = sh ? a.s_down : a.down;
+      const size_t row0 = size_t(sh ? 0 : e) * D + d0;
+      const uint16_t* src = (r ? mq.biases : mq.scales) + row0 * Gi;
+      cp16(fsm + (r ? L.dbi : L.dsc) + j * dsb + o, reinterpret_cast<const uint8_t*>(src) + o);
+    }
   };
 
   // --- start: barriers and byte counts; bulk copies of the router rows.
@@ -584,15 +592,14 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
   }
   __syncthreads();
   // groups 0, 1, 2: the scales and biases (small rows, by cp.async) of item 0,
-  // item 1 and the down slots. Issued only now: cp.async requests still in
-  // flight hold up the top-k's reads of the logits behind them.
+  // item 1 and the down slots, a few 16-byte pieces per thread (item 1's
+  // pieces start half a CTA further, so other threads take them)
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
-    if (has_item(m)) item_small(m, s_exp[item_slot(m)]);
+    if (has_item(m)) item_small(m, s_exp[item_slot(m)], (threadIdx.x + m * (blockDim.x / 2)) % blockDim.x);
     cp_commit();
   }
-  if (has_down)
-    for (int j = 0; j < S; ++j) down_small(j, s_exp[j]);
+  if (has_down) down_small(threadIdx.x);
   cp_commit();
 
   // --- gate/up: warp w takes row w of each item
