@@ -226,7 +226,7 @@ constexpr bool kRtWdup = false, kRtXf = false;  // measured fastest: the extra s
 
 // Top-k and weights of each token of a chunk, and the chunk's per-expert
 // assignment counts. One warp per token.
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 1024;
 template <int MPL>
 __global__ void __launch_bounds__(kTopkThreads)
     topk_hist_kernel(const float* __restrict__ logits, int T, int E, int k,
