@@ -21,24 +21,22 @@
 namespace moe {
 namespace {
 
-// Router logits in the order above for larger T. A warp computes 8 tokens x
-// 8 experts: lane l holds partial sum l of each of those 64 logits (as 32
-// pairs of tokens for the packed FMA), and the shuffle tree reduces them at
-// the end. A CTA of kRtWarps warps covers kRtTok tokens x kRtExp experts. D
-// is walked in chunks of kRtDC, staged in shared memory one chunk ahead:
-//   W  (router-weight rows): WDUP = false, fp32 as in memory (cp.async);
-//      WDUP = true, each value twice, the (w, w) operand of the packed FMA;
-//   x  (token rows): XF = false, words holding one column of two tokens as
-//      bf16; XF = true, the same pair as two fp32 values.
-// With both set the inner step is loads and paired FMAs only.
-constexpr int kRtTok = 32, kRtExp = 32, kRtWarps = 16, kRtDC = 128;
-template <bool WDUP, bool XF>
-constexpr size_t rt_w_bytes() { return size_t(2) * kRtExp * kRtDC * (WDUP ? 8 : 4); }
-template <bool WDUP, bool XF>
-constexpr size_t rt_smem() { return rt_w_bytes<WDUP, XF>() + size_t(2) * (kRtTok / 2) * kRtDC * (XF ? 8 : 4); }
-static_assert((kRtTok / 8) * (kRtExp / 8) == kRtWarps, "one 8 x 8 logit tile per warp");
-static_assert((kRtTok / 2) * (kRtDC / 4) == kRtWarps * 32, "one token-pair item per thread and chunk");
-static_assert(kRtExp * (kRtDC / 4) == 2 * kRtWarps * 32, "two router-weight pieces per thread and chunk");
+// Router logits in the order above for larger T. A warp computes 16 tokens x
+// 8 experts: lane l holds partial sum l of each of those 128 logits (as 64
+// pairs of tokens for the packed FMA), and the tree reduces them at the end.
+// A CTA of kRtWarps warps covers kRtTok tokens x kRtExp experts. D is walked
+// in chunks of kRtDC, staged in shared memory one chunk ahead: W (router-
+// weight rows) fp32 as in memory, by cp.async; x as words holding one column
+// of two tokens in bf16.
+constexpr int kRtTok = 32, kRtExp = 32, kRtWarps = 8, kRtDC = 256;
+constexpr int kRtWT = 16, kRtWE = 8;  // tokens and experts of a warp
+constexpr size_t kRtWBytes = size_t(2) * kRtExp * kRtDC * 4;
+constexpr size_t kRtSmem = kRtWBytes + size_t(2) * (kRtTok / 2) * kRtDC * 4;
+static_assert((kRtTok / kRtWT) * (kRtExp / kRtWE) == kRtWarps, "one 16 x 8 logit tile per warp");
+constexpr int kRtXItems = (kRtTok / 2) * (kRtDC / 4) / (kRtWarps * 32);  // token-pair items per thread and chunk
+constexpr int kRtWItems = kRtExp * (kRtDC / 4) / (kRtWarps * 32);        // router-weight pieces per thread and chunk
+static_assert(kRtXItems * kRtWarps * 32 == (kRtTok / 2) * (kRtDC / 4), "whole token-pair items");
+static_assert(kRtWItems * kRtWarps * 32 == kRtExp * (kRtDC / 4), "whole router-weight pieces");
 
 __device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -46,7 +44,20 @@ __device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit_all() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-template <bool WDUP, bool XF>
+// One level of the recursive halving: values 0..2H-1 of each lane, partner
+// lane ^ o; the lane keeps the lower H (o bit clear) or the upper H, moved
+// down, each plus the partner's value of the same index.
+template <int H>
+__device__ __forceinline__ void halve_level(float (&v)[128], int lane, int o) {
+  const bool upper = (lane & o) != 0;
+#pragma unroll
+  for (int i = 0; i < H; ++i) {
+    const float send = upper ? v[i] : v[i + H];
+    const float keep = upper ? v[i + H] : v[i];
+    v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+  }
+}
+
 __global__ void __launch_bounds__(kRtWarps * 32, 1)
     router_tree_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
                        int T, int D, int E, float* __restrict__ logits, WsHeader* hdr,
@@ -66,80 +77,56 @@ __global__ void __launch_bounds__(kRtWarps * 32, 1)
       yacc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   extern __shared__ __align__(16) uint8_t rt_smem_raw[];
-  uint8_t* wsb = rt_smem_raw;                            // [2][kRtExp][kRtDC] of float or float2
-  uint8_t* xpb = rt_smem_raw + rt_w_bytes<WDUP, XF>();  // [2][kRtTok/2][kRtDC] of bf16 pair or float2
+  float* wsb = reinterpret_cast<float*>(rt_smem_raw);                    // [2][kRtExp][kRtDC]
+  uint32_t* xpb = reinterpret_cast<uint32_t*>(rt_smem_raw + kRtWBytes);  // [2][kRtTok/2][kRtDC]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t0 = blockIdx.x * kRtTok, eb = blockIdx.y * kRtExp;
-  const int tg = warp / (kRtExp / 8), eg = warp % (kRtExp / 8);  // token pairs 4tg.., experts 8eg..
+  const int tg = warp / (kRtExp / kRtWE), eg = warp % (kRtExp / kRtWE);  // token pairs 8tg.., experts 8eg..
 
-  // W pieces: 16 bytes (4 columns) of router-weight row r, rows eb .. (clamped to E-1)
-  float4 wreg[2];
-  auto w_piece = [&](int m, int& r, int& c4) {
-    const int i = threadIdx.x + m * blockDim.x;
-    r = i / (kRtDC / 4);
-    c4 = i % (kRtDC / 4);
-  };
+  // W pieces m: 16 bytes (4 columns) of router-weight row r (clamped to E-1)
   auto issue_w = [&](int buf, int d0, int dc) {
 #pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      int r, c4;
-      w_piece(m, r, c4);
-      const float* src = wr + size_t(min(eb + r, E - 1)) * D + d0 + c4 * 4;
-      if (WDUP) {
-        wreg[m] = 4 * c4 < dc ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
-      } else if (4 * c4 < dc) {
-        cp_async16_cg(smem_u32(wsb + ((size_t(buf) * kRtExp + r) * kRtDC + c4 * 4) * 4), src);
-      }
+    for (int m = 0; m < kRtWItems; ++m) {
+      const int i = threadIdx.x + m * blockDim.x, r = i / (kRtDC / 4), c4 = i % (kRtDC / 4);
+      if (4 * c4 < dc)
+        cp_async16_cg(smem_u32(wsb + (size_t(buf) * kRtExp + r) * kRtDC + c4 * 4),
+                      wr + size_t(min(eb + r, E - 1)) * D + d0 + c4 * 4);
     }
-    if (!WDUP) cp_async_commit_all();
+    cp_async_commit_all();
   };
-  auto store_w = [&](int buf) {
-    if (WDUP) {
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        int r, c4;
-        w_piece(m, r, c4);
-        float4* dst = reinterpret_cast<float4*>(wsb + ((size_t(buf) * kRtExp + r) * kRtDC + c4 * 4) * 8);
-        dst[0] = make_float4(wreg[m].x, wreg[m].x, wreg[m].y, wreg[m].y);
-        dst[1] = make_float4(wreg[m].z, wreg[m].z, wreg[m].w, wreg[m].w);
-      }
-    }
-  };
-  // this thread's x item: token pair ip, columns 4 dq .. +3 of the chunk
-  const int ip = threadIdx.x / (kRtDC / 4), dq = threadIdx.x % (kRtDC / 4);
-  const int ta = t0 + 2 * ip, tb = ta + 1;
-  uint2 xa = make_uint2(0u, 0u), xb = xa;
+  // x items m: token pair ip, columns 4 dq .. +3 of the chunk
+  uint2 xa[kRtXItems], xb[kRtXItems];
   auto load_x = [&](int d0, int dc) {
-    const bool in = 4 * dq < dc;
-    xa = (in && ta < T) ? *reinterpret_cast<const uint2*>(x + size_t(ta) * D + d0 + 4 * dq) : make_uint2(0u, 0u);
-    xb = (in && tb < T) ? *reinterpret_cast<const uint2*>(x + size_t(tb) * D + d0 + 4 * dq) : make_uint2(0u, 0u);
+#pragma unroll
+    for (int m = 0; m < kRtXItems; ++m) {
+      const int i = threadIdx.x + m * blockDim.x, ip = i / (kRtDC / 4), dq = i % (kRtDC / 4);
+      const int ta = t0 + 2 * ip, tb = ta + 1;
+      const bool in = 4 * dq < dc;
+      xa[m] = (in && ta < T) ? *reinterpret_cast<const uint2*>(x + size_t(ta) * D + d0 + 4 * dq) : make_uint2(0u, 0u);
+      xb[m] = (in && tb < T) ? *reinterpret_cast<const uint2*>(x + size_t(tb) * D + d0 + 4 * dq) : make_uint2(0u, 0u);
+    }
   };
-  auto store_x = [&](int buf) {
-    if (XF) {  // (token ta, token tb) of each column as two fp32 values
-      float4* dst = reinterpret_cast<float4*>(xpb + ((size_t(buf) * (kRtTok / 2) + ip) * kRtDC + 4 * dq) * 8);
-      dst[0] = make_float4(__uint_as_float(xa.x << 16), __uint_as_float(xb.x << 16),
-                           __uint_as_float(xa.x & 0xFFFF0000u), __uint_as_float(xb.x & 0xFFFF0000u));
-      dst[1] = make_float4(__uint_as_float(xa.y << 16), __uint_as_float(xb.y << 16),
-                           __uint_as_float(xa.y & 0xFFFF0000u), __uint_as_float(xb.y & 0xFFFF0000u));
-    } else {  // word = (token ta, token tb) of one column, bf16
-      *reinterpret_cast<uint4*>(xpb + ((size_t(buf) * (kRtTok / 2) + ip) * kRtDC + 4 * dq) * 4) =
-          make_uint4(__byte_perm(xa.x, xb.x, 0x5410), __byte_perm(xa.x, xb.x, 0x7632),
-                     __byte_perm(xa.y, xb.y, 0x5410), __byte_perm(xa.y, xb.y, 0x7632));
+  auto store_x = [&](int buf) {  // word = (token ta, token tb) of one column, bf16
+#pragma unroll
+    for (int m = 0; m < kRtXItems; ++m) {
+      const int i = threadIdx.x + m * blockDim.x, ip = i / (kRtDC / 4), dq = i % (kRtDC / 4);
+      *reinterpret_cast<uint4*>(xpb + (size_t(buf) * (kRtTok / 2) + ip) * kRtDC + 4 * dq) =
+          make_uint4(__byte_perm(xa[m].x, xb[m].x, 0x5410), __byte_perm(xa[m].x, xb[m].x, 0x7632),
+                     __byte_perm(xa[m].y, xb[m].y, 0x5410), __byte_perm(xa[m].y, xb[m].y, 0x7632));
     }
   };
 
-  float2 acc[4][8];  // [token pair][expert]: .x token 8tg+2p, .y token 8tg+2p+1
+  float2 acc[8][8];  // [token pair][expert]: .x token 16tg+2p, .y token 16tg+2p+1
 #pragma unroll
-  for (int p = 0; p < 4; ++p)
+  for (int p = 0; p < 8; ++p)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[p][j] = make_float2(0.f, 0.f);
 
   const int nchunks = (D + kRtDC - 1) / kRtDC;
   issue_w(0, 0, min(kRtDC, D));
   load_x(0, min(kRtDC, D));
-  store_w(0);
   store_x(0);
-  if (!WDUP) cp_async_wait_all();
+  cp_async_wait_all();
   __syncthreads();
   for (int kc = 0; kc < nchunks; ++kc) {
     const int buf = kc & 1, d0 = kc * kRtDC, dc = min(kRtDC, D - d0);
@@ -149,80 +136,63 @@ __global__ void __launch_bounds__(kRtWarps * 32, 1)
       issue_w(buf ^ 1, d0 + kRtDC, dn);
       load_x(d0 + kRtDC, dn);
     }
-#pragma unroll 2
+    const float* wrow = wsb + (size_t(buf) * kRtExp + kRtWE * eg) * kRtDC + lane;
+    const uint32_t* xrow = xpb + (size_t(buf) * (kRtTok / 2) + (kRtWT / 2) * tg) * kRtDC + lane;
+#pragma unroll 1
     for (int c = 0; c < dc / 32; ++c) {
-      const int col = 32 * c + lane;
       float2 wv[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const size_t wi = (size_t(buf) * kRtExp + 8 * eg + j) * kRtDC + col;
-        if (WDUP) {
-          wv[j] = reinterpret_cast<const float2*>(wsb)[wi];
-        } else {
-          const float w = reinterpret_cast<const float*>(wsb)[wi];
-          wv[j] = make_float2(w, w);
-        }
+        const float w = wrow[j * kRtDC + 32 * c];
+        wv[j] = make_float2(w, w);
       }
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const size_t xi = (size_t(buf) * (kRtTok / 2) + 4 * tg + p) * kRtDC + col;
-        float2 xv;
-        if (XF) {
-          xv = reinterpret_cast<const float2*>(xpb)[xi];
-        } else {
-          const uint32_t w2 = reinterpret_cast<const uint32_t*>(xpb)[xi];
-          xv = make_float2(__uint_as_float(w2 << 16), __uint_as_float(w2 & 0xFFFF0000u));
-        }
+      for (int p = 0; p < 8; ++p) {
+        const uint32_t w2 = xrow[p * kRtDC + 32 * c];
+        const float2 xv = make_float2(__uint_as_float(w2 << 16), __uint_as_float(w2 & 0xFFFF0000u));
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[p][j] = __ffma2_rn(xv, wv[j], acc[p][j]);
       }
     }
     if (nxt) {
-      store_w(buf ^ 1);
       store_x(buf ^ 1);
-      if (!WDUP) cp_async_wait_all();
+      cp_async_wait_all();
     }
     __syncthreads();
   }
 
-  // The 32 partial sums of each of the 64 logits are reduced by the tree of
+  // The 32 partial sums of each of the 128 logits are reduced by the tree of
   // the canonical order (lane offsets 16, 8, 4, 2, 1) as a recursive halving:
   // at each level a lane keeps half of its values, sends the other half to
   // its partner and adds what it receives. Every addition joins the same two
   // sub-tree sums as the shuffle-down tree (fp32 addition is commutative), so
-  // the logits are bit-identical, with 62 shuffles instead of 320. Lane l
-  // ends with entry l = 8p + j of the tile: v[0] for token 8tg+2p, v[1] for
-  // token 8tg+2p+1, expert 8eg+j.
-  float v[64];
+  // the logits are bit-identical, with 124 shuffles instead of 640. Value n =
+  // 2(8p + j) + b is token 16tg+2p+b, expert 8eg+j; lane l ends with values
+  // n = 4l .. 4l+3 in v[0..3].
+  float v[128];
 #pragma unroll
-  for (int p = 0; p < 4; ++p)
+  for (int p = 0; p < 8; ++p)
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       v[2 * (8 * p + j)] = acc[p][j].x;
       v[2 * (8 * p + j) + 1] = acc[p][j].y;
     }
+  halve_level<64>(v, lane, 16);
+  halve_level<32>(v, lane, 8);
+  halve_level<16>(v, lane, 4);
+  halve_level<8>(v, lane, 2);
+  halve_level<4>(v, lane, 1);
 #pragma unroll
-  for (int lvl = 0; lvl < 5; ++lvl) {
-    const int o = 16 >> lvl, half = 32 >> lvl;  // partner offset; values kept after this level
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? v[i] : v[i + half];
-      const float keep = upper ? v[i + half] : v[i];
-      v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
-    }
-  }
-  {
-    const int p = lane >> 3, j = lane & 7;
-    const int e = eb + 8 * eg + j, t = t0 + 8 * tg + 2 * p;
+  for (int m = 0; m < 2; ++m) {
+    const int q = 2 * lane + m, p = q >> 3, j = q & 7;
+    const int e = eb + kRtWE * eg + j, t = t0 + kRtWT * tg + 2 * p;
     if (e < E) {
       const float be = bias ? bias[e] : 0.f;
-      if (t < T) logits[size_t(t) * E + e] = bias ? __fadd_rn(v[0], be) : v[0];
-      if (t + 1 < T) logits[size_t(t + 1) * E + e] = bias ? __fadd_rn(v[1], be) : v[1];
+      if (t < T) logits[size_t(t) * E + e] = bias ? __fadd_rn(v[2 * m], be) : v[2 * m];
+      if (t + 1 < T) logits[size_t(t + 1) * E + e] = bias ? __fadd_rn(v[2 * m + 1], be) : v[2 * m + 1];
     }
   }
 }
-constexpr bool kRtWdup = false, kRtXf = false;  // measured fastest: the extra shared-memory bytes cost more
 
 // Top-k and weights of each token of a chunk, and the chunk's per-expert
 // assignment counts. One warp per token.
@@ -596,8 +566,8 @@ cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
     return cudaSuccess;
   }
   {
-    auto* rk = router_tree_kernel<kRtWdup, kRtXf>;
-    const size_t smem = rt_smem<kRtWdup, kRtXf>();
+    auto* rk = router_tree_kernel;
+    const size_t smem = kRtSmem;
     if (!ensure_smem_limit(reinterpret_cast<const void*>(rk), int(smem))) return cudaErrorInvalidValue;
     const bool zero = yacc_zeroed != nullptr;
     rk<<<dim3((c.T + kRtTok - 1) / kRtTok, (c.E + kRtExp - 1) / kRtExp), kRtWarps * 32, smem, c.stream>>>(
