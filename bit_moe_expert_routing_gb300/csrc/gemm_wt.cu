@@ -57,7 +57,7 @@ constexpr uint32_t kCBytes = WM * WK / 2;               // 4 KB of codes
 constexpr uint32_t kAccCols = kMaxN;                    // fp32 columns of one accumulator
 constexpr uint32_t kAGroupCols = WK / 2;                // 32 columns: one group's 64 bf16 per lane
 constexpr uint32_t kAStageCols = kAGroupCols * kGroupsPerStage;
-constexpr uint32_t kAColBase = 2 * kAccCols;  // 384
+constexpr uint32_t kAColBase = 2 * kAccCols;  // 384: after the two accumulators
 constexpr uint32_t kTmemCols = 512;
 static_assert(kAColBase + kAStages * kAStageCols <= kTmemCols, "tensor memory budget");
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpB0 = 2, kNumBWarps = 4, kWarpDq0 = 6, kNumDqWarps = 8,
@@ -65,8 +65,8 @@ constexpr int kWarpTma = 0, kWarpMma = 1, kWarpB0 = 2, kNumBWarps = 4, kWarpDq0 
 constexpr int kNumWarps = 22;
 constexpr int kGatherPerThread = kMaxN * 8 / (kNumBWarps * 32);  // 16-byte chunks per thread per K block
 constexpr int kNumThreads = kNumWarps * 32;
-constexpr int kXposeStride = 36;
-constexpr int kEpiChunks = (kMaxN + 31) / 32;  // 16-token chunks per epilogue warp and tile  // floats per row of an epilogue transpose buffer (conflict-free float4 reads)
+constexpr int kXposeStride = 36;               // floats per row of an epilogue transpose buffer (conflict-free float4 reads)
+constexpr int kEpiChunks = (kMaxN + 31) / 32;  // 16-token chunks per epilogue warp and tile
 
 constexpr uint32_t kOffB = 0;
 constexpr uint32_t kOffC = kOffB + kBStages * kBBytes;
