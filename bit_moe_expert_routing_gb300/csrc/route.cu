@@ -10,7 +10,8 @@
 //   for c = 0 .. D/32-1:  acc[l] = fma(float(x[t, 32c+l]), W_r[e, 32c+l], acc[l])
 //   for off = 16, 8, 4, 2, 1:  acc[l] = acc[l] + acc[l+off]   (l < off)
 //   logit = acc[0] (+ bias[e])
-// Lane l of a warp owns partial sum l; the tree is a shuffle-down reduction.
+// Lane l of a warp owns partial sum l; the tree's additions are done with
+// warp shuffles.
 #include <climits>
 
 #include "common.cuh"
@@ -195,7 +196,8 @@ __global__ void __launch_bounds__(kRtWarps * 32, 1)
 }
 
 // Top-k and weights of each token of a chunk, and the chunk's per-expert
-// assignment counts. One warp per token.
+// assignment counts. A warp takes kChunkTokens / (kTopkThreads / 32) of the
+// chunk's tokens.
 constexpr int kTopkThreads = 1024;
 template <int MPL>
 __global__ void __launch_bounds__(kTopkThreads)
