@@ -346,13 +346,13 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_down_kernel(GemvArgs a) 
 // Fused decode for one token: router logits, top-k, gate/up + SwiGLU and
 // down + combine in one cooperative kernel.
 //   1. At once: each CTA bulk-copies its router rows (experts blockIdx.x +
-//      m * gridDim.x) and every weight that does not depend on the routing
-//      (the shared expert's gate/up items and down rows), and stages x.
+//      m * gridDim.x) and stages x.
 //   2. Logits of its experts in the canonical order; grid barrier.
 //   3. Every CTA takes the top-k of all logits itself (the same deterministic
-//      selection), then copies the routed experts' rows of its two gate/up
-//      items (expert slot x 16 intermediate rows) and of its 16 output
-//      columns; computes its h rows; grid barrier.
+//      selection), then copies the rows of its two gate/up items (expert
+//      slot x 16 intermediate rows) and of its 16 output columns for all
+//      k+1 slots: codes by bulk copy, scales and biases by cp.async spread
+//      over the CTA; computes its h rows; grid barrier.
 //   4. Its 16 columns of y from all k+1 slots.
 // Slot j < k is the token's j-th expert, slot k the shared expert.
 constexpr int kFdRows = 16;  // intermediate rows per gate/up item
