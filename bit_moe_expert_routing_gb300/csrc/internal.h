@@ -44,7 +44,17 @@ struct Ctx {
   float* y_acc;
   cudaStream_t stream;
   bool yacc_zeroed = false;  // set when routing already cleared y_acc
+  // x still arriving from the host on another stream: rows before
+  // x_slice_end[i] are in place once x_ready[i] has completed (the last slice
+  // ends at T). The router starts on each slice as it lands; every other
+  // kernel runs after all of them. n_x_slices = 0: x is ready on `stream`.
+  int n_x_slices = 0;
+  const int* x_slice_end = nullptr;
+  const cudaEvent_t* x_ready = nullptr;
 };
+
+// Makes `c.stream` wait until all of x has arrived (no-op without slices).
+cudaError_t wait_x(const Ctx& c);
 
 // Bookkeeping of launches: counts this library's kernels and, when kernel
 // timing is on, records an event after each one.

@@ -267,14 +267,22 @@ moe_status moe_workspace_view(const moe_weights* w, int T, void* workspace, size
 
 // One pass of the layer over T tokens (T no larger than the workspace was
 // laid out for). Adds its launches to the thread's count.
+// With n_x_slices > 0, x arrives on another stream in slices (see Ctx).
 static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* workspace,
-                               size_t workspace_bytes, void* stream) {
+                               size_t workspace_bytes, void* stream, int n_x_slices = 0,
+                               const int* x_slice_end = nullptr, const cudaEvent_t* x_ready = nullptr) {
   Ctx c;
   if (moe_status s = make_ctx(w, x, T, y, workspace, workspace_bytes, stream, &c)) return s;
   if (T == 0) return MOE_OK;
+  c.n_x_slices = n_x_slices;
+  c.x_slice_end = x_slice_end;
+  c.x_ready = x_ready;
   const Path path = plan(c);
   timing_begin(c.stream);
-  if (path == Path::DecodeFused) return cuda_status(decode_fused(c));  // routing included
+  if (path == Path::DecodeFused) {  // routing included
+    if (wait_x(c) != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(decode_fused(c));
+  }
   cudaError_t err = route(c, path == Path::Gemv ? nullptr : &c.yacc_zeroed);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (g_opt.host_sync_routing) {
@@ -314,6 +322,35 @@ moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uin
   return MOE_OK;
 }
 
+// The host entry point's copy stream and events, one set per thread and
+// device, created on first use and kept for the life of the process.
+constexpr int kHostSlices = 4;         // x goes in as up to this many slices
+constexpr int kHostSliceTokens = 512;  // ... of at least this many tokens
+struct HostPipe {
+  int device = -1;
+  cudaStream_t copy = nullptr;
+  cudaEvent_t start = nullptr;
+  cudaEvent_t ready[kHostSlices] = {};
+};
+
+static HostPipe* host_pipe() {
+  static thread_local HostPipe pipes[8];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  for (HostPipe& p : pipes) {
+    if (p.device == dev) return &p;
+    if (p.device >= 0) continue;
+    if (cudaStreamCreateWithFlags(&p.copy, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+    for (cudaEvent_t& e : p.ready)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    p.device = dev;
+    return &p;
+  }
+  return nullptr;
+}
+
 moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, int T, uint16_t* y_host,
                                   void* workspace, size_t workspace_bytes, void* stream) {
   if (check_weights(w) != MOE_OK) return check_weights(w);
@@ -328,17 +365,35 @@ moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, 
   uint16_t* xd = reinterpret_cast<uint16_t*>(base + need);
   uint16_t* yd = reinterpret_cast<uint16_t*>(base + need + stage);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int launches = 0;
+  HostPipe* hp = host_pipe();
+  if (!hp) return MOE_ERR_CUDA;
+  t_launches = 0;
   for (int t0 = 0; t0 < T; t0 += step) {
     const int n = std::min(step, T - t0);
-    const size_t at = size_t(t0) * w->D, bytes = size_t(n) * w->D * 2;
-    if (cudaMemcpyAsync(xd, x_host + at, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
-    moe_status st = moe_layer_forward(w, xd, n, yd, workspace, need, stream);
-    if (st != MOE_OK) return st;
-    launches += t_launches;
-    if (cudaMemcpyAsync(y_host + at, yd, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+    const size_t at = size_t(t0) * w->D;
+    // x goes in on the copy stream, in slices, once the stream's earlier work
+    // (which may still read the staging buffer) is done; the router starts
+    // on each slice as it lands, and the copy overlaps it
+    const int n_sl = std::max(1, std::min(kHostSlices, n / kHostSliceTokens));
+    int end[kHostSlices];
+    for (int i = 0; i < n_sl; ++i) end[i] = i + 1 == n_sl ? n : std::min(n, (n / n_sl * (i + 1) + 31) / 32 * 32);
+    if (cudaEventRecord(hp->start, s) != cudaSuccess || cudaStreamWaitEvent(hp->copy, hp->start, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    for (int i = 0, r0 = 0; i < n_sl; r0 = end[i], ++i) {
+      const size_t bytes = size_t(end[i] - r0) * w->D * 2;
+      if (bytes && cudaMemcpyAsync(xd + size_t(r0) * w->D, x_host + at + size_t(r0) * w->D, bytes,
+                                   cudaMemcpyHostToDevice, hp->copy) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      if (cudaEventRecord(hp->ready[i], hp->copy) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    moe_status st = forward_pass(w, xd, n, yd, workspace, need, stream, n_sl, end, hp->ready);
+    if (st != MOE_OK) {
+      cudaStreamSynchronize(hp->copy);  // no copy into the workspace outlives the call
+      return st;
+    }
+    if (cudaMemcpyAsync(y_host + at, yd, size_t(n) * w->D * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
   }
-  t_launches = launches;
   return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -63,9 +63,10 @@ __global__ void __launch_bounds__(kRtWarps * 32, 1)
     router_tree_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
                        int T, int D, int E, float* __restrict__ logits, WsHeader* hdr,
                        float4* __restrict__ yacc, size_t yacc_n4) {
-  // First kernel of every call: start the call's device status afresh. No
-  // other CTA of this kernel reports, so nothing races with the clear.
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+  // First kernel of every call: start the call's device status afresh (hdr
+  // is null for the later launches of a sliced router). No other CTA of this
+  // kernel reports, so nothing races with the clear.
+  if (hdr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     hdr->status = 0;
     hdr->detail = 0;
     hdr->counter = 0;
@@ -550,11 +551,20 @@ cudaError_t route_logits_small(const Ctx& c) {
   return cudaSuccess;
 }
 
+cudaError_t wait_x(const Ctx& c) {
+  for (int i = 0; i < c.n_x_slices; ++i) {
+    const cudaError_t err = cudaStreamWaitEvent(c.stream, c.x_ready[i], 0);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
   const moe_weights* w = c.w;
   cudaError_t err;
   // one CTA of 1024 threads does the small-T top-k: up to 16 logits per lane
   if (c.T <= kSmallRouteTokens && c.D <= 4096 && c.E <= 512) {
+    if ((err = wait_x(c)) != cudaSuccess) return err;
     if ((err = route_logits_small(c)) != cudaSuccess) return err;
     const int mpl = (c.E + 31) / 32;
     void (*rs)(const float*, int, int, int, int, int, int32_t*, float*, int32_t*, int32_t*, int32_t*, int32_t*,
@@ -572,13 +582,25 @@ cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
     const size_t smem = kRtSmem;
     if (!ensure_smem_limit(reinterpret_cast<const void*>(rk), int(smem))) return cudaErrorInvalidValue;
     const bool zero = yacc_zeroed != nullptr;
-    rk<<<dim3((c.T + kRtTok - 1) / kRtTok, (c.E + kRtExp - 1) / kRtExp), kRtWarps * 32, smem, c.stream>>>(
-        c.x, w->router_w, w->router_bias, c.T, c.D, c.E, c.logits, c.hdr,
-        zero ? reinterpret_cast<float4*>(c.y_acc) : nullptr, zero ? size_t(c.T) * c.D / 4 : 0);
+    // one launch per slice of x still arriving from the host (one launch for
+    // all of x otherwise); each clears the y_acc rows of its own tokens
+    const int n_sl = c.n_x_slices > 0 ? c.n_x_slices : 1;
+    for (int i = 0, t0 = 0; i < n_sl; ++i) {
+      const int t1 = c.n_x_slices > 0 ? c.x_slice_end[i] : c.T;
+      if (c.n_x_slices > 0 && (err = cudaStreamWaitEvent(c.stream, c.x_ready[i], 0)) != cudaSuccess) return err;
+      if (t1 > t0) {
+        const int n = t1 - t0;
+        rk<<<dim3((n + kRtTok - 1) / kRtTok, (c.E + kRtExp - 1) / kRtExp), kRtWarps * 32, smem, c.stream>>>(
+            c.x + size_t(t0) * c.D, w->router_w, w->router_bias, n, c.D, c.E, c.logits + size_t(t0) * c.E,
+            t0 == 0 ? c.hdr : nullptr, zero ? reinterpret_cast<float4*>(c.y_acc + size_t(t0) * c.D) : nullptr,
+            zero ? size_t(n) * c.D / 4 : 0);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        launch_done("router_logits", c.stream);
+      }
+      t0 = t1;
+    }
     if (zero) *yacc_zeroed = true;
   }
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  launch_done("router_logits", c.stream);
 
   {
     const int mpl = (c.E + 31) / 32;

@@ -439,6 +439,37 @@ def test_host_buffers_entry_point_matches_device_entry_point(path):
     check_output(y_host, O.forward(O.OracleLayer(layer), x), "host entry point")
 
 
+def test_host_entry_slices_its_input_copy():
+    # 2100 tokens go in as four slices (544, 1056, 1600 and 2100 rows) on the
+    # library's copy stream, and the router runs on each slice as it lands.
+    # Logits, top-k and weights must equal the device entry point's bit for
+    # bit; y agrees up to the fp32 combine's summation order.
+    layer, x = config("prefill4096_zipf")
+    x = x[:2100]
+    T = x.shape[0]
+    dl = dev_layer("prefill4096_zipf", layer)
+    y_dev, ws_dev = run_forward(dl, x, moe.PATH_GEMM)
+    ws = dl.workspace(T, host_staging=True)
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    r = moe.moe_layer_forward_host(dl.w, xh.data_ptr(), T, yh.data_ptr(), ws.data_ptr(), ws.numel(), None)
+    assert r == moe.MOE_OK
+    assert moe.moe_get_device_status(ctypes.c_void_p(ws.data_ptr()), None) == moe.MOE_OK
+
+    def tables(w_):
+        v = moe.moe_route_view()
+        assert moe.moe_workspace_view(dl.w, T, w_.data_ptr(), w_.numel(), v) == moe.MOE_OK
+        g = lambda p, shape, dt: moe.ws_tensor(w_, p, shape, dt).cpu().numpy()
+        return (g(v.logits, (T, layer.E), torch.float32).view(np.uint32),
+                g(v.topk_idx, (T, layer.k), torch.int32),
+                g(v.topk_w, (T, layer.k), torch.float32).view(np.uint32))
+
+    for a, b, what in zip(tables(ws), tables(ws_dev), ("logits", "top-k", "weights")):
+        assert np.array_equal(a, b), what
+    y_host = synth.bf16_bits_to_f32(yh.numpy().view(np.uint16)).astype(np.float64)
+    assert np.allclose(y_host, y_dev, rtol=2 ** -7, atol=1e-6)
+
+
 def test_gemv_path_is_deterministic():
     layer, x = config("sweep")
     dl = dev_layer("sweep", layer)
