@@ -55,6 +55,10 @@ struct Ctx {
 
 // Makes `c.stream` wait until all of x has arrived (no-op without slices).
 cudaError_t wait_x(const Ctx& c);
+// Tokens whose router tiles fill exactly one wave of CTAs on this GPU (the
+// unit in which x slices are sized, so that no router launch ends in a
+// partial wave).
+int router_wave_tokens(int E);
 
 // Bookkeeping of launches: counts this library's kernels and, when kernel
 // timing is on, records an event after each one.

@@ -324,8 +324,7 @@ moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uin
 
 // The host entry point's copy stream and events, one set per thread and
 // device, created on first use and kept for the life of the process.
-constexpr int kHostSlices = 4;         // x goes in as up to this many slices
-constexpr int kHostSliceTokens = 512;  // ... of at least this many tokens
+constexpr int kHostSlices = 16;  // x goes in as up to this many slices
 struct HostPipe {
   int device = -1;
   cudaStream_t copy = nullptr;
@@ -374,9 +373,12 @@ moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, 
     // x goes in on the copy stream, in slices, once the stream's earlier work
     // (which may still read the staging buffer) is done; the router starts
     // on each slice as it lands, and the copy overlaps it
-    const int n_sl = std::max(1, std::min(kHostSlices, n / kHostSliceTokens));
+    // slices of whole router waves, so each router launch fills the GPU
+    const int wave = router_wave_tokens(w->E);
+    const int per = wave * std::max(1, (n + kHostSlices * wave - 1) / (kHostSlices * wave));
+    const int n_sl = (n + per - 1) / per;
     int end[kHostSlices];
-    for (int i = 0; i < n_sl; ++i) end[i] = i + 1 == n_sl ? n : std::min(n, (n / n_sl * (i + 1) + 31) / 32 * 32);
+    for (int i = 0; i < n_sl; ++i) end[i] = std::min(n, per * (i + 1));
     if (cudaEventRecord(hp->start, s) != cudaSuccess || cudaStreamWaitEvent(hp->copy, hp->start, 0) != cudaSuccess)
       return MOE_ERR_CUDA;
     for (int i = 0, r0 = 0; i < n_sl; r0 = end[i], ++i) {

@@ -12,6 +12,7 @@
 //   logit = acc[0] (+ bias[e])
 // Lane l of a warp owns partial sum l; the tree's additions are done with
 // warp shuffles.
+#include <algorithm>
 #include <climits>
 
 #include "common.cuh"
@@ -549,6 +550,11 @@ cudaError_t route_logits_small(const Ctx& c) {
   if (err != cudaSuccess) return err;
   launch_done("router_small", c.stream);
   return cudaSuccess;
+}
+
+int router_wave_tokens(int E) {
+  const int expert_tiles = (E + kRtExp - 1) / kRtExp;  // one CTA per SM (254 registers per thread)
+  return kRtTok * std::max(1, num_sms() / expert_tiles);
 }
 
 cudaError_t wait_x(const Ctx& c) {

@@ -183,11 +183,12 @@ moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uin
  * `stream` before it returns. Page-locked host buffers make the copies
  * asynchronous DMA. The workspace must hold moe_workspace_size(w, T) +
  * moe_host_staging_size(w, T) (x and y staging for one pass).
- * The x rows of a pass go in as up to four slices (of at least 512 tokens)
- * on a copy stream of the library's own, ordered after the work already on
- * `stream`; the router starts on each slice as it lands, so the copy
- * overlaps the router. The result is the same as with one copy. The copy
- * stream and its five events are created on the first call of each host
+ * The x rows of a pass go in as up to 16 slices on a copy stream of the
+ * library's own, ordered after the work already on `stream`. A slice holds
+ * the tokens of one or more whole waves of router CTAs on this GPU (608 at
+ * E = 256 on 152 SMs). The router starts on each slice as it lands, so the
+ * copy overlaps the router. The result is the same as with one copy. The
+ * copy stream and its 17 events are created on the first call of each host
  * thread on each device and kept for the life of the process. */
 size_t moe_host_staging_size(const moe_weights* w, int T);
 moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, int T,

@@ -440,8 +440,9 @@ def test_host_buffers_entry_point_matches_device_entry_point(path):
 
 
 def test_host_entry_slices_its_input_copy():
-    # 2100 tokens go in as four slices (544, 1056, 1600 and 2100 rows) on the
-    # library's copy stream, and the router runs on each slice as it lands.
+    # 2100 tokens go in as slices of whole router waves (four at E = 256 on a
+    # 152-SM GPU, the last one ragged) on the library's copy stream, and the
+    # router runs on each slice as it lands.
     # Logits, top-k and weights must equal the device entry point's bit for
     # bit; y agrees up to the fp32 combine's summation order.
     layer, x = config("prefill4096_zipf")
