@@ -366,6 +366,17 @@ moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   HostPipe* hp = host_pipe();
   if (!hp) return MOE_ERR_CUDA;
+  // page-locked y that this device can address is written by the layer's
+  // last kernel directly (no staging, no copy back)
+  uint16_t* y_direct = nullptr;
+  {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, y_host) == cudaSuccess && pa.type == cudaMemoryTypeHost && pa.devicePointer &&
+        aligned16(pa.devicePointer))
+      y_direct = static_cast<uint16_t*>(pa.devicePointer);
+    else
+      cudaGetLastError();  // an unregistered pointer is not an error here
+  }
   t_launches = 0;
   for (int t0 = 0; t0 < T; t0 += step) {
     const int n = std::min(step, T - t0);
@@ -388,12 +399,13 @@ moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, 
         return MOE_ERR_CUDA;
       if (cudaEventRecord(hp->ready[i], hp->copy) != cudaSuccess) return MOE_ERR_CUDA;
     }
-    moe_status st = forward_pass(w, xd, n, yd, workspace, need, stream, n_sl, end, hp->ready);
+    moe_status st = forward_pass(w, xd, n, y_direct ? y_direct + at : yd, workspace, need, stream, n_sl, end, hp->ready);
     if (st != MOE_OK) {
       cudaStreamSynchronize(hp->copy);  // no copy into the workspace outlives the call
       return st;
     }
-    if (cudaMemcpyAsync(y_host + at, yd, size_t(n) * w->D * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    if (!y_direct &&
+        cudaMemcpyAsync(y_host + at, yd, size_t(n) * w->D * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
   return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

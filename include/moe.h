@@ -189,7 +189,10 @@ moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uin
  * E = 256 on 152 SMs). The router starts on each slice as it lands, so the
  * copy overlaps the router. The result is the same as with one copy. The
  * copy stream and its 17 events are created on the first call of each host
- * thread on each device and kept for the life of the process. */
+ * thread on each device and kept for the life of the process. When y_host is
+ * page-locked memory this device can address (16-byte aligned), the layer's
+ * last kernel writes y into it directly, with no staging and no copy back;
+ * other host memory is staged and copied. */
 size_t moe_host_staging_size(const moe_weights* w, int T);
 moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, int T,
                                   uint16_t* y_host, void* workspace, size_t workspace_bytes,

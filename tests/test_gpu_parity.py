@@ -439,10 +439,12 @@ def test_host_buffers_entry_point_matches_device_entry_point(path):
     check_output(y_host, O.forward(O.OracleLayer(layer), x), "host entry point")
 
 
-def test_host_entry_slices_its_input_copy():
+@pytest.mark.parametrize("y_pinned", [True, False], ids=["y-written-directly", "y-staged"])
+def test_host_entry_slices_its_input_copy(y_pinned):
     # 2100 tokens go in as slices of whole router waves (four at E = 256 on a
     # 152-SM GPU, the last one ragged) on the library's copy stream, and the
-    # router runs on each slice as it lands.
+    # router runs on each slice as it lands. Page-locked y is written by the
+    # layer's last kernel directly; pageable y is staged and copied back.
     # Logits, top-k and weights must equal the device entry point's bit for
     # bit; y agrees up to the fp32 combine's summation order.
     layer, x = config("prefill4096_zipf")
@@ -452,7 +454,9 @@ def test_host_entry_slices_its_input_copy():
     y_dev, ws_dev = run_forward(dl, x, moe.PATH_GEMM)
     ws = dl.workspace(T, host_staging=True)
     xh = torch.from_numpy(x.view(np.int16)).pin_memory()
-    yh = torch.empty_like(xh).pin_memory()
+    yh = torch.empty_like(xh)
+    if y_pinned:
+        yh = yh.pin_memory()
     r = moe.moe_layer_forward_host(dl.w, xh.data_ptr(), T, yh.data_ptr(), ws.data_ptr(), ws.numel(), None)
     assert r == moe.MOE_OK
     assert moe.moe_get_device_status(ctypes.c_void_p(ws.data_ptr()), None) == moe.MOE_OK
