@@ -475,6 +475,35 @@ def test_host_entry_slices_its_input_copy(y_pinned):
     assert np.allclose(y_host, y_dev, rtol=2 ** -7, atol=1e-6)
 
 
+def test_host_entry_chunked_passes_and_unaligned_y():
+    # 1300 tokens in passes of 608 (608, 608, 84): each pass copies its x on
+    # the library's copy stream once the previous pass is done with the
+    # staging buffer, and reuses the slice events. y starts 2 bytes into a
+    # page-locked buffer, so it is not 16-byte aligned: the layer writes it to
+    # the staging buffer and copies it back. The output must match the device
+    # entry point run with the same passes.
+    layer, x = config("prefill4096_zipf")
+    x = x[:1300]
+    T = x.shape[0]
+    dl = dev_layer("prefill4096_zipf", layer)
+    old = moe.moe_get_option(moe.MOE_OPT_CHUNK_TOKENS)
+    try:
+        assert moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, 608) == moe.MOE_OK
+        y_dev, _ = run_forward(dl, x, moe.PATH_GEMM)
+        ws = dl.workspace(T, host_staging=True)
+        xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+        buf = torch.empty(T * layer.D + 8, dtype=torch.int16).pin_memory()
+        yh = buf[1:1 + T * layer.D]
+        assert yh.data_ptr() % 16 == 2
+        r = moe.moe_layer_forward_host(dl.w, xh.data_ptr(), T, yh.data_ptr(), ws.data_ptr(), ws.numel(), None)
+        assert r == moe.MOE_OK
+        assert moe.moe_get_device_status(ctypes.c_void_p(ws.data_ptr()), None) == moe.MOE_OK
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, old)
+    y_host = synth.bf16_bits_to_f32(yh.numpy().view(np.uint16).reshape(T, layer.D)).astype(np.float64)
+    assert np.allclose(y_host, y_dev, rtol=2 ** -7, atol=1e-6)
+
+
 def test_gemv_path_is_deterministic():
     layer, x = config("sweep")
     dl = dev_layer("sweep", layer)
