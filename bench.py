@@ -16,6 +16,7 @@ the value counts every rank's tokens. --impl reference times the CPU oracle
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import math
 import os
@@ -122,32 +123,46 @@ def sum_over_ranks(dist, value: float, device=None) -> float:
 # --- clocks ----------------------------------------------------------------------------------
 
 class ClockSampler:
-    """Samples nvidia-smi SM clocks and throttle reasons while running."""
+    """Samples nvidia-smi SM clocks and throttle reasons every 20 ms while running.
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    The sampler is running before the caller starts timing (its first line has
+    arrived), and summary() keeps only the samples stamped inside the window
+    the caller marks with window_start() / window_end() (wall clock)."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines: list[str] = []
+        self.lines: list[tuple[float, str]] = []
         self._t = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
+            deadline = time.time() + 5.0
+            while not self.lines and time.time() < deadline and self.proc.poll() is None:
+                time.sleep(0.01)
         except OSError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def window_start(self):
+        self.t0 = time.time()
+
+    def window_end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -159,28 +174,42 @@ class ClockSampler:
             if self._t is not None:
                 self._t.join(timeout=2)
 
+    @staticmethod
+    def _stamp(text: str):
+        """Wall-clock seconds of an nvidia-smi timestamp such as 2026/12/02 13:45:01.123."""
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self) -> dict:
         rows = []
-        for ln in self.lines:
+        for t_read, ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
+            t = self._stamp(parts[0])
             try:
-                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), active=parts[4],
-                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+                rows.append(dict(t=t if t is not None else t_read, sm=float(parts[2]), smax=float(parts[3]),
+                                 active=parts[5], hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
             except ValueError:
                 continue
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        if self.t0 is not None and self.t1 is not None:
+            inside = [r for r in rows if self.t0 <= r["t"] <= self.t1]
+        else:
+            inside = rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": rows[0]["smax"] if rows else None, "reasons": ["unsampled"],
+                    "samples": 0}
         reasons = set()
-        for r in rows:
+        for r in inside:
             for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
                               ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
                 if r[key].lower() == "active":
                     reasons.add(name)
-        sms = sorted(r["sm"] for r in rows)
-        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": rows[0]["smax"], "reasons": sorted(reasons),
-                "samples": len(rows)}
+        sms = sorted(r["sm"] for r in inside)
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": inside[0]["smax"], "reasons": sorted(reasons),
+                "samples": len(inside), "sm_mhz_min": sms[0]}
 
 
 # --- algorithmic work ------------------------------------------------------------------------
@@ -259,6 +288,7 @@ def run_ours(args) -> dict:
     barrier(dist, device)
     torch.cuda.synchronize(device)
     with ClockSampler(device.index) as clk:
+        clk.window_start()
         t_wall = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()
@@ -269,6 +299,7 @@ def run_ours(args) -> dict:
             launches += moe.moe_last_launch_count()
         torch.cuda.synchronize(device)
         t_wall = time.perf_counter() - t_wall
+        clk.window_end()
     barrier(dist, device)
     moe.moe_set_option(moe.MOE_OPT_KERNEL_TIMING, 0)
     kt = moe.moe_kernel_times()
@@ -633,7 +664,7 @@ def run_ablations(args) -> dict:
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
