@@ -69,4 +69,31 @@ __device__ __forceinline__ void dq8_bf16(uint32_t w, __nv_bfloat162 s2, __nv_bfl
   out[3] = __byte_perm(v[2], v[3], 0x7632);  // (w6, w7)
 }
 
+// The same eight weights in the paired order (below): out[i] holds
+// elements i (low half) and i + 4 (high half), with no reordering step. A
+// matrix product over K is unchanged when both operands take this order
+// inside every group of eight (the activations are permuted once to match).
+__device__ __forceinline__ void dq8_bf16_paired(uint32_t w, __nv_bfloat162 s2, __nv_bfloat162 b2, uint32_t out[4]) {
+  const __nv_bfloat162 k128 = __halves2bfloat162(__ushort_as_bfloat16(0x4300), __ushort_as_bfloat16(0x4300));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t p = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;  // (128+q_i, 128+q_{i+4})
+    __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&p), k128);
+    __nv_bfloat162 r = __hfma2(q, s2, b2);
+    out[i] = *reinterpret_cast<uint32_t*>(&r);
+  }
+}
+
+// Paired order of eight consecutive K elements (positions 0..7 hold elements
+// 0, 4, 1, 5, 2, 6, 3, 7): the order dq8_bf16_paired emits weights in.
+// pair_order8_first/second(lo, hi) take elements 0..3 (lo) and 4..7 (hi), two bf16 per
+// word, and returns positions 0..3 (first) or 4..7 (second) of the permuted
+// chunk.
+__device__ __forceinline__ uint2 pair_order8_first(uint2 lo, uint2 hi) {
+  return make_uint2(__byte_perm(lo.x, hi.x, 0x5410), __byte_perm(lo.x, hi.x, 0x7632));  // (0,4), (1,5)
+}
+__device__ __forceinline__ uint2 pair_order8_second(uint2 lo, uint2 hi) {
+  return make_uint2(__byte_perm(lo.y, hi.y, 0x5410), __byte_perm(lo.y, hi.y, 0x7632));  // (2,6), (3,7)
+}
+
 }  // namespace moe

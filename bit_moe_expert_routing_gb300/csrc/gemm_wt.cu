@@ -514,15 +514,28 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
           const uint4 w1 = *reinterpret_cast<const uint4*>(crow + 16);
           const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16(sc), __ushort_as_bfloat16(sc));
           const __nv_bfloat162 b2 = __halves2bfloat162(__ushort_as_bfloat16(bi), __ushort_as_bfloat16(bi));
+          // gate/up: K in the paired order inside every group of eight (x was
+          // permuted to match by the router); down: natural order (h)
           uint32_t o[32];
-          dq8_bf16(w0.x, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 0));
-          dq8_bf16(w0.y, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 4));
-          dq8_bf16(w0.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 8));
-          dq8_bf16(w0.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 12));
-          dq8_bf16(w1.x, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 16));
-          dq8_bf16(w1.y, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 20));
-          dq8_bf16(w1.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 24));
-          dq8_bf16(w1.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 28));
+          if (GATEUP) {
+            dq8_bf16_paired(w0.x, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 0));
+            dq8_bf16_paired(w0.y, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 4));
+            dq8_bf16_paired(w0.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 8));
+            dq8_bf16_paired(w0.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 12));
+            dq8_bf16_paired(w1.x, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 16));
+            dq8_bf16_paired(w1.y, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 20));
+            dq8_bf16_paired(w1.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 24));
+            dq8_bf16_paired(w1.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 28));
+          } else {
+            dq8_bf16(w0.x, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 0));
+            dq8_bf16(w0.y, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 4));
+            dq8_bf16(w0.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 8));
+            dq8_bf16(w0.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 12));
+            dq8_bf16(w1.x, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 16));
+            dq8_bf16(w1.y, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 20));
+            dq8_bf16(w1.z, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 24));
+            dq8_bf16(w1.w, s2, b2, *reinterpret_cast<uint32_t(*)[4]>(o + 28));
+          }
           // the code stage goes back to the TMA only after every lane's reads
           // of it have returned: one instruction consumes all the words read
           // (a warp issues in order, so it waits for every lane's loads), and
@@ -676,11 +689,12 @@ bool gemm_wt_supported(const Ctx& c) {
 cudaError_t gemm_wt(const Ctx& c) {
   const moe_weights* w = c.w;
   if (c.BM < 1 || c.BM > kWtBlockRows) return cudaErrorInvalidValue;  // a tile takes one block of <= 192 rows
+  if (!c.xperm) return cudaErrorInvalidValue;  // gate/up gathers the paired-order x the router wrote
   if (!ensure_smem_limit(reinterpret_cast<const void*>(gemm_wt_kernel<true>), int(kSmemBytes)) ||
       !ensure_smem_limit(reinterpret_cast<const void*>(gemm_wt_kernel<false>), int(kSmemBytes)))
     return cudaErrorInvalidValue;
   const int A = c.T * c.k;
-  WtArgs a{c.x,      w->gate, w->up,   w->s_gate, w->s_up, c.blocks, c.n_blocks, c.perm, c.topk_w,
+  WtArgs a{c.xperm,  w->gate, w->up,   w->s_gate, w->s_up, c.blocks, c.n_blocks, c.perm, c.topk_w,
            c.h,      c.y_acc, c.hdr,   c.T,       c.D,     c.E,      c.k,        c.I,    c.max_blocks,
            tc_epilogue_wait_limit()};
   WtMaps maps;

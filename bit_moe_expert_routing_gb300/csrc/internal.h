@@ -42,6 +42,11 @@ struct Ctx {
   int32_t* n_blocks;
   uint16_t* h;
   float* y_acc;
+  // x with every 8-element chunk in the paired order (dq8_bf16_paired), written
+  // by the router for the gate/up GEMM of the tensor-memory path; null when no
+  // kernel of the call reads it
+  uint16_t* xperm = nullptr;
+  uint16_t* xperm_area = nullptr;  // its place in the workspace
   cudaStream_t stream;
   bool yacc_zeroed = false;  // set when routing already cleared y_acc
   // x still arriving from the host on another stream: rows before

@@ -64,7 +64,7 @@ size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct Layout {
   int BM, max_blocks, n_chunks;
-  size_t logits, topk_idx, topk_w, count, off, perm, inv, chunk, blocks, n_blocks, h, y_acc, total;
+  size_t logits, topk_idx, topk_w, count, off, perm, inv, chunk, blocks, n_blocks, h, y_acc, xperm, total;
 };
 
 Layout layout(const moe_weights* w, int T) {
@@ -92,6 +92,7 @@ Layout layout(const moe_weights* w, int T) {
   L.n_blocks = put(4);
   L.h = put((A + T) * size_t(w->I) * 2);
   L.y_acc = put(size_t(T) * w->D * 4);
+  L.xperm = put(size_t(T) * w->D * 2);
   L.total = o;
   return L;
 }
@@ -152,7 +153,9 @@ moe_status make_ctx(const moe_weights* w, const uint16_t* x, int T, uint16_t* y,
   c->n_blocks = reinterpret_cast<int32_t*>(base + L.n_blocks);
   c->h = reinterpret_cast<uint16_t*>(base + L.h);
   c->y_acc = reinterpret_cast<float*>(base + L.y_acc);
+  c->xperm = nullptr;  // set by the path that reads it
   c->stream = static_cast<cudaStream_t>(stream);
+  c->xperm_area = reinterpret_cast<uint16_t*>(base + L.xperm);
   return MOE_OK;
 }
 
@@ -278,6 +281,7 @@ static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, u
   c.x_slice_end = x_slice_end;
   c.x_ready = x_ready;
   const Path path = plan(c);
+  if (path == Path::GemmWt) c.xperm = c.xperm_area;  // the router writes the paired-order x it gathers
   timing_begin(c.stream);
   if (path == Path::DecodeFused) {  // routing included
     if (wait_x(c) != cudaSuccess) return MOE_ERR_CUDA;
