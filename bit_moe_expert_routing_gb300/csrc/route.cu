@@ -63,7 +63,7 @@ __device__ __forceinline__ void halve_level(float (&v)[128], int lane, int o) {
 __global__ void __launch_bounds__(kRtWarps * 32, 1)
     router_tree_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
                        int T, int D, int E, float* __restrict__ logits, WsHeader* hdr,
-                       float4* __restrict__ yacc, size_t yacc_n4, uint16_t* __restrict__ xperm) {
+                       float4* __restrict__ yacc, size_t yacc_n4) {
   // First kernel of every call: start the call's device status afresh (hdr
   // is null for the later launches of a sliced router). No other CTA of this
   // kernel reports, so nothing races with the clear.
@@ -118,25 +118,6 @@ __global__ void __launch_bounds__(kRtWarps * 32, 1)
                      __byte_perm(xa[m].y, xb[m].y, 0x5410), __byte_perm(xa[m].y, xb[m].y, 0x7632));
     }
   };
-  // the paired-order copy of x (CTAs of the first expert tile): lanes 2j and
-  // 2j+1 hold the two halves of one 8-element chunk of a token and swap them
-  auto store_xperm = [&](int d0, int dc) {
-#pragma unroll
-    for (int m = 0; m < kRtXItems; ++m) {
-      const int i = threadIdx.x + m * blockDim.x, ip = i / (kRtDC / 4), dq = i % (kRtDC / 4);
-      const int ta = t0 + 2 * ip, tb = ta + 1;
-      const uint2 oa = make_uint2(__shfl_xor_sync(0xffffffffu, xa[m].x, 1), __shfl_xor_sync(0xffffffffu, xa[m].y, 1));
-      const uint2 ob = make_uint2(__shfl_xor_sync(0xffffffffu, xb[m].x, 1), __shfl_xor_sync(0xffffffffu, xb[m].y, 1));
-      const bool first = (dq & 1) == 0;
-      const uint2 pa = first ? pair_order8_first(xa[m], oa) : pair_order8_second(oa, xa[m]);
-      const uint2 pb = first ? pair_order8_first(xb[m], ob) : pair_order8_second(ob, xb[m]);
-      if (4 * dq < dc) {
-        if (ta < T) *reinterpret_cast<uint2*>(xperm + size_t(ta) * D + d0 + 4 * dq) = pa;
-        if (tb < T) *reinterpret_cast<uint2*>(xperm + size_t(tb) * D + d0 + 4 * dq) = pb;
-      }
-    }
-  };
-  const bool write_xperm = xperm != nullptr && blockIdx.y == 0;
 
   float2 acc[8][8];  // [token pair][expert]: .x token 16tg+2p, .y token 16tg+2p+1
 #pragma unroll
@@ -148,7 +129,6 @@ __global__ void __launch_bounds__(kRtWarps * 32, 1)
   issue_w(0, 0, min(kRtDC, D));
   load_x(0, min(kRtDC, D));
   store_x(0);
-  if (write_xperm) store_xperm(0, min(kRtDC, D));
   cp_async_wait_all();
   __syncthreads();
   for (int kc = 0; kc < nchunks; ++kc) {
@@ -179,7 +159,6 @@ __global__ void __launch_bounds__(kRtWarps * 32, 1)
     }
     if (nxt) {
       store_x(buf ^ 1);
-      if (write_xperm) store_xperm(d0 + kRtDC, min(kRtDC, D - d0 - kRtDC));
       cp_async_wait_all();
     }
     __syncthreads();
@@ -226,7 +205,21 @@ template <int MPL>
 __global__ void __launch_bounds__(kTopkThreads)
     topk_hist_kernel(const float* __restrict__ logits, int T, int E, int k,
                      int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                     int32_t* __restrict__ chunk_count) {
+                     int32_t* __restrict__ chunk_count, int n_chunks, const uint16_t* __restrict__ x, int D,
+                     uint16_t* __restrict__ xperm) {
+  if (int(blockIdx.x) >= n_chunks) {
+    // CTAs past the chunks write the paired-order copy of x for the
+    // tensor-memory gate/up GEMM (see permute_x_kernel), on SMs the top-k
+    // leaves idle
+    const size_t n8 = size_t(T) * D / 8, step = size_t(gridDim.x - n_chunks) * blockDim.x;
+    for (size_t i = size_t(blockIdx.x - n_chunks) * blockDim.x + threadIdx.x; i < n8; i += step) {
+      const uint4 v = reinterpret_cast<const uint4*>(x)[i];
+      const uint2 lo = make_uint2(v.x, v.y), hi = make_uint2(v.z, v.w);
+      const uint2 a = pair_order8_first(lo, hi), b = pair_order8_second(lo, hi);
+      reinterpret_cast<uint4*>(xperm)[i] = make_uint4(a.x, a.y, b.x, b.y);
+    }
+    return;
+  }
   extern __shared__ int hist[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -639,7 +632,7 @@ cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
         rk<<<dim3((n + kRtTok - 1) / kRtTok, (c.E + kRtExp - 1) / kRtExp), kRtWarps * 32, smem, c.stream>>>(
             c.x + size_t(t0) * c.D, w->router_w, w->router_bias, n, c.D, c.E, c.logits + size_t(t0) * c.E,
             t0 == 0 ? c.hdr : nullptr, zero ? reinterpret_cast<float4*>(c.y_acc + size_t(t0) * c.D) : nullptr,
-            zero ? size_t(n) * c.D / 4 : 0, c.xperm ? c.xperm + size_t(t0) * c.D : nullptr);
+            zero ? size_t(n) * c.D / 4 : 0);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
         launch_done("router_logits", c.stream);
       }
@@ -650,11 +643,14 @@ cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
 
   {
     const int mpl = (c.E + 31) / 32;
-    void (*tk)(const float*, int, int, int, int32_t*, float*, int32_t*) =
+    void (*tk)(const float*, int, int, int, int32_t*, float*, int32_t*, int, const uint16_t*, int, uint16_t*) =
         mpl <= 4 ? topk_hist_kernel<4> : mpl <= 8 ? topk_hist_kernel<8> : mpl <= 16 ? topk_hist_kernel<16>
                                                                                   : topk_hist_kernel<32>;
-    tk<<<c.n_chunks, kTopkThreads, c.E * sizeof(int), c.stream>>>(c.logits, c.T, c.E, c.k, c.topk_idx, c.topk_w,
-                                                                  c.chunk);
+    // with the paired-order copy of x to write, the SMs the chunks leave idle
+    // (at least 16 CTAs) take it
+    const int n_copy = c.xperm ? std::max(16, num_sms() - c.n_chunks) : 0;
+    tk<<<c.n_chunks + n_copy, kTopkThreads, c.E * sizeof(int), c.stream>>>(
+        c.logits, c.T, c.E, c.k, c.topk_idx, c.topk_w, c.chunk, c.n_chunks, c.x, c.D, c.xperm);
   }
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done("topk_hist", c.stream);
