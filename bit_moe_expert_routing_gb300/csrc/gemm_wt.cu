@@ -194,12 +194,6 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return uint32_t((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// bf16 number gi (0..7) of a 16-byte vector, without indexing registers.
-__device__ __forceinline__ uint16_t pick_bf16(uint4 v, int gi) {
-  const uint32_t w = (gi & 4) ? ((gi & 2) ? v.w : v.z) : ((gi & 2) ? v.y : v.x);
-  return uint16_t((gi & 1) ? (w >> 16) : (w & 0xFFFFu));
-}
-
 struct WtArgs {
   const uint16_t* x;
   moe_qmatrix m0, m1;  // routed: gate, up (gate/up kernel) or down in m0
@@ -455,7 +449,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
     const int par = (warp - kWarpDq0) >> 2;          // stage parity this warp fills
     const int L = q * 32 + lane;                     // TMEM lane = weight row of the tile
     const int srow_stage = GATEUP ? ((L & 1) ? 64 + (L >> 1) : (L >> 1)) : L;  // row in the code stage
-    const bool vec_sb = (K / 64) % 8 == 0;
     uint32_t g0 = 0, t0 = 0;  // groups and stages of the tiles before this one
     bool ok = true;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, g0 += KS, t0 += KT) {
@@ -470,44 +463,22 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
       const size_t row = GATEUP ? size_t(ex) * a.I + j * 64 + (L >> 1) : size_t(ex) * a.D + j * WM + L;
       const uint16_t* srow = m.scales + row * (K / 64);
       const uint16_t* brow = m.biases + row * (K / 64);
-      // scales and biases of 8 groups at a time (one 16-byte load each), one window ahead
-      uint4 s_cur = make_uint4(0u, 0u, 0u, 0u), b_cur = s_cur, s_nxt = s_cur, b_nxt = s_cur;
-      if (vec_sb) {
-        s_cur = *reinterpret_cast<const uint4*>(srow);
-        b_cur = *reinterpret_cast<const uint4*>(brow);
-        if (KS > 8) {
-          s_nxt = *reinterpret_cast<const uint4*>(srow + 8);
-          b_nxt = *reinterpret_cast<const uint4*>(brow + 8);
-        }
-      }
-      int win = 0;
       for (int t = par; t < KT && ok; t += 2) {
         const uint32_t is = t0 + t;
         const int s = is % kAStages;
         const uint32_t ph = (is / kAStages) & 1u;
+        // the stage's two scales and two biases, one 32-bit load each (K / 64
+        // is even and the arrays 16-byte aligned)
+        const uint32_t sc2 = *reinterpret_cast<const uint32_t*>(srow + t * kGroupsPerStage);
+        const uint32_t bi2 = *reinterpret_cast<const uint32_t*>(brow + t * kGroupsPerStage);
 #pragma unroll 1
         for (int hb = 0; hb < kGroupsPerStage; ++hb) {
           const int ks = t * kGroupsPerStage + hb;
           const uint32_t ig = g0 + ks;
           const int cs = ig % kCStages;
           const uint32_t cph = (ig / kCStages) & 1u;
-          uint16_t sc, bi;
-          if (vec_sb) {
-            if ((ks >> 3) != win) {  // next window of 8 groups
-              win = ks >> 3;
-              s_cur = s_nxt;
-              b_cur = b_nxt;
-              if (8 * (win + 1) < KS) {
-                s_nxt = *reinterpret_cast<const uint4*>(srow + 8 * (win + 1));
-                b_nxt = *reinterpret_cast<const uint4*>(brow + 8 * (win + 1));
-              }
-            }
-            sc = pick_bf16(s_cur, ks & 7);
-            bi = pick_bf16(b_cur, ks & 7);
-          } else {
-            sc = srow[ks];
-            bi = brow[ks];
-          }
+          const uint16_t sc = uint16_t(hb ? (sc2 >> 16) : (sc2 & 0xFFFFu));
+          const uint16_t bi = uint16_t(hb ? (bi2 >> 16) : (bi2 & 0xFFFFu));
           if (!(ok = mbar_wait(cfull(cs), cph, abort_flag, a.hdr))) break;
           const uint8_t* crow = gbase + kOffC + cs * kCBytes + srow_stage * 32;
           const uint4 w0 = *reinterpret_cast<const uint4*>(crow);
