@@ -396,18 +396,25 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
           }
           src[m] = reinterpret_cast<const char*>(a.x + size_t(t) * a.D) + ch * 16;
         }
+        // this thread copies chunk column bt & 7 of rows r0 + 16 m: in the
+        // swizzled tile those land at sw0 + 2048 m (row & 7 is the same for all m)
+        const int r0 = bt >> 3;
+        const uint32_t sw0 = sw128(r0, bt & 7);
+        uint32_t live = 0;  // bit m: row r0 + 16 m is read by the MMA
+#pragma unroll
+        for (int m = 0; m < kGatherPerThread; ++m)
+          if (r0 + 16 * m < n) live |= 1u << m;
         for (int t = 0; t < KT; ++t, ++it) {
           const int s = it % kBStages;
           const uint32_t ph = (it / kBStages) & 1u;
           if (!(ok = mbar_wait(bempty(s), ph ^ 1u, abort_flag, a.hdr))) break;
-          const uint32_t dst = base + kOffB + s * kBBytes;
+          const uint32_t dst = base + kOffB + s * kBBytes + sw0;
+          const int koff = t * kGroupsPerStage * 128;
 #pragma unroll
           for (int hb = 0; hb < kGroupsPerStage; ++hb)
 #pragma unroll
-            for (int m = 0; m < kGatherPerThread; ++m) {
-              const int lin = bt + 128 * m, row = lin >> 3, ch = lin & 7;
-              if (row < n) cp_async16(dst + hb * kBHalf + sw128(row, ch), src[m] + (t * kGroupsPerStage + hb) * 128, 16u);
-            }
+            for (int m = 0; m < kGatherPerThread; ++m)
+              if (live & (1u << m)) cp_async16(dst + hb * kBHalf + 2048u * m, src[m] + koff + hb * 128, 16u);
           cp_async_arrive_noinc(bfull(s));
         }
       }
