@@ -29,6 +29,8 @@
 //      decision, an integer, is taken identically by both implementations.
 //   R4 top-k is taken on the logits: larger logit first, lower expert index
 //      on ties. Weights: softmax over all E, renormalised over the k kept.
+//      The pages are silent on non-finite logits: a NaN logit is ranked and
+//      weighted as -inf, and -0 equals +0 (so the lower index wins).
 //   R5 the shared expert has weight 1 and no gate.
 //   R6 SwiGLU: h = silu(g) * u with silu(z) = z / (1 + exp(-z)).
 //   R7 within an expert's segment rows are in ascending assignment index
@@ -106,30 +108,39 @@ float router_logit(const oracle_layer& L, const uint16_t* xt, int e) {
   return logit;
 }
 
-// Routing for one token: logits, top-k by (logit desc, index asc), and the
-// renormalised softmax weights (reading R4).
-void route_token(const oracle_layer& L, const uint16_t* xt, float* logits, int* idx, double* w) {
-  std::vector<int> order(L.E);
-  for (int e = 0; e < L.E; ++e) {
-    logits[e] = router_logit(L, xt, e);
-    order[e] = e;
-  }
+// Value a logit is ranked and weighted by (reading R4): a NaN logit counts
+// as -inf, so every logit has a place in one total order; -0 and +0 are the
+// same value there (they compare equal), so the lower index goes first.
+double rank_value(float v) { return std::isnan(v) ? -INFINITY : double(v); }
+
+// Top-k of one token's E logits by (rank value desc, index asc), and the
+// renormalised softmax weights (reading R4): softmax over all E, then each
+// kept expert's probability divided by the sum over the k kept.
+void topk_of_logits(const float* logits, int E, int k, int* idx, double* w) {
+  std::vector<int> order(E);
+  for (int e = 0; e < E; ++e) order[e] = e;
   std::stable_sort(order.begin(), order.end(),
-                   [&](int a, int b) { return logits[a] > logits[b]; });
-  double lmax = logits[order[0]];
-  std::vector<double> p(L.E);
+                   [&](int a, int b) { return rank_value(logits[a]) > rank_value(logits[b]); });
+  const double lmax = rank_value(logits[order[0]]);
+  std::vector<double> p(E);
   double z = 0.0;
-  for (int e = 0; e < L.E; ++e) {
-    p[e] = std::exp(double(logits[e]) - lmax);
+  for (int e = 0; e < E; ++e) {
+    p[e] = std::exp(rank_value(logits[e]) - lmax);
     z += p[e];
   }
-  for (int e = 0; e < L.E; ++e) p[e] /= z;  // softmax over all experts
+  for (int e = 0; e < E; ++e) p[e] /= z;  // softmax over all experts
   double kept = 0.0;
-  for (int j = 0; j < L.k; ++j) {
+  for (int j = 0; j < k; ++j) {
     idx[j] = order[j];
     kept += p[order[j]];
   }
-  for (int j = 0; j < L.k; ++j) w[j] = p[idx[j]] / kept;  // renormalise over the k
+  for (int j = 0; j < k; ++j) w[j] = p[idx[j]] / kept;  // renormalise over the k
+}
+
+// Routing for one token: its logits, then their top-k and weights.
+void route_token(const oracle_layer& L, const uint16_t* xt, float* logits, int* idx, double* w) {
+  for (int e = 0; e < L.E; ++e) logits[e] = router_logit(L, xt, e);
+  topk_of_logits(logits, L.E, L.k, idx, w);
 }
 
 // One SwiGLU expert on one token row, fp64 throughout (reading R6).
@@ -188,6 +199,14 @@ int oracle_dequant(const oracle_qmat* m, int expert, int rows, int K, double* ou
   if (!m || K % 64 != 0 || rows <= 0) return 1;
   for (int n = 0; n < rows; ++n)
     for (int kk = 0; kk < K; ++kk) out[size_t(n) * K + kk] = dq(*m, rows, K, expert, n, kk);
+  return 0;
+}
+
+// Top-k and renormalised weights of one token's given logits [E] (reading
+// R4; the router's own logits go through the same function).
+int oracle_topk(const float* logits, int E, int k, int* topk_idx, double* topk_w) {
+  if (!logits || E < 1 || k < 1 || k > E) return 1;
+  topk_of_logits(logits, E, k, topk_idx, topk_w);
   return 0;
 }
 

@@ -51,6 +51,7 @@ def lib():
         vp, ci = ctypes.c_void_p, ctypes.c_int
         _lib.oracle_dequant.argtypes = [ctypes.POINTER(_QMat), ci, ci, ci, vp]
         _lib.oracle_route.argtypes = [ctypes.POINTER(_Layer), vp, ci, vp, vp, vp, ci]
+        _lib.oracle_topk.argtypes = [vp, ci, ci, vp, vp]
         _lib.oracle_route_tables.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, vp, vp, ci]
         _lib.oracle_expert_h.argtypes = [ctypes.POINTER(_Layer), ci, vp, vp]
         _lib.oracle_moe_forward.argtypes = [ctypes.POINTER(_Layer), vp, ci, vp, ci, vp, ci]
@@ -106,6 +107,15 @@ def route(ol: OracleLayer, x: np.ndarray, n_threads: int = 0):
     w = np.empty((T, ol.k), dtype=np.float64)
     assert lib().oracle_route(ctypes.byref(ol.s), _p(x), T, _p(logits), _p(idx), _p(w), n_threads) == 0
     return logits, idx, w
+
+
+def topk(logits: np.ndarray, k: int):
+    """Top-k of one token's given fp32 logits [E]: (indices int32 [k], weights fp64 [k])."""
+    lg = _c(logits, np.float32)
+    idx = np.empty(k, np.int32)
+    w = np.empty(k, np.float64)
+    assert lib().oracle_topk(_p(lg), lg.shape[0], k, _p(idx), _p(w)) == 0
+    return idx, w
 
 
 def route_tables(topk_idx: np.ndarray, E: int, BM: int):

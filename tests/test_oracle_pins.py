@@ -161,6 +161,27 @@ def test_topk_order_ties_and_weights():
             assert j3 < j9
 
 
+def test_topk_non_finite_and_signed_zero_logits_hand_worked():
+    # The pages give no rule for non-finite logits. The reading: a NaN logit
+    # ranks (and weighs) as -inf, -0 equals +0, and equal values go to the
+    # lower index. Worked by hand for logits [NaN, 1, -0, +0, -inf, 2]:
+    #   order 5 (2), 1 (1), 2 (-0) before 3 (+0), then 0 (NaN = -inf) before
+    #   4 (-inf); weights exp(l - 2) over the kept: 1, e^-1, e^-2, e^-2, 0, 0.
+    lg = np.array([np.nan, 1.0, -0.0, 0.0, -np.inf, 2.0], np.float32)
+    assert np.signbit(lg[2]) and not np.signbit(lg[3])
+    e1, e2 = np.exp(-1.0), np.exp(-2.0)
+    for k, order, num in ((6, [5, 1, 2, 3, 0, 4], [1.0, e1, e2, e2, 0.0, 0.0]),
+                          (4, [5, 1, 2, 3], [1.0, e1, e2, e2]),
+                          (1, [5], [1.0])):
+        idx, w = O.topk(lg, k)
+        assert list(idx) == order, k
+        want = np.array(num) / sum(num)
+        assert np.allclose(w, want, rtol=0, atol=1e-15), (k, w, want)
+    # +0 listed before -0 keeps index order as well: the sign is no tie-break
+    idx, _ = O.topk(np.array([0.0, -0.0, -1.0], np.float32), 2)
+    assert list(idx) == [0, 1]
+
+
 def _check_tables(idx, E, BM, tb):
     T, k = idx.shape
     A = T * k
