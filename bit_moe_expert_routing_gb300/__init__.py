@@ -65,6 +65,7 @@ SIGNATURES = {
     "moe_workspace_size": (_SZ, [_W, _CI]),
     "moe_layer_forward": (_CI, [_W, _VP, _CI, _VP, _VP, _SZ, _VP]),
     "moe_layer_forward_static": (_CI, [_W, _VP, _CI, _VP, _VP]),
+    "moe_get_device_status_static": (_CI, [_VP]),
     "moe_host_staging_size": (_SZ, [_W, _CI]),
     "moe_layer_forward_host": (_CI, [_W, _VP, _CI, _VP, _VP, _SZ, _VP]),
     "moe_route": (_CI, [_W, _VP, _CI, _VP, _SZ, _VP, ctypes.POINTER(moe_route_view)]),
@@ -123,8 +124,13 @@ def moe_layer_forward(w, x_ptr, T, y_ptr, ws_ptr, ws_bytes, stream) -> int:
 
 def moe_layer_forward_static(w, x_ptr, T, y_ptr, stream) -> int:
     """The layer with the library's fixed device scratch array as its
-    workspace, for callers that cannot allocate device memory (see include/moe.h)."""
+    workspace, for callers that cannot allocate device memory (include/moe.h
+    says which)."""
     return lib().moe_layer_forward_static(ctypes.byref(w), x_ptr, T, y_ptr, stream)
+
+
+def moe_get_device_status_static(stream) -> int:
+    return lib().moe_get_device_status_static(stream)
 
 
 def moe_layer_forward_host(w, x_host_ptr, T, y_host_ptr, ws_ptr, ws_bytes, stream) -> int:

@@ -191,7 +191,7 @@ cudaError_t zero_yacc(const Ctx& c) {
   const size_t n4 = size_t(c.T) * c.D / 4;
   zero_f32_kernel<<<4 * 152, 256, 0, c.stream>>>(reinterpret_cast<float4*>(c.y_acc), n4);
   cudaError_t err = cudaGetLastError();
-  if (err == cudaSuccess) launch_done("zero_yacc", c.stream);
+  if (err == cudaSuccess) launch_done(c, "zero_yacc");
   return err;
 }
 
@@ -200,7 +200,7 @@ cudaError_t cast_y(const Ctx& c) {
   cast_bf16_kernel<<<4 * 152, 256, 0, c.stream>>>(reinterpret_cast<const float4*>(c.y_acc),
                                                   reinterpret_cast<uint2*>(c.y), n4);
   cudaError_t err = cudaGetLastError();
-  if (err == cudaSuccess) launch_done("cast_y", c.stream);
+  if (err == cudaSuccess) launch_done(c, "cast_y");
   return err;
 }
 
@@ -217,12 +217,12 @@ cudaError_t gemm_simt(const Ctx& c) {
   if (err != cudaSuccess) return err;
   gemm_simt_kernel<true><<<dim3(c.max_blocks, c.I / SBN), 256, simt_smem_bytes(2), c.stream>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  launch_done("gateup_simt", c.stream);
+  launch_done(c, "gateup_simt");
   a.m0 = w->down;
   a.s0 = w->s_down;
   gemm_simt_kernel<false><<<dim3(c.max_blocks, c.D / SBN), 256, simt_smem_bytes(1), c.stream>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  launch_done("down_simt", c.stream);
+  launch_done(c, "down_simt");
   return cast_y(c);
 }
 

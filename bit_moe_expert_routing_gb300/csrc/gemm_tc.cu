@@ -589,11 +589,6 @@ int num_sms() {
   return n;
 }
 
-long long g_epi_wait_limit = 0;  // 0: no test wait
-
-void set_tc_epilogue_wait_limit(long long cycles) { g_epi_wait_limit = cycles > 0 ? cycles : 0; }
-long long tc_epilogue_wait_limit() { return g_epi_wait_limit; }
-
 cudaError_t debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, uint16_t* out, cudaStream_t s) {
   debug_dequant_kernel<<<256, 256, 0, s>>>(*m, expert, rows, K, out);
   return cudaGetLastError();
@@ -609,7 +604,7 @@ cudaError_t gemm_tc(const Ctx& c) {
   const int A = c.T * c.k;
   TcArgs a{c.x,      w->gate,   w->up,      w->s_gate, w->s_up, c.blocks, c.n_blocks, c.perm,
            c.topk_w, c.h,       c.y_acc,    c.hdr,     c.T,     c.D,      c.E,        c.k,
-           c.I,      c.max_blocks, g_epi_wait_limit};
+           c.I,      c.max_blocks, (long long)c.opt.test_wait_cycles};
   TcMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   const auto U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
@@ -625,7 +620,7 @@ cudaError_t gemm_tc(const Ctx& c) {
   const int grid1 = std::max(1, std::min(num_sms(), c.max_blocks * (c.I / 128)));
   gemm_tc_kernel<true><<<grid1, kNumThreads, kSmemBytes, c.stream>>>(a, maps);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  launch_done("gateup_tc", c.stream);
+  launch_done(c, "gateup_tc");
 
   a.m0 = w->down;
   a.s0 = w->s_down;
@@ -638,7 +633,7 @@ cudaError_t gemm_tc(const Ctx& c) {
   const int grid2 = std::max(1, std::min(num_sms(), c.max_blocks * (c.D / BN)));
   gemm_tc_kernel<false><<<grid2, kNumThreads, kSmemBytes, c.stream>>>(a, maps);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  launch_done("down_tc", c.stream);
+  launch_done(c, "down_tc");
   return cast_y(c);
 }
 

@@ -674,7 +674,7 @@ cudaError_t gemm_wt(const Ctx& c) {
   const int A = c.T * c.k;
   WtArgs a{c.xperm,  w->gate, w->up,   w->s_gate, w->s_up, c.blocks, c.n_blocks, c.perm, c.topk_w,
            c.h,      c.y_acc, c.hdr,   c.T,       c.D,     c.E,      c.k,        c.I,    c.max_blocks,
-           tc_epilogue_wait_limit()};
+           (long long)c.opt.test_wait_cycles};
   WtMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   const auto U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
@@ -689,7 +689,7 @@ cudaError_t gemm_wt(const Ctx& c) {
   const int grid1 = std::max(1, std::min(num_sms(), c.max_blocks * (c.I / 64)));
   gemm_wt_kernel<true><<<grid1, kNumThreads, kSmemBytes, c.stream>>>(a, maps);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  launch_done("gateup_tc", c.stream);
+  launch_done(c, "gateup_tc");
 
   a.m0 = w->down;
   a.s0 = w->s_down;
@@ -702,7 +702,7 @@ cudaError_t gemm_wt(const Ctx& c) {
   const int grid2 = std::max(1, std::min(num_sms(), c.max_blocks * (c.D / WM)));
   gemm_wt_kernel<false><<<grid2, kNumThreads, kSmemBytes, c.stream>>>(a, maps);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  launch_done("down_tc", c.stream);
+  launch_done(c, "down_tc");
   return cast_y(c);
 }
 

@@ -34,6 +34,7 @@
 // Lane l works on chunk c = l + 32m, so the lanes of a warp read consecutive
 // float4s and consecutive 16-byte code chunks (no bank conflicts).
 #include <algorithm>
+#include <cstddef>
 #include <mutex>
 #include <vector>
 
@@ -728,10 +729,10 @@ cudaError_t gemv(const Ctx& c) {
   cudaError_t err;
   gemv_gateup_kernel<<<dim3(c.max_blocks, (c.I + kGateupRows - 1) / kGateupRows), kGemvWarps * 32, s1, c.stream>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  launch_done("gemv_gateup", c.stream);
+  launch_done(c, "gemv_gateup");
   gemv_down_kernel<<<dim3(c.D / kDownCols, c.T), kGemvWarps * 32, s2, c.stream>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  launch_done("gemv_down", c.stream);
+  launch_done(c, "gemv_down");
   return cudaSuccess;
 }
 
@@ -800,15 +801,18 @@ cudaError_t decode_fused(const Ctx& c) {
               w->router_w,  w->router_bias, c.logits, c.topk_idx,  c.topk_w,  c.count, c.off,
               c.perm,       c.inv,          c.blocks, c.n_blocks,  c.h,       c.y,     c.hdr,
               c.D,          c.E,            c.k,      c.I,         p.n_items, p.n_groups};
-  // status and grid-barrier counter start at zero for this call
-  cudaError_t err = cudaMemsetAsync(c.hdr, 0, 16, c.stream);
+  // the grid-barrier counter starts at zero; on the call's first pass the
+  // status does too (later passes keep what earlier ones recorded)
+  static_assert(offsetof(WsHeader, counter) == 8, "status, detail, counter");
+  cudaError_t err = c.first_pass ? cudaMemsetAsync(c.hdr, 0, 12, c.stream)
+                                 : cudaMemsetAsync(&c.hdr->counter, 0, 4, c.stream);
   if (err != cudaSuccess) return err;
   void* args[] = {&a};
   const void* f = p.mpl == 8 ? reinterpret_cast<const void*>(decode_fused_kernel<8>)
                              : reinterpret_cast<const void*>(decode_fused_kernel<16>);
   err = cudaLaunchCooperativeKernel(f, dim3(p.grid), dim3(kFdWarps * 32), args, p.smem, c.stream);
   if (err != cudaSuccess) return err;
-  launch_done("decode_fused", c.stream);
+  launch_done(c, "decode_fused");
   return cudaSuccess;
 }
 

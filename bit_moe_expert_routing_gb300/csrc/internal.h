@@ -20,8 +20,26 @@ constexpr int kTcBlockRows = 128;  // weights dequantised into shared memory (MM
 constexpr int kWtBlockRows = 192;  // weights dequantised into tensor memory (MMA N = tokens)
 constexpr int kMinBlockM = 16;      // smallest block size MOE_OPT_BLOCK_M accepts; sizes the block map
 
+// Library options (moe_set_option). A call works on its own copy, taken
+// once when the call starts, so that another thread's moe_set_option cannot
+// change a call part-way.
+struct Options {
+  int gemv_max_rows = 4;
+  int force_path = 0;
+  int kernel_timing = 0;
+  int gemm_impl = 0;
+  int test_wait_cycles = 0;
+  int block_m = 0;  // 0: the path's own block size
+  int decode_fused = 1;
+  int chunk_tokens = 8192;  // 0: one pass over all T
+  int host_sync_routing = 0;
+};
+Options options_snapshot();
+
 // One call's resolved sizes and device pointers.
 struct Ctx {
+  Options opt;      // the call's options
+  bool first_pass = true;  // first pass of its call: its first kernel clears the device status
   const moe_weights* w;
   int T, D, E, k, I;
   int BM;          // rows per block-map entry
@@ -67,8 +85,8 @@ int router_wave_tokens(int E);
 
 // Bookkeeping of launches: counts this library's kernels and, when kernel
 // timing is on, records an event after each one.
-void launch_done(const char* name, cudaStream_t s);
-void timing_begin(cudaStream_t s);
+void launch_done(const Ctx& c, const char* name);
+void timing_begin(const Ctx& c);
 
 // Routing: logits, top-k + weights + per-chunk histogram, scan + block map,
 // scatter. Returns the first CUDA error. With yacc_zeroed given, the router
@@ -84,8 +102,6 @@ cudaError_t cast_y(const Ctx& c);
 cudaError_t gemm_simt(const Ctx& c);
 cudaError_t gemm_tc(const Ctx& c);
 bool gemm_tc_supported(const Ctx& c);
-void set_tc_epilogue_wait_limit(long long cycles);  // <= 0: the normal limit
-long long tc_epilogue_wait_limit();
 cudaError_t gemm_wt(const Ctx& c);
 bool gemm_wt_supported(const Ctx& c);
 int num_sms();
@@ -103,10 +119,27 @@ bool gemv_supported(const Ctx& c);
 // (with the header zeroed on the stream first).
 cudaError_t decode_fused(const Ctx& c);
 bool decode_fused_supported(const Ctx& c);
-// Router logits only, for up to 16 tokens; also zeroes the header counter.
+// Router logits only, for up to 16 tokens.
 cudaError_t route_logits_small(const Ctx& c);
 
 cudaError_t debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, uint16_t* out,
                           cudaStream_t s);
+
+// Host-side checks and sizes shared by the entry points.
+constexpr int kMaxTokens = 1 << 20;
+moe_status check_weights(const moe_weights* w);
+// Tokens of one pass of a T-token call: T, or the chunk size when chunking
+// is on and T is larger.
+int pass_tokens(int T, const Options& opt);
+// Workspace bytes of one pass over T tokens.
+size_t pass_workspace_bytes(const moe_weights* w, int T);
+// Starts this thread's launch count of a call at zero.
+void reset_launch_count();
+
+// The layer over T tokens as consecutive passes of at most `pass_tokens`
+// tokens, all reusing one workspace laid out for a pass (the body of the
+// workspace entry points). Counts the call's launches from zero.
+moe_status forward_passes(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* workspace,
+                          size_t workspace_bytes, void* stream, int pass_tokens, const Options& opt);
 
 }  // namespace moe

@@ -16,19 +16,9 @@ namespace {
 
 constexpr int kDefaultBlockM = 128;
 
-struct Options {
-  int gemv_max_rows = 4;
-  int force_path = 0;
-  int kernel_timing = 0;
-  int gemm_impl = 0;
-  int test_wait_cycles = 0;
-  int block_m = 0;  // 0: the path's own block size
-  int decode_fused = 1;
-  int chunk_tokens = 8192;  // 0: one pass over all T
-  int host_sync_routing = 0;
-};
-Options g_opt;
-std::mutex g_mu;
+Options g_opt;         // process-wide options, under g_opt_mu
+std::mutex g_opt_mu;
+std::mutex g_mu;       // kernel-timing marks
 
 thread_local int t_launches = 0;
 
@@ -105,6 +95,8 @@ moe_status check_qmat(const moe_qmatrix& m) {
   return MOE_OK;
 }
 
+}  // namespace
+
 moe_status check_weights(const moe_weights* w) {
   if (!w) return MOE_ERR_ARG;
   if (w->D < 64 || w->D > 16384 || w->D % 64 || w->I < 64 || w->I > 4096 || w->I % 64) return MOE_ERR_SHAPE;
@@ -116,19 +108,25 @@ moe_status check_weights(const moe_weights* w) {
   return MOE_OK;
 }
 
-constexpr int kMaxT = 1 << 20;
+constexpr int kMaxT = kMaxTokens;
 
-// Tokens of one pass: T, or the chunk size when chunking is on and T is larger.
-int pass_tokens(int T) { return (g_opt.chunk_tokens > 0 && T > g_opt.chunk_tokens) ? g_opt.chunk_tokens : T; }
+int pass_tokens(int T, const Options& o) { return (o.chunk_tokens > 0 && T > o.chunk_tokens) ? o.chunk_tokens : T; }
+
+size_t pass_workspace_bytes(const moe_weights* w, int T) { return layout(w, T).total; }
+
+void reset_launch_count() { t_launches = 0; }
+
+namespace {
 
 moe_status make_ctx(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* ws, size_t ws_bytes,
-                    void* stream, Ctx* c) {
+                    void* stream, const Options& opt, Ctx* c) {
   if (moe_status s = check_weights(w)) return s;
   if (T < 0 || T > kMaxT) return MOE_ERR_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return MOE_ERR_WORKSPACE;
   const Layout L = layout(w, T);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   char* base = static_cast<char*>(ws);
+  c->opt = opt;
   c->w = w;
   c->T = T;
   c->D = w->D;
@@ -184,19 +182,20 @@ enum class Path { DecodeFused, Gemv, GemmWt, GemmTc, GemmSimt };
 // consumes: 192 tokens per block for the tensor-core GEMM with weights in
 // tensor memory, 128 for the others.
 Path plan(Ctx& c) {
-  int path = g_opt.force_path;
-  if (path == 0) path = (c.T <= g_opt.gemv_max_rows) ? 1 : 2;
+  const Options& o = c.opt;
+  int path = o.force_path;
+  if (path == 0) path = (c.T <= o.gemv_max_rows) ? 1 : 2;
   Path p;
   if (path == 1 && gemv_supported(c))
-    p = (g_opt.decode_fused && decode_fused_supported(c)) ? Path::DecodeFused : Path::Gemv;
-  else if (g_opt.gemm_impl == 0 && gemm_wt_supported(c))
+    p = (o.decode_fused && decode_fused_supported(c)) ? Path::DecodeFused : Path::Gemv;
+  else if (o.gemm_impl == 0 && gemm_wt_supported(c))
     p = Path::GemmWt;
-  else if (g_opt.gemm_impl == 2 && gemm_tc_supported(c))
+  else if (o.gemm_impl == 2 && gemm_tc_supported(c))
     p = Path::GemmTc;
   else
     p = Path::GemmSimt;
   const int path_bm = (p == Path::GemmWt) ? kWtBlockRows : (p == Path::GemmTc) ? kTcBlockRows : kDefaultBlockM;
-  c.BM = g_opt.block_m > 0 ? std::min(g_opt.block_m, path_bm) : path_bm;
+  c.BM = o.block_m > 0 ? std::min(o.block_m, path_bm) : path_bm;
   return p;
 }
 
@@ -220,13 +219,18 @@ bool ensure_smem_limit(const void* func, int bytes) {
   return true;
 }
 
-void launch_done(const char* name, cudaStream_t s) {
+void launch_done(const Ctx& c, const char* name) {
   ++t_launches;
-  if (g_opt.kernel_timing) mark(name, s);
+  if (c.opt.kernel_timing) mark(name, c.stream);
 }
 
-void timing_begin(cudaStream_t s) {
-  if (g_opt.kernel_timing) mark(nullptr, s);
+void timing_begin(const Ctx& c) {
+  if (c.opt.kernel_timing) mark(nullptr, c.stream);
+}
+
+Options options_snapshot() {
+  std::lock_guard<std::mutex> lk(g_opt_mu);
+  return g_opt;
 }
 
 }  // namespace moe
@@ -237,24 +241,25 @@ extern "C" {
 
 size_t moe_workspace_size(const moe_weights* w, int T) {
   if (check_weights(w) != MOE_OK || T < 0 || T > kMaxT) return 0;
-  return layout(w, pass_tokens(T)).total;
+  return layout(w, pass_tokens(T, options_snapshot())).total;
 }
 
 size_t moe_host_staging_size(const moe_weights* w, int T) {
   if (check_weights(w) != MOE_OK || T < 0 || T > kMaxT) return 0;
-  return 2 * al256(size_t(pass_tokens(T)) * w->D * 2);
+  return 2 * al256(size_t(pass_tokens(T, options_snapshot())) * w->D * 2);
 }
 
 moe_status moe_route(const moe_weights* w, const uint16_t* x, int T, void* workspace, size_t workspace_bytes,
                      void* stream, moe_route_view* view) {
   Ctx c;
-  if (moe_status s = make_ctx(w, x, T, nullptr, workspace, workspace_bytes, stream, &c)) return s;
+  if (moe_status s = make_ctx(w, x, T, nullptr, workspace, workspace_bytes, stream, options_snapshot(), &c))
+    return s;
   if (T > 0 && (!x || !aligned16(x))) return MOE_ERR_ARG;
   t_launches = 0;
   plan(c);
   if (view) fill_view(c, view);
   if (T == 0) return MOE_OK;
-  timing_begin(c.stream);
+  timing_begin(c);
   return cuda_status(route(c));
 }
 
@@ -262,7 +267,8 @@ moe_status moe_workspace_view(const moe_weights* w, int T, void* workspace, size
                               moe_route_view* view) {
   Ctx c;
   if (!view) return MOE_ERR_ARG;
-  if (moe_status s = make_ctx(w, nullptr, T, nullptr, workspace, workspace_bytes, nullptr, &c)) return s;
+  if (moe_status s = make_ctx(w, nullptr, T, nullptr, workspace, workspace_bytes, nullptr, options_snapshot(), &c))
+    return s;
   plan(c);
   fill_view(c, view);
   return MOE_OK;
@@ -271,25 +277,29 @@ moe_status moe_workspace_view(const moe_weights* w, int T, void* workspace, size
 // One pass of the layer over T tokens (T no larger than the workspace was
 // laid out for). Adds its launches to the thread's count.
 // With n_x_slices > 0, x arrives on another stream in slices (see Ctx).
+// first_pass: the pass's first kernel starts the call's device status afresh
+// (later passes keep what earlier ones recorded).
 static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* workspace,
-                               size_t workspace_bytes, void* stream, int n_x_slices = 0,
-                               const int* x_slice_end = nullptr, const cudaEvent_t* x_ready = nullptr) {
+                               size_t workspace_bytes, void* stream, const Options& opt, bool first_pass,
+                               int n_x_slices = 0, const int* x_slice_end = nullptr,
+                               const cudaEvent_t* x_ready = nullptr) {
   Ctx c;
-  if (moe_status s = make_ctx(w, x, T, y, workspace, workspace_bytes, stream, &c)) return s;
+  if (moe_status s = make_ctx(w, x, T, y, workspace, workspace_bytes, stream, opt, &c)) return s;
   if (T == 0) return MOE_OK;
+  c.first_pass = first_pass;
   c.n_x_slices = n_x_slices;
   c.x_slice_end = x_slice_end;
   c.x_ready = x_ready;
   const Path path = plan(c);
   if (path == Path::GemmWt) c.xperm = c.xperm_area;  // the router writes the paired-order x it gathers
-  timing_begin(c.stream);
+  timing_begin(c);
   if (path == Path::DecodeFused) {  // routing included
     if (wait_x(c) != cudaSuccess) return MOE_ERR_CUDA;
     return cuda_status(decode_fused(c));
   }
   cudaError_t err = route(c, path == Path::Gemv ? nullptr : &c.yacc_zeroed);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
-  if (g_opt.host_sync_routing) {
+  if (c.opt.host_sync_routing) {
     // the host-scheduled variant: the block count comes back to the host
     // before the expert kernels are launched (a stream synchronisation)
     static thread_local int* nb_host = nullptr;
@@ -305,6 +315,24 @@ static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, u
   return cuda_status(gemm_simt(c));
 }
 
+}  // extern "C"
+
+moe_status moe::forward_passes(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* workspace,
+                               size_t workspace_bytes, void* stream, int step, const Options& opt) {
+  t_launches = 0;
+  if (T == 0) return forward_pass(w, x, 0, y, workspace, workspace_bytes, stream, opt, true);  // checks the workspace
+  if (!x || !y || !aligned16(x) || !aligned16(y) || x == y || step < 1) return MOE_ERR_ARG;
+  for (int t0 = 0; t0 < T; t0 += step) {
+    const int n = std::min(step, T - t0);
+    const size_t at = size_t(t0) * w->D;
+    if (moe_status s = forward_pass(w, x + at, n, y + at, workspace, workspace_bytes, stream, opt, t0 == 0))
+      return s;
+  }
+  return MOE_OK;
+}
+
+extern "C" {
+
 // Prompt chunking ("Optimizing on-device inference for Apple Silicon",
 // section "Bound temporary memory with prompt chunking"): T above the chunk
 // size runs as consecutive passes over bounded token ranges on the caller's
@@ -312,18 +340,10 @@ static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, u
 // independent in this layer, so the output is the one pass's output.
 moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* workspace,
                              size_t workspace_bytes, void* stream) {
+  const Options opt = options_snapshot();
   if (moe_status s = check_weights(w)) return s;
   if (T < 0 || T > kMaxT) return MOE_ERR_ARG;
-  t_launches = 0;
-  if (T == 0) return forward_pass(w, x, 0, y, workspace, workspace_bytes, stream);  // checks the workspace
-  if (!x || !y || !aligned16(x) || !aligned16(y) || x == y) return MOE_ERR_ARG;
-  const int step = pass_tokens(T);
-  for (int t0 = 0; t0 < T; t0 += step) {
-    const int n = std::min(step, T - t0);
-    const size_t at = size_t(t0) * w->D;
-    if (moe_status s = forward_pass(w, x + at, n, y + at, workspace, workspace_bytes, stream)) return s;
-  }
-  return MOE_OK;
+  return forward_passes(w, x, T, y, workspace, workspace_bytes, stream, pass_tokens(T, opt), opt);
 }
 
 // The host entry point's copy stream and events, one set per thread and
@@ -356,13 +376,15 @@ static HostPipe* host_pipe() {
 
 moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, int T, uint16_t* y_host,
                                   void* workspace, size_t workspace_bytes, void* stream) {
+  const Options opt = options_snapshot();
   if (check_weights(w) != MOE_OK) return check_weights(w);
   if (T < 0 || T > kMaxT) return MOE_ERR_ARG;
+  t_launches = 0;
   if (T == 0) return MOE_OK;
   if (!x_host || !y_host) return MOE_ERR_ARG;
   // one pass's tokens are staged at a time: x in, the layer, y out
-  const int step = pass_tokens(T);
-  const size_t need = moe_workspace_size(w, T), stage = al256(size_t(step) * w->D * 2);
+  const int step = pass_tokens(T, opt);
+  const size_t need = layout(w, step).total, stage = al256(size_t(step) * w->D * 2);
   if (!workspace || workspace_bytes < need + 2 * stage) return MOE_ERR_WORKSPACE;
   char* base = static_cast<char*>(workspace);
   uint16_t* xd = reinterpret_cast<uint16_t*>(base + need);
@@ -381,7 +403,6 @@ moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, 
     else
       cudaGetLastError();  // an unregistered pointer is not an error here
   }
-  t_launches = 0;
   for (int t0 = 0; t0 < T; t0 += step) {
     const int n = std::min(step, T - t0);
     const size_t at = size_t(t0) * w->D;
@@ -403,7 +424,8 @@ moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, 
         return MOE_ERR_CUDA;
       if (cudaEventRecord(hp->ready[i], hp->copy) != cudaSuccess) return MOE_ERR_CUDA;
     }
-    moe_status st = forward_pass(w, xd, n, y_direct ? y_direct + at : yd, workspace, need, stream, n_sl, end, hp->ready);
+    moe_status st = forward_pass(w, xd, n, y_direct ? y_direct + at : yd, workspace, need, stream, opt, t0 == 0,
+                                 n_sl, end, hp->ready);
     if (st != MOE_OK) {
       cudaStreamSynchronize(hp->copy);  // no copy into the workspace outlives the call
       return st;
@@ -429,6 +451,7 @@ moe_status moe_get_device_status(void* workspace, void* stream) {
 }
 
 moe_status moe_set_option(int option, int value) {
+  std::lock_guard<std::mutex> lk(g_opt_mu);
   switch (option) {
     case MOE_OPT_GEMV_MAX_ROWS:
       if (value < 0 || value > 8) return MOE_ERR_ARG;
@@ -465,7 +488,6 @@ moe_status moe_set_option(int option, int value) {
     case MOE_OPT_TEST_WAIT_CYCLES:
       if (value < 0) return MOE_ERR_ARG;
       g_opt.test_wait_cycles = value;
-      set_tc_epilogue_wait_limit(value);
       return MOE_OK;
     default:
       return MOE_ERR_ARG;
@@ -473,6 +495,7 @@ moe_status moe_set_option(int option, int value) {
 }
 
 int moe_get_option(int option) {
+  std::lock_guard<std::mutex> lk(g_opt_mu);
   switch (option) {
     case MOE_OPT_GEMV_MAX_ROWS: return g_opt.gemv_max_rows;
     case MOE_OPT_FORCE_PATH: return g_opt.force_path;

@@ -1,10 +1,9 @@
 // The layer with its scratch memory in a fixed device array of this library,
-// for callers that cannot allocate device memory. Such callers include code
-// that runs while a CUDA graph is being captured or replayed, real-time or
-// embedded loops that forbid cudaMalloc after start-up (it can synchronise
-// the device and fail when memory is fragmented), and plug-in hosts that own
-// the device allocator and give their plug-ins only input and output
-// buffers.
+// for callers that cannot allocate device memory. Such callers include
+// real-time or embedded loops that forbid cudaMalloc after start-up (it can
+// synchronise the device and fail when memory is fragmented), and plug-in
+// hosts that own the device allocator and give their plug-ins only input
+// and output buffers.
 //
 // The scratch array below is part of the library image: every GPU that loads
 // the library holds it until the process exits, whether or not this entry
@@ -19,6 +18,7 @@
 #include <mutex>
 
 #include "../../include/moe.h"
+#include "internal.h"
 
 namespace {
 
@@ -44,15 +44,16 @@ void* static_scratch_on_current_device() {
   return ptrs[dev];
 }
 
-// Largest token count, at most T, whose workspace fits the array (0 if even
-// one token does not). The size grows with the token count up to the chunk
-// size and is flat beyond it, so a bisection finds it.
-int tokens_fitting(const moe_weights* w, int T) {
-  if (moe_workspace_size(w, T) <= kStaticScratchBytes) return T;
-  int lo = 0, hi = T;  // size(lo) fits (or lo = 0), size(hi) does not
+// Largest token count, at most the call's pass size, whose workspace fits the
+// array (0 if even one token does not). The size grows with the token count,
+// so a bisection finds it.
+int tokens_fitting(const moe_weights* w, int T, const moe::Options& opt) {
+  const int cap = moe::pass_tokens(T, opt);
+  if (moe::pass_workspace_bytes(w, cap) <= kStaticScratchBytes) return cap;
+  int lo = 0, hi = cap;  // size(lo) fits (or lo = 0), size(hi) does not
   while (hi - lo > 1) {
     const int mid = lo + (hi - lo) / 2;
-    if (moe_workspace_size(w, mid) <= kStaticScratchBytes)
+    if (moe::pass_workspace_bytes(w, mid) <= kStaticScratchBytes)
       lo = mid;
     else
       hi = mid;
@@ -60,21 +61,29 @@ int tokens_fitting(const moe_weights* w, int T) {
   return lo;
 }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 }  // namespace
 
 extern "C" moe_status moe_layer_forward_static(const moe_weights* w, const uint16_t* x, int T, uint16_t* y,
                                                void* stream) {
-  const size_t need = moe_workspace_size(w, T);
-  if (need == 0 || T == 0) return moe_layer_forward(w, x, T, y, nullptr, 0, stream);  // names the error, or T = 0
-  const int step = tokens_fitting(w, T);
+  const moe::Options opt = moe::options_snapshot();
+  if (moe_status s = moe::check_weights(w)) return s;
+  if (T < 0 || T > moe::kMaxTokens) return MOE_ERR_ARG;
+  if (T == 0) {  // a no-op, as for the workspace entry point
+    moe::reset_launch_count();
+    return MOE_OK;
+  }
+  if (!x || !y || !aligned16(x) || !aligned16(y) || x == y) return MOE_ERR_ARG;
+  const int step = tokens_fitting(w, T, opt);
   if (step == 0) return MOE_ERR_WORKSPACE;
   void* scratch = static_scratch_on_current_device();
   if (!scratch) return MOE_ERR_CUDA;
-  if (!x || !y) return MOE_ERR_ARG;
-  for (int t0 = 0; t0 < T; t0 += step) {
-    const int n = T - t0 < step ? T - t0 : step;
-    const size_t at = size_t(t0) * w->D;
-    if (moe_status s = moe_layer_forward(w, x + at, n, y + at, scratch, kStaticScratchBytes, stream)) return s;
-  }
-  return MOE_OK;
+  return moe::forward_passes(w, x, T, y, scratch, kStaticScratchBytes, stream, step, opt);
+}
+
+extern "C" moe_status moe_get_device_status_static(void* stream) {
+  void* scratch = static_scratch_on_current_device();
+  if (!scratch) return MOE_ERR_CUDA;
+  return moe_get_device_status(scratch, stream);  // the status word heads the array
 }

@@ -64,9 +64,10 @@ __global__ void __launch_bounds__(kRtWarps * 32, 1)
     router_tree_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
                        int T, int D, int E, float* __restrict__ logits, WsHeader* hdr,
                        float4* __restrict__ yacc, size_t yacc_n4) {
-  // First kernel of every call: start the call's device status afresh (hdr
-  // is null for the later launches of a sliced router). No other CTA of this
-  // kernel reports, so nothing races with the clear.
+  // First kernel of a call: start the call's device status afresh (hdr is
+  // null for the later launches of a sliced router and for the later passes
+  // of a call, which keep what earlier passes recorded). No other CTA of
+  // this kernel reports, so nothing races with the clear.
   if (hdr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     hdr->status = 0;
     hdr->detail = 0;
@@ -420,7 +421,7 @@ template <int TT>
 __global__ void __launch_bounds__(kRouterSmallExperts * 32)
     router_small_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
                         const float* __restrict__ bias, int T, int D, int E, float* __restrict__ logits,
-                        WsHeader* hdr) {
+                        WsHeader* hdr, int clear_status) {
   extern __shared__ __align__(128) uint8_t rsm[];
   const uint32_t bar = smem_u32(rsm);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(rsm + 8);
@@ -430,10 +431,9 @@ __global__ void __launch_bounds__(kRouterSmallExperts * 32)
   const int e0 = blockIdx.x * kRouterSmallExperts;
   const int ne = min(kRouterSmallExperts, E - e0);
   if (threadIdx.x == 0) {
-    if (blockIdx.x == 0) {  // first kernel of the call: start its status afresh
+    if (blockIdx.x == 0 && clear_status) {  // first kernel of the call: start its status afresh
       hdr->status = 0;
       hdr->detail = 0;
-      hdr->counter = 0;  // the fused decode's grid barrier counts from here
     }
     *abort_flag = 0;
     mbar_init(bar, 1);
@@ -554,15 +554,15 @@ cudaError_t route_logits_small(const Ctx& c) {
   const moe_weights* w = c.w;
   if (c.T > kSmallRouteTokens || c.D > 4096) return cudaErrorInvalidValue;
   const int tt = c.T <= 2 ? 2 : c.T <= 8 ? 8 : 16;
-  void (*rk)(const uint16_t*, const float*, const float*, int, int, int, float*, WsHeader*) =
+  void (*rk)(const uint16_t*, const float*, const float*, int, int, int, float*, WsHeader*, int) =
       tt == 2 ? router_small_kernel<2> : tt == 8 ? router_small_kernel<8> : router_small_kernel<16>;
   const size_t smem = router_small_smem(tt, c.D);
   if (!ensure_smem_limit(reinterpret_cast<const void*>(rk), int(smem))) return cudaErrorInvalidValue;
   rk<<<(c.E + kRouterSmallExperts - 1) / kRouterSmallExperts, kRouterSmallExperts * 32, smem, c.stream>>>(
-      c.x, w->router_w, w->router_bias, c.T, c.D, c.E, c.logits, c.hdr);
+      c.x, w->router_w, w->router_bias, c.T, c.D, c.E, c.logits, c.hdr, c.first_pass ? 1 : 0);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  launch_done("router_small", c.stream);
+  launch_done(c, "router_small");
   return cudaSuccess;
 }
 
@@ -602,7 +602,7 @@ cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
       permute_x_kernel<<<unsigned(std::min<size_t>((n8 + 255) / 256, size_t(num_sms()))), 256, 0, c.stream>>>(
           c.x, c.xperm, n8);
       if ((err = cudaGetLastError()) != cudaSuccess) return err;
-      launch_done("permute_x", c.stream);
+      launch_done(c, "permute_x");
     }
     if ((err = route_logits_small(c)) != cudaSuccess) return err;
     const int mpl = (c.E + 31) / 32;
@@ -613,7 +613,7 @@ cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
                                                  c.topk_w, c.count, c.off, c.perm, c.inv, c.blocks, c.n_blocks,
                                                  c.hdr);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    launch_done("route_small", c.stream);
+    launch_done(c, "route_small");
     return cudaSuccess;
   }
   {
@@ -631,10 +631,10 @@ cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
         const int n = t1 - t0;
         rk<<<dim3((n + kRtTok - 1) / kRtTok, (c.E + kRtExp - 1) / kRtExp), kRtWarps * 32, smem, c.stream>>>(
             c.x + size_t(t0) * c.D, w->router_w, w->router_bias, n, c.D, c.E, c.logits + size_t(t0) * c.E,
-            t0 == 0 ? c.hdr : nullptr, zero ? reinterpret_cast<float4*>(c.y_acc + size_t(t0) * c.D) : nullptr,
+            (t0 == 0 && c.first_pass) ? c.hdr : nullptr, zero ? reinterpret_cast<float4*>(c.y_acc + size_t(t0) * c.D) : nullptr,
             zero ? size_t(n) * c.D / 4 : 0);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
-        launch_done("router_logits", c.stream);
+        launch_done(c, "router_logits");
       }
       t0 = t1;
     }
@@ -653,17 +653,17 @@ cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
         c.logits, c.T, c.E, c.k, c.topk_idx, c.topk_w, c.chunk, c.n_chunks, c.x, c.D, c.xperm);
   }
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  launch_done("topk_hist", c.stream);
+  launch_done(c, "topk_hist");
 
   scan_blocks_kernel<<<1, 1024, 0, c.stream>>>(c.T, c.E, c.k, c.BM, c.n_chunks, c.max_blocks, c.chunk,
                                                c.count, c.off, c.blocks, c.n_blocks, c.hdr);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  launch_done("scan_blocks", c.stream);
+  launch_done(c, "scan_blocks");
 
   scatter_kernel<<<c.n_chunks, 256, 9 * c.E * sizeof(int), c.stream>>>(c.topk_idx, c.T, c.E, c.k, c.chunk,
                                                                        c.perm, c.inv, c.hdr);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  launch_done("scatter", c.stream);
+  launch_done(c, "scatter");
   return cudaSuccess;
 }
 

@@ -30,7 +30,9 @@
  *     reported by moe_get_device_status().
  *   - Not re-entrant on one workspace: two calls that overlap on the GPU must
  *     use distinct workspaces. Distinct workspaces and streams are
- *     independent. Options (moe_set_option) are process-wide.
+ *     independent. Options (moe_set_option) are process-wide; each call
+ *     takes a copy of them when it starts, so a moe_set_option from another
+ *     thread never changes a call part-way (it applies from the next call).
  */
 #ifndef MOE_H_
 #define MOE_H_
@@ -166,15 +168,26 @@ typedef enum {
 /* Bytes of workspace one call with T tokens needs (pure host; 0 on bad
  * arguments): the tables and buffers of one pass of min(T, chunk tokens)
  * tokens (MOE_OPT_CHUNK_TOKENS), so it stops growing at the chunk size. The
- * workspace also holds the device status word. */
+ * workspace also holds the device status word. The buffers are the routing
+ * tables of "Keep expert routing on the GPU" (logits, top-k, counts, offsets,
+ * permutation, block map), the intermediate of "Reduce intermediate and
+ * state traffic" and the one-pass bound of "Bound temporary memory with
+ * prompt chunking" ("Optimizing on-device inference for Apple Silicon"). */
 size_t moe_workspace_size(const moe_weights* w, int T);
 
-/* The whole layer on the GPU: routing (logits, top-k, weights, histogram,
- * scan, scatter, block map), then either the grouped-GEMM path or the decode
- * GEMV path, then the combine into y. Everything is enqueued on `stream` with
- * no host synchronisation. x: device bf16 [T, D]; y: device bf16 [T, D]
- * (may not alias x); workspace: device, >= moe_workspace_size(w, T) bytes,
- * 256-byte aligned. T = 0 is a no-op returning MOE_OK. */
+/* The whole layer on the GPU ("Optimizing on-device inference for Apple
+ * Silicon": the routed and shared experts of "Qwen creates three workload
+ * shapes", the routing of "Keep expert routing on the GPU", the fused
+ * dequantising matrix kernels of "Dequantise weights during matrix
+ * multiplication" for many rows and the single-row path of "Optimise the
+ * single-row weight path" for few, with the row-count switch of "Why
+ * continuous batching halved LLM throughput on an M2 Mac mini"): routing
+ * (logits, top-k, weights, histogram, scan, scatter, block map), then either
+ * the grouped-GEMM path or the decode GEMV path, then the combine into y.
+ * Everything is enqueued on `stream` with no host synchronisation.
+ * x: device bf16 [T, D]; y: device bf16 [T, D] (may not alias x); workspace:
+ * device, >= moe_workspace_size(w, T) bytes, 256-byte aligned. T = 0 is a
+ * no-op returning MOE_OK. */
 moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uint16_t* y,
                              void* workspace, size_t workspace_bytes, void* stream);
 
@@ -198,8 +211,11 @@ moe_status moe_layer_forward_host(const moe_weights* w, const uint16_t* x_host, 
                                   uint16_t* y_host, void* workspace, size_t workspace_bytes,
                                   void* stream);
 
-/* Routing only (the first five steps of the layer), on `stream`, no host
- * sync; fills `view` with device pointers into the workspace. The tables are
+/* Routing only (the first five steps of the layer: the router and top-k of
+ * "Qwen creates three workload shapes", then the histogram, scan, scatter and
+ * block map of "Keep expert routing on the GPU", "Optimizing on-device
+ * inference for Apple Silicon"), on `stream`, no host sync; fills `view`
+ * with device pointers into the workspace. The tables are
  * the ones moe_layer_forward builds for the same T (same block_m). All T
  * tokens are routed in one pass: for T above the chunk size the workspace
  * must be sized with chunking off (MOE_OPT_CHUNK_TOKENS = 0), else the call
@@ -213,7 +229,9 @@ moe_status moe_workspace_view(const moe_weights* w, int T, void* workspace,
                               size_t workspace_bytes, moe_route_view* view);
 
 /* Synchronises `stream`, then returns (and clears) the device status word of
- * `workspace`: MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_CHECK. */
+ * `workspace`: MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_CHECK, the
+ * first error any pass of the last call on that workspace recorded (a call
+ * starts the word afresh; its later passes keep what earlier ones found). */
 moe_status moe_get_device_status(void* workspace, void* stream);
 
 moe_status moe_set_option(int option, int value);
@@ -240,11 +258,13 @@ moe_status moe_debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, 
 /* The whole layer, like moe_layer_forward(), but with no workspace argument:
  * its scratch memory is a fixed 8 MiB device array inside this library, so
  * the call allocates no device memory at all. (The source pages have no
- * counterpart; this serves callers that cannot allocate: code running while a
- * CUDA graph is captured, loops that forbid cudaMalloc after start-up because
- * it can synchronise the device or fail on fragmentation, and hosts that hand
- * their plug-ins only input and output buffers.)
+ * counterpart; this serves callers that cannot allocate: loops that forbid
+ * cudaMalloc after start-up because it can synchronise the device or fail on
+ * fragmentation, and hosts that hand their plug-ins only input and output
+ * buffers.)
  *   x, y, stream: as for moe_layer_forward(); the caller still owns them.
+ *   T = 0 is a no-op returning MOE_OK; bad arguments are rejected on the
+ *   host, before anything is enqueued, as for moe_layer_forward().
  *   Any T: the tokens run in consecutive passes of the largest count whose
  *   workspace fits MOE_STATIC_SCRATCH_BYTES (and no larger than the chunk
  *   size; for the D=2048, E=256, k=8, I=512 layer, 451 tokens). A layer whose
@@ -260,7 +280,13 @@ moe_status moe_debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, 
 moe_status moe_layer_forward_static(const moe_weights* w, const uint16_t* x, int T, uint16_t* y,
                                     void* stream);
 
-/* Number of this library's kernels the last forward on this thread launched. */
+/* moe_get_device_status() for the scratch array of moe_layer_forward_static()
+ * on the current device: synchronises `stream`, then returns and clears the
+ * first device-side error any pass of the last static call recorded. */
+moe_status moe_get_device_status_static(void* stream);
+
+/* Number of this library's kernels the last forward call on this thread
+ * launched (all of its passes). */
 int moe_last_launch_count(void);
 
 const char* moe_status_string(moe_status s);

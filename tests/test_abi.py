@@ -73,6 +73,22 @@ def test_host_side_validation_needs_no_gpu(lib):
     assert moe.moe_last_launch_count() == 0
 
 
+def test_static_entry_point_host_checks(lib):
+    # the allocation-free entry point validates on the host like the others,
+    # and an empty call is a no-op that needs no device
+    w = _weights()
+    assert moe.moe_layer_forward_static(w, 0x2000, 0, 0x3000, None) == moe.MOE_OK
+    assert moe.moe_last_launch_count() == 0
+    assert moe.moe_layer_forward_static(w, None, 0, None, None) == moe.MOE_OK
+    assert moe.moe_layer_forward_static(w, None, 4, 0x3000, None) == moe.MOE_ERR_ARG
+    assert moe.moe_layer_forward_static(w, 0x2000, 4, None, None) == moe.MOE_ERR_ARG
+    assert moe.moe_layer_forward_static(w, 0x2000, 4, 0x2000, None) == moe.MOE_ERR_ARG  # y aliases x
+    assert moe.moe_layer_forward_static(w, 0x2000, -1, 0x3000, None) == moe.MOE_ERR_ARG
+    assert moe.moe_layer_forward_static(_weights(D=100), 0x2000, 4, 0x3000, None) == moe.MOE_ERR_SHAPE
+    assert moe.moe_layer_forward_static(_weights(ptr=0), 0x2000, 0, 0x3000, None) == moe.MOE_ERR_ARG
+    assert lib.moe_layer_forward_static(None, 0x2000, 4, 0x3000, None) == moe.MOE_ERR_ARG
+
+
 def test_workspace_view_layout(lib):
     w = _weights(D=256, E=16, k=2, I=128)
     T = 37

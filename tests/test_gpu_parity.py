@@ -2,6 +2,7 @@
 edge cases. Routing tables and logits must be bit-exact; the layer output must
 be within the tolerance of gpu_util.check_output."""
 import ctypes
+import functools
 
 import numpy as np
 import pytest
@@ -84,6 +85,15 @@ def test_debug_dequant_golden_vectors():
 
 # --- routing: bit-exact --------------------------------------------------------------------
 
+def check_logits(got, want):
+    """Logits bit for bit; a NaN only has to be a NaN on both sides (the
+    payload bits of a NaN that an fma propagates differ between the CPU and
+    the GPU, and the rank of a NaN does not depend on them)."""
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan), "NaN logits differ"
+    assert np.array_equal(got.view(np.uint32)[~nan], want.view(np.uint32)[~nan]), "router logits differ in bits"
+
+
 def check_routing(layer, x_bits, name):
     dl = dev_layer(name, layer)
     x = x_to_device(x_bits)
@@ -96,8 +106,7 @@ def check_routing(layer, x_bits, name):
     tb = O.route_tables(idx, layer.E, v.block_m)
     g = lambda p, shape, dt: moe.ws_tensor(ws, p, shape, dt).cpu().numpy()
     A = T * layer.k
-    assert np.array_equal(g(v.logits, (T, layer.E), torch.float32).view(np.uint32), logits.view(np.uint32)), \
-        "router logits differ in bits"
+    check_logits(g(v.logits, (T, layer.E), torch.float32), logits)
     assert np.array_equal(g(v.topk_idx, (T, layer.k), torch.int32), idx)
     assert np.abs(g(v.topk_w, (T, layer.k), torch.float32) - w).max() <= WEIGHT_ATOL
     assert np.array_equal(g(v.count, (layer.E,), torch.int32), tb["count"])
@@ -132,6 +141,69 @@ def test_routing_ties_go_to_lower_index():
     layer.router_w[15] = layer.router_w[2]
     x = synth.make_x(32, 96, 256)
     check_routing(layer, x, "ties")
+
+
+def _special_logit_layer(k):
+    """A 16-expert layer whose router yields every kind of logit the ordering
+    rule covers: expert 2 NaN (one NaN weight), 7 -inf (bias), 5 and 11 +0
+    (zero rows); expert 9's row is -2^-140 everywhere, so a token whose x is
+    2^-12 everywhere gets the logit -0 from it (each product rounds to -0),
+    and a token whose x is -2^-12 gets +0. The other rows carry a bias of -3,
+    so the zero-valued logits lead the top-k."""
+    layer = synth.make_layer(36, 256, 16, k, 128)
+    layer.router_w[2, 7] = np.nan
+    layer.router_w[5, :] = 0.0
+    layer.router_w[11, :] = 0.0
+    layer.router_w[9, :] = -np.float32(2.0 ** -140)
+    bias = np.full(16, -3.0, np.float32)
+    bias[[5, 9, 11]] = -0.0  # -0 + -0 keeps the sign; +0 + -0 is +0
+    bias[7] = -np.inf
+    layer.router_bias = bias
+    return layer
+
+
+def _special_logit_tokens(T):
+    x = synth.make_x(36, T, 256)
+    x[0] = synth.f32_to_bf16_bits(np.full(256, 2.0 ** -12, np.float32))
+    x[1] = synth.f32_to_bf16_bits(np.full(256, -(2.0 ** -12), np.float32))
+    return x
+
+
+@pytest.mark.parametrize("T", [3, 70])
+@pytest.mark.parametrize("k", [6, 16])
+def test_routing_non_finite_and_signed_zero_logits(k, T):
+    # NaN ranks as -inf, -0 equals +0, and equal values go to the lower
+    # expert index, on the small-T and the larger-T routing kernels; with
+    # k = E every expert is kept, so NaN and -inf take the last two slots in
+    # index order with weight 0.
+    layer = _special_logit_layer(k)
+    x = _special_logit_tokens(T)
+    logits, idx, _ = O.route(O.OracleLayer(layer), x)
+    assert np.signbit(logits[0, 9]) and logits[0, 9] == 0 and not np.signbit(logits[1, 9])
+    assert np.isnan(logits[:, 2]).all() and np.isneginf(logits[:, 7]).all()
+    assert list(idx[0, :3]) == [5, 9, 11]
+    if k == 16:
+        assert list(idx[0, -2:]) == [2, 7]
+    check_routing(layer, x, f"special{k}_{T}")
+
+
+@pytest.mark.parametrize("path", [moe.PATH_GEMV, moe.PATH_GEMM], ids=["gemv", "gemm"])
+@pytest.mark.parametrize("T", [1, 3])
+def test_layer_with_non_finite_and_signed_zero_logits(path, T):
+    # every expert kept (k = E): the NaN and -inf experts carry weight 0, so
+    # the layer output stays finite and matches the oracle
+    layer = _special_logit_layer(16)
+    x = _special_logit_tokens(max(T, 2))[:T]
+    dl = moe.DeviceLayer(layer)
+    y, ws = run_forward(dl, x, path)
+    assert np.isfinite(y).all()
+    ol = O.OracleLayer(layer)
+    check_output(y, O.forward(ol, x), f"special logits T={T}")
+    # the top-k the forward itself wrote into its workspace
+    _, idx, w = O.route(ol, x)
+    v = dl.view(T, ws)
+    assert np.array_equal(moe.ws_tensor(ws, v.topk_idx, (T, 16), torch.int32).cpu().numpy(), idx)
+    assert np.abs(moe.ws_tensor(ws, v.topk_w, (T, 16), torch.float32).cpu().numpy() - w).max() <= WEIGHT_ATOL
 
 
 @pytest.mark.parametrize("T", [3, 16, 70])
@@ -306,14 +378,35 @@ def _sample_tokens(idx, count, T):
     return np.array(sorted(set(int(t) for t in pick)), dtype=np.int32)
 
 
-@pytest.mark.parametrize("impl", [moe.GEMM_TENSOR_CORE, moe.GEMM_CUDA_CORE], ids=["tc", "simt"])
-def test_layer_prefill4096_zipf_sampled(impl):
+@functools.lru_cache(maxsize=1)
+def _prefill4096_reference():
+    """The oracle's output for all 4096 tokens of the Zipf-routed prefill
+    workload (about 20 s on 16 host cores), shared by the tests below."""
     layer, x = config("prefill4096_zipf")
-    y, _ = run_forward(dev_layer("prefill4096_zipf", layer), x, moe.PATH_GEMM, impl)
+    return O.forward(O.OracleLayer(layer), x)
+
+
+def test_layer_prefill4096_zipf_all_tokens():
+    # the headline configuration in the launch configuration the benchmark
+    # times (tensor-core path, 192-token blocks): every token of the output,
+    # element by element, against the oracle
+    layer, x = config("prefill4096_zipf")
+    y, _ = run_forward(dev_layer("prefill4096_zipf", layer), x, moe.PATH_GEMM, moe.GEMM_TENSOR_CORE)
+    assert np.isfinite(y).all()
+    ref = _prefill4096_reference()
+    check_output(y, ref, "prefill4096, all tokens")
+    # and per token block of 256, so that one bad tile cannot hide in the mean
+    for t0 in range(0, x.shape[0], 256):
+        check_output(y[t0:t0 + 256], ref[t0:t0 + 256], f"prefill4096 tokens {t0}..{t0 + 255}")
+
+
+def test_layer_prefill4096_zipf_sampled_cuda_core():
+    layer, x = config("prefill4096_zipf")
+    y, _ = run_forward(dev_layer("prefill4096_zipf", layer), x, moe.PATH_GEMM, moe.GEMM_CUDA_CORE)
     ol = O.OracleLayer(layer)
     _, idx, _ = O.route(ol, x)
     toks = _sample_tokens(idx, np.bincount(idx.reshape(-1), minlength=layer.E), x.shape[0])
-    check_output(y[toks], O.forward(ol, x, tokens=toks), "prefill4096 sampled")
+    check_output(y[toks], _prefill4096_reference()[toks], "prefill4096 sampled, CUDA cores")
     assert np.isfinite(y).all()
 
 
@@ -502,6 +595,32 @@ def test_host_entry_chunked_passes_and_unaligned_y():
         moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, old)
     y_host = synth.bf16_bits_to_f32(yh.numpy().view(np.uint16).reshape(T, layer.D)).astype(np.float64)
     assert np.allclose(y_host, y_dev, rtol=2 ** -7, atol=1e-6)
+
+
+def test_device_status_survives_later_passes():
+    # 515 tokens in passes of 256, 256 and 3: the test hook makes the
+    # grouped-GEMM passes record MOE_ERR_DEVICE_TIMEOUT, the 3-token GEMV pass
+    # runs no such wait; its first kernel must not clear the call's status
+    layer, x = config("prefill512")
+    x = np.concatenate([x, x[:3]])
+    dl = dev_layer("prefill512", layer)
+    xd = x_to_device(x)
+    ws = dl.workspace(x.shape[0])
+    old = moe.moe_get_option(moe.MOE_OPT_CHUNK_TOKENS)
+    try:
+        assert moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, 256) == moe.MOE_OK
+        assert moe.moe_set_option(moe.MOE_OPT_FORCE_PATH, moe.PATH_AUTO) == moe.MOE_OK
+        assert moe.moe_set_option(moe.MOE_OPT_TEST_WAIT_CYCLES, 20000) == moe.MOE_OK
+        ws = dl.workspace(x.shape[0])
+        dl.forward(xd, workspace=ws)
+        assert moe.moe_set_option(moe.MOE_OPT_TEST_WAIT_CYCLES, 0) == moe.MOE_OK
+        st = moe.moe_get_device_status(ctypes.c_void_p(ws.data_ptr()), None)
+        assert st == moe.MOE_ERR_DEVICE_TIMEOUT, moe.moe_status_string(st)
+        y, _ = run_forward(dl, x)  # a fresh call starts its status afresh
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_TEST_WAIT_CYCLES, 0)
+        moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, old)
+    check_output(y, O.forward(O.OracleLayer(layer), x), "after a timeout in an earlier pass")
 
 
 def test_gemv_path_is_deterministic():

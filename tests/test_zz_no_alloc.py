@@ -1,8 +1,8 @@
 """The allocation-free entry point, moe_layer_forward_static().
 
-It serves callers that cannot allocate device memory: code running while a
-CUDA graph is captured, loops that forbid cudaMalloc after start-up, and hosts
-that give plug-ins only their input and output buffers. It must give the same
+It serves callers that cannot allocate device memory: loops that forbid
+cudaMalloc after start-up, and hosts that give plug-ins only their input and
+output buffers. It must give the same
 layer output as the regular entry point (within the tests' tolerance), also
 on a second call in a row (the shared scratch keeps the previous call's
 contents), and for token counts whose scratch would not fit in one pass.
@@ -66,9 +66,52 @@ def test_static_scratch_runs_large_token_counts_in_passes():
     ref = bf16_to_np(dl.forward(x))
     torch.cuda.synchronize()
     y = bf16_to_np(_static_forward(dl, x))
+    static_launches = moe.moe_last_launch_count()
     torch.cuda.synchronize()
     check_output(y, ref, "static scratch, 1000 tokens in passes")
     assert np.isfinite(y).all()
+    assert moe.moe_get_device_status_static(None) == moe.MOE_OK
+    # the launch count covers every pass: the same passes through the
+    # workspace entry point (chunks of 451 tokens) launch as many kernels
+    old = moe.moe_get_option(moe.MOE_OPT_CHUNK_TOKENS)
+    try:
+        assert moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, 451) == moe.MOE_OK
+        dl.forward(x)
+        assert moe.moe_last_launch_count() == static_launches
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, old)
+    torch.cuda.synchronize()
+
+
+def test_static_status_keeps_an_earlier_pass_error():
+    # 453 tokens run as a 451-token grouped-GEMM pass and a 2-token GEMV
+    # pass. The test hook makes the tensor-core epilogue of the first pass
+    # give up a bounded wait (MOE_ERR_DEVICE_TIMEOUT); the second pass has no
+    # such wait, and must not wipe the first pass's error. The next call
+    # starts afresh and is correct.
+    layer, x_bits = synth.make_config("prefill512", 453)
+    dl = moe.DeviceLayer(layer)
+    x = x_to_device(x_bits)
+    assert moe.moe_set_option(moe.MOE_OPT_TEST_WAIT_CYCLES, 20000) == moe.MOE_OK
+    try:
+        _static_forward(dl, x)
+        st = moe.moe_get_device_status_static(None)
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_TEST_WAIT_CYCLES, 0)
+    assert st == moe.MOE_ERR_DEVICE_TIMEOUT, moe.moe_status_string(st)
+    assert moe.moe_get_device_status_static(None) == moe.MOE_OK  # read and cleared
+    ref = bf16_to_np(dl.forward(x))
+    y = bf16_to_np(_static_forward(dl, x))
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status_static(None) == moe.MOE_OK
+    check_output(y, ref, "static scratch after a recorded timeout")
+
+
+def test_static_empty_call_is_a_noop():
+    layer, x_bits = synth.make_config("tiny", 4)
+    dl = moe.DeviceLayer(layer)
+    assert moe.moe_layer_forward_static(dl.w, None, 0, None, None) == moe.MOE_OK
+    assert moe.moe_last_launch_count() == 0
 
 
 def moe_static_bytes():
