@@ -235,6 +235,163 @@ def layer_work(layer, idx_np) -> dict:
         router_flops=2.0 * T * E * D)
 
 
+def touched_weight_bytes(layer, idx_np) -> int:
+    """Packed bytes of the distinct experts a batch's top-k selects, plus the shared expert."""
+    import numpy as np
+    return (len(np.unique(idx_np)) + 1) * expert_bytes(layer.D, layer.I)
+
+
+def capture_graph(torch, device, stream, fn):
+    """A CUDA graph of fn() (which launches on torch's current stream); one
+    eager run on a side stream first, outside the capture."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        fn()
+    stream.wait_stream(side)
+    torch.cuda.synchronize(device)
+    with torch.cuda.graph(g, stream=side):
+        fn()
+    torch.cuda.synchronize(device)
+    return g
+
+
+def sample_us(torch, stream, flush, fn) -> float:
+    """Device µs of one fn() on `stream` between CUDA events, with L2 flushed
+    before it and a GPU-side lead so the host has enqueued fn() in time."""
+    flush.zero_()
+    torch.cuda._sleep(HOST_LEAD_CYCLES)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    fn()
+    b.record(stream)
+    b.synchronize()
+    return 1e3 * a.elapsed_time(b)
+
+
+def med(v):
+    v = sorted(v)
+    return v[len(v) // 2]
+
+
+def p95(v):
+    v = sorted(v)
+    return v[int(0.95 * (len(v) - 1))]
+
+
+def run_workloads(args, moe, synth, torch, device, stream, peaks, headline: dict, decode: dict | None) -> dict:
+    """The five seeded workloads side by side: µs, tokens/s and roofline
+    fraction of each (C1, the tiny case, is a correctness case only), and the
+    small-row sweep run on both the GEMV and the grouped-GEMM path to fix the
+    row count where the GEMM takes over."""
+    import ctypes
+
+    import numpy as np
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    out = {"prefill4096_zipf": headline}
+    if decode is not None:
+        out["decode"] = dict(T=1, us=decode["us_per_token"], tokens_per_s=decode["tokens_per_s"],
+                             bound="hbm", weight_bytes=decode["roofline"]["bytes_per_launch"],
+                             frac_hbm=decode["layer_GBps_on_expert_bytes"] / peaks["hbm_gbs"],
+                             timing="graph replay, median")
+
+    def layer_forward(dl, x, y, ws, T):
+        def fwd():
+            sp = ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+            st = moe.moe_layer_forward(dl.w, x.data_ptr(), T, y.data_ptr(), ws.data_ptr(), ws.numel(), sp)
+            if st != moe.MOE_OK:
+                raise moe.MoEError(st, "moe_layer_forward")
+        return fwd
+
+    def status_ok(ws):
+        st = moe.moe_get_device_status(ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+        if st != moe.MOE_OK:
+            raise moe.MoEError(st, "device status")
+
+    # C3: T=512, near-uniform routing (HBM-bound: ~all experts touched)
+    layer, x_np = synth.make_config("prefill512")
+    dl = moe.DeviceLayer(layer, device=device)
+    T = x_np.shape[0]
+    x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).to(device)
+    y = torch.empty_like(x)
+    ws = dl.workspace(T)
+    fwd = layer_forward(dl, x, y, ws, T)
+    for _ in range(3):
+        fwd()
+    g = capture_graph(torch, device, stream, fwd)
+    n = max(args.steps, 50)
+    us = [sample_us(torch, stream, flush, g.replay) for _ in range(n)]
+    status_ok(ws)
+    v = dl.view(T, ws)
+    idx = moe.ws_tensor(ws, v.topk_idx, (T, layer.k), torch.int32).cpu().numpy()
+    work = layer_work(layer, idx)
+    t = med(us)
+    out["prefill512"] = dict(
+        T=T, us=t, us_p95=p95(us), tokens_per_s=T / (t / 1e6), bound="hbm", weight_bytes=work["weight_bytes"],
+        experts_touched=work["experts_touched"], frac_hbm=work["weight_bytes"] / (t / 1e6) / 1e9 / peaks["hbm_gbs"],
+        flops=work["gateup_flops"] + work["down_flops"],
+        frac_tensor=(work["gateup_flops"] + work["down_flops"]) / (t / 1e6) / 1e12 / peaks["bf16_tflops"],
+        samples=n, timing="graph replay, median; L2 flushed before each sample")
+    del dl, x, y, ws, g
+
+    # C5: T in {2,3,4,5,8} on both paths, forced; graph-replayed, L2 flushed,
+    # blocks of samples alternating between the paths
+    layer, x_all = synth.make_config("sweep")
+    dl = moe.DeviceLayer(layer, device=device)
+    block = 20
+    n_blocks = 2 * max(5, (args.sweep_samples + block - 1) // block)  # half of the blocks per path
+    sweep = {}
+    old_force = moe.moe_get_option(moe.MOE_OPT_FORCE_PATH)
+    try:
+        for T in synth.SWEEP_T:
+            x = torch.from_numpy(np.ascontiguousarray(x_all[:T]).view(np.int16)).view(torch.bfloat16).to(device)
+            graphs, wss, ys = {}, {}, {}
+            for name, path in (("gemv", moe.PATH_GEMV), ("gemm", moe.PATH_GEMM)):
+                moe.moe_set_option(moe.MOE_OPT_FORCE_PATH, path)
+                ys[name], wss[name] = torch.empty_like(x), dl.workspace(T)
+                f = layer_forward(dl, x, ys[name], wss[name], T)
+                for _ in range(3):
+                    f()
+                graphs[name] = capture_graph(torch, device, stream, f)
+            moe.moe_set_option(moe.MOE_OPT_FORCE_PATH, old_force)
+            times = {"gemv": [], "gemm": []}
+            for b in range(n_blocks):
+                for name in (("gemv", "gemm") if b % 2 == 0 else ("gemm", "gemv")):
+                    for _ in range(block):
+                        times[name].append(sample_us(torch, stream, flush, graphs[name].replay))
+            for name in wss:
+                status_ok(wss[name])
+            v = dl.view(T, wss["gemv"])
+            idx = moe.ws_tensor(wss["gemv"], v.topk_idx, (T, layer.k), torch.int32).cpu().numpy()
+            wb = touched_weight_bytes(layer, idx)
+            row = dict(weight_bytes=wb, experts_touched=len(np.unique(idx)) + 1, samples=len(times["gemv"]))
+            for name in ("gemv", "gemm"):
+                t = med(times[name])
+                row[f"{name}_us"] = t
+                row[f"{name}_p95_us"] = p95(times[name])
+                row[f"{name}_frac_hbm"] = wb / (t / 1e6) / 1e9 / peaks["hbm_gbs"]
+            row["faster"] = "gemv" if row["gemv_us"] < row["gemm_us"] else "gemm"
+            sweep[str(T)] = row
+            del graphs, wss, ys, x
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_FORCE_PATH, old_force)
+    out["sweep"] = sweep
+    # the switch point: the largest swept row count up to which the GEMV path
+    # is faster at every swept count (1 if the GEMM wins already at 2 rows)
+    thr = 1
+    for T in synth.SWEEP_T:
+        if sweep[str(T)]["faster"] != "gemv":
+            break
+        thr = T
+    out["crossover"] = dict(measured_gemv_max_rows=thr,
+                            library_default=moe.moe_get_option(moe.MOE_OPT_GEMV_MAX_ROWS),
+                            rule="largest swept T with the GEMV path faster at every swept T up to it",
+                            timing=f"graph replay, median of {block * n_blocks // 2} samples per point, "
+                                   f"L2 flushed, blocks of {block} alternating between the paths")
+    return out
+
+
 # --- our arm ---------------------------------------------------------------------------------
 
 def run_ours(args) -> dict:
@@ -354,6 +511,15 @@ def run_ours(args) -> dict:
                h2d_bytes_per_step=T * layer.D * 2, d2h_bytes_per_step=T * layer.D * 2, ms_per_step=e2e_ms_v)
 
     decode = run_decode(args, moe, synth, torch, device, stream, peaks) if not args.no_decode else None
+    headline = dict(T=T, us=ms * 1e3, tokens_per_s=T / (ms / 1e3), bound="tensor",
+                    flops=work["gateup_flops"] + work["down_flops"], frac_tensor=whole / peaks["bf16_tflops"],
+                    weight_bytes=work["weight_bytes"],
+                    frac_hbm=work["weight_bytes"] / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                    experts_touched=work["experts_touched"], samples=args.steps,
+                    timing="stream-launched, mean of the timed steps; L2 flushed before each")
+    workloads = None
+    if not args.no_workloads and rank == 0 and world == 1:
+        workloads = run_workloads(args, moe, synth, torch, device, stream, peaks, headline, decode)
 
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -378,6 +544,7 @@ def run_ours(args) -> dict:
         "wall_s_timed": t_wall,
         "clocks": clk.summary(),
         "decode": decode,
+        "workloads": workloads,
         "peaks": peaks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -451,8 +618,8 @@ def run_decode(args, moe, synth, torch, device, stream, peaks) -> dict:
     med = lambda m: m[len(m) // 2]
     us, us_g = 1e3 * med(ms), 1e3 * med(ms_g)
     kern = {nm: dict(ms_per_launch=t / c, launches=c) for nm, (t, c) in kt.items()}
-    # the fused one-token kernel when it ran, else the two GEMV kernels
-    names = ("decode_fused",) if "decode_fused" in kern else ("gemv_gateup", "gemv_down")
+    # the one-launch small-row kernel when it ran, else the two GEMV kernels
+    names = ("decode_rows",) if "decode_rows" in kern else ("gemv_gateup", "gemv_down")
     gemv_ms = sum(kern[nm]["ms_per_launch"] for nm in names if nm in kern)
     ach = work["weight_bytes"] / (gemv_ms / 1e3) / 1e9 if gemv_ms else None
     return {"us_per_token": us_g, "us_per_token_stream": us, "us_p95_stream": 1e3 * ms[int(0.95 * (n - 1))],
@@ -669,6 +836,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the 512-token layer and the small-row GEMV/GEMM sweep")
+    ap.add_argument("--sweep-samples", type=int, default=200, help="samples per (row count, path) of the sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ablations", action="store_true",

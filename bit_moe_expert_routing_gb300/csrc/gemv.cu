@@ -23,22 +23,14 @@
 // at once (bulk copies do not hold registers), and the grids fill the GPU in
 // about one wave.
 //
-// Per group of 64 weights w = s*q + b, so a dot product over a 32-code chunk
-// of one group is s * sum(x*q) + b * sum(x). The codes enter the sum as fp32
-// values 128 + q built by bit operations (OR the code into the mantissa of
-// 128.0f), and 128 * sum(x) is removed per chunk. The per-chunk sums of x are
-// computed once per token and shared by every row.
-//
-// Activations live in shared memory chunk-major: for a row of K values with
-// nch = K/32 chunks, float4 number (jq * nch + c) holds values 32c+4jq..32c+4jq+3.
-// Lane l works on chunk c = l + 32m, so the lanes of a warp read consecutive
-// float4s and consecutive 16-byte code chunks (no bank conflicts).
+// The dequantising dot products are in dot.cuh.
 #include <algorithm>
 #include <cstddef>
 #include <mutex>
 #include <vector>
 
 #include "common.cuh"
+#include "dot.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "topk.cuh"
@@ -50,35 +42,6 @@ constexpr int kMaxGemvRows = 8;
 constexpr int kGemvWarps = 8;
 constexpr int kGateupRows = 16;  // intermediate rows per gate/up CTA
 constexpr int kDownCols = 8;     // output columns per down CTA
-
-// fp32 value 128 + q of the nibble in bits 16..19 of w_shifted.
-__device__ __forceinline__ float q128(uint32_t w_shifted) {
-  return __uint_as_float((w_shifted & 0x000F0000u) | 0x43000000u);
-}
-
-// acc += sum_j x[j] * (128 + q_j) over the 8 codes of word w; xa holds
-// activations 0..3 of the word, xb 4..7. Even and odd terms go to .x and .y.
-__device__ __forceinline__ float2 dot8_128(uint32_t w, float4 xa, float4 xb, float2 acc) {
-  const uint32_t sw = __byte_perm(w, 0, 0x1032);  // codes 0..3 into bits 16..31
-  acc = __ffma2_rn(make_float2(xa.x, xa.y), make_float2(q128(sw), q128(sw >> 4)), acc);
-  acc = __ffma2_rn(make_float2(xa.z, xa.w), make_float2(q128(sw >> 8), q128(sw >> 12)), acc);
-  acc = __ffma2_rn(make_float2(xb.x, xb.y), make_float2(q128(w), q128(w >> 4)), acc);
-  acc = __ffma2_rn(make_float2(xb.z, xb.w), make_float2(q128(w >> 8), q128(w >> 12)), acc);
-  return acc;
-}
-
-// s * sum(x*q) + b * sum(x) over one 32-code chunk of a row: w4 holds its
-// codes, xv its 32 activations (chunk-major float4s), xsum their sum, s and b
-// the bf16 scale and bias of its group.
-__device__ __forceinline__ float chunk_dot_r(const uint4 w4, const float4 (&xv)[8], float xsum, uint16_t s,
-                                             uint16_t b) {
-  float2 d0 = make_float2(0.f, 0.f), d1 = d0;
-  d0 = dot8_128(w4.x, xv[0], xv[1], d0);
-  d1 = dot8_128(w4.y, xv[2], xv[3], d1);
-  d0 = dot8_128(w4.z, xv[4], xv[5], d0);
-  d1 = dot8_128(w4.w, xv[6], xv[7], d1);
-  return bf16_to_f32(s) * ((d0.x + d0.y) + (d1.x + d1.y) - 128.f * xsum) + bf16_to_f32(b) * xsum;
-}
 
 struct GemvArgs {
   const uint16_t* x;
@@ -94,29 +57,6 @@ struct GemvArgs {
   WsHeader* hdr;
   int T, D, E, k, I;
 };
-
-// Stages 8 bf16 values (number q8 of a row) into a chunk-major fp32 row.
-__device__ __forceinline__ void stage_bf16x8(float4* rowdst, int nch, int q8, uint4 v) {
-  const int c = q8 >> 2, jq = (q8 & 3) * 2;
-  rowdst[jq * nch + c] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
-  rowdst[(jq + 1) * nch + c] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
-}
-
-// Per-chunk sums of `rows` staged rows (thread per (row, chunk)).
-__device__ __forceinline__ void chunk_sums(const float4* xs4, float* xsum, int rows, int nch) {
-  for (int q = threadIdx.x; q < rows * nch; q += blockDim.x) {
-    const int r = q / nch, c = q % nch;
-    const float4* xr = xs4 + size_t(r) * 8 * nch;
-    float s = 0.f;
-#pragma unroll
-    for (int jq = 0; jq < 8; ++jq) {
-      const float4 v = xr[jq * nch + c];
-      s += (v.x + v.y) + (v.z + v.w);
-    }
-    xsum[q] = s;
-  }
-}
-
 
 // Shared-memory layout of a gate/up CTA (D input columns, R token rows).
 struct GateupSmem {
@@ -417,17 +357,18 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned target, vol
     atomicAdd(&hdr->counter, 1u);
     const long long t0 = clock64();
     int ok = 1;
-    while (true) {
+    while (true) {  // relaxed polls with a short sleep, then one acquire fence
       unsigned v;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(&hdr->counter) : "memory");
+      asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(&hdr->counter) : "memory");
       if (v >= target) break;
       if (clock64() - t0 > kWaitLimit) {
         report(hdr, MOE_ERR_DEVICE_TIMEOUT, 110);
         ok = 0;
         break;
       }
-      __nanosleep(64);
+      __nanosleep(32);
     }
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
     *result = ok;
   }
   __syncthreads();
@@ -707,6 +648,35 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
 #pragma unroll
     for (int w = 0; w < kFdWarps; ++w) yv += red[w * kFdCols + threadIdx.x];
     a.y[d0 + threadIdx.x] = f32_to_bf16(yv);
+  }
+  // CTA 0: the routing tables for inspection (one token: each selected
+  // expert holds one row; the permutation orders the slots by expert)
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int cnt = 0, below = 0;
+      for (int j = 0; j < k; ++j) {
+        cnt += (s_exp[j] == e);
+        below += (s_exp[j] < e);
+      }
+      a.count[e] = cnt;
+      a.off[e] = below;
+    }
+    for (int j = threadIdx.x; j < k; j += blockDim.x) {
+      int rank = 0;
+      for (int j2 = 0; j2 < k; ++j2) rank += (s_exp[j2] < s_exp[j]);
+      a.perm[rank] = j;
+      a.inv[j] = rank;
+      a.blocks[3 * rank + 0] = s_exp[j];
+      a.blocks[3 * rank + 1] = rank;
+      a.blocks[3 * rank + 2] = 1;
+    }
+    if (threadIdx.x == 0) {
+      a.off[E] = k;
+      a.blocks[3 * k + 0] = E;  // the shared expert's row
+      a.blocks[3 * k + 1] = k;
+      a.blocks[3 * k + 2] = 1;
+      *a.n_blocks = k + 1;
+    }
   }
 }
 

@@ -24,7 +24,7 @@ constexpr int kMinBlockM = 16;      // smallest block size MOE_OPT_BLOCK_M accep
 // once when the call starts, so that another thread's moe_set_option cannot
 // change a call part-way.
 struct Options {
-  int gemv_max_rows = 4;
+  int gemv_max_rows = 8;  // the measured small-row sweep: the GEMV path is faster at every row count it takes
   int force_path = 0;
   int kernel_timing = 0;
   int gemm_impl = 0;
@@ -115,10 +115,14 @@ bool tmap_encoder_available();
 // Decode GEMV path (a few rows).
 cudaError_t gemv(const Ctx& c);
 bool gemv_supported(const Ctx& c);
-// One token: router logits, top-k, gate/up and down in one cooperative kernel
-// (with the header zeroed on the stream first).
+// One token: router logits, top-k, gate/up and down in one cooperative
+// kernel (with the header counter zeroed on the stream first).
 cudaError_t decode_fused(const Ctx& c);
 bool decode_fused_supported(const Ctx& c);
+// Two to eight rows: the same steps in one cooperative kernel that streams
+// the union of the rows' experts through shared-memory rings.
+cudaError_t decode_rows(const Ctx& c);
+bool decode_rows_supported(const Ctx& c);
 // Router logits only, for up to 16 tokens.
 cudaError_t route_logits_small(const Ctx& c);
 

@@ -176,7 +176,7 @@ void fill_view(const Ctx& c, moe_route_view* v) {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-enum class Path { DecodeFused, Gemv, GemmWt, GemmTc, GemmSimt };
+enum class Path { DecodeFused, DecodeRows, Gemv, GemmWt, GemmTc, GemmSimt };
 
 // Chooses the expert path for this call and the block-map row count it
 // consumes: 192 tokens per block for the tensor-core GEMM with weights in
@@ -186,8 +186,12 @@ Path plan(Ctx& c) {
   int path = o.force_path;
   if (path == 0) path = (c.T <= o.gemv_max_rows) ? 1 : 2;
   Path p;
-  if (path == 1 && gemv_supported(c))
-    p = (o.decode_fused && decode_fused_supported(c)) ? Path::DecodeFused : Path::Gemv;
+  if (path == 1 && o.decode_fused && c.T == 1 && decode_fused_supported(c))
+    p = Path::DecodeFused;
+  else if (path == 1 && o.decode_fused && c.T > 1 && decode_rows_supported(c))
+    p = Path::DecodeRows;
+  else if (path == 1 && gemv_supported(c))
+    p = Path::Gemv;
   else if (o.gemm_impl == 0 && gemm_wt_supported(c))
     p = Path::GemmWt;
   else if (o.gemm_impl == 2 && gemm_tc_supported(c))
@@ -293,9 +297,9 @@ static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, u
   const Path path = plan(c);
   if (path == Path::GemmWt) c.xperm = c.xperm_area;  // the router writes the paired-order x it gathers
   timing_begin(c);
-  if (path == Path::DecodeFused) {  // routing included
+  if (path == Path::DecodeFused || path == Path::DecodeRows) {  // routing included
     if (wait_x(c) != cudaSuccess) return MOE_ERR_CUDA;
-    return cuda_status(decode_fused(c));
+    return cuda_status(path == Path::DecodeFused ? decode_fused(c) : decode_rows(c));
   }
   cudaError_t err = route(c, path == Path::Gemv ? nullptr : &c.yacc_zeroed);
   if (err != cudaSuccess) return MOE_ERR_CUDA;

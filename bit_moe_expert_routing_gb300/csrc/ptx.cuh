@@ -43,9 +43,9 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for the phase of `parity` to complete. Gives up when the CTA's
 // abort flag is set (unless draining) or after `limit` cycles (then sets the
-// flag and records MOE_ERR_DEVICE_TIMEOUT).
+// flag and records MOE_ERR_DEVICE_TIMEOUT with `site` as its detail).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr,
-                                          long long limit = kWaitLimit, bool draining = false) {
+                                          long long limit = kWaitLimit, bool draining = false, int site = 100) {
   if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
@@ -53,7 +53,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (!draining && *abort_flag) return false;
     if (clock64() - t0 > limit) {
       *abort_flag = 1;
-      report(hdr, MOE_ERR_DEVICE_TIMEOUT, 100);
+      report(hdr, MOE_ERR_DEVICE_TIMEOUT, site);
       return false;
     }
   }

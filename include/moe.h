@@ -118,7 +118,10 @@ typedef struct {
 
 /* Options (process-wide). */
 typedef enum {
-  MOE_OPT_GEMV_MAX_ROWS = 1, /* T <= this runs the decode GEMV path (default 4) */
+  MOE_OPT_GEMV_MAX_ROWS = 1, /* T <= this runs the decode GEMV path (default 8, its
+                                maximum: on the D=2048, E=256, k=8, I=512 layer the
+                                GEMV path measured faster than the grouped GEMM
+                                at every row count from 2 to 8) */
   MOE_OPT_FORCE_PATH = 2,    /* 0 auto by row count, 1 GEMV, 2 grouped GEMM */
   MOE_OPT_KERNEL_TIMING = 3, /* 1: record CUDA events around each kernel of
                                 the next forwards (read with moe_kernel_times) */
@@ -140,10 +143,11 @@ typedef enum {
                                 others; 16..192 in steps of 16 is clamped to
                                 the path's size. The workspace always has
                                 room for 16-row blocks. */
-  MOE_OPT_DECODE_FUSED = 7,  /* 1 (default): one token on the GEMV path runs the
-                                router logits, top-k, gate/up and down in one
-                                cooperative kernel (when the device can hold all
-                                its CTAs at once); 0: the separate routing and
+  MOE_OPT_DECODE_FUSED = 7,  /* 1 (default): a forward on the GEMV path (1 to 8
+                                rows) runs the router logits, top-k, gate/up and
+                                down in one cooperative kernel, when the device
+                                can hold all its CTAs at once and the shape fits
+                                its shared memory; 0: the separate routing and
                                 GEMV kernels */
   MOE_OPT_CHUNK_TOKENS = 8,  /* prompt chunking ("Optimizing on-device inference
                                 for Apple Silicon", "Bound temporary memory with

@@ -279,31 +279,44 @@ def test_layer_decode(path):
 
 
 @pytest.mark.parametrize("fused", [0, 1], ids=["separate", "fused"])
-def test_layer_decode_fused_and_separate(fused):
-    # one token on the GEMV path: the cooperative kernel (router, grid barrier,
-    # top-k, gate/up, grid barrier, down) and the separate routing + GEMV
-    # kernels, both against the oracle
-    layer, x = config("decode")
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_layer_decode_fused_and_separate(fused, T):
+    # a few rows on the GEMV path: the one-launch cooperative kernel (router,
+    # grid barrier, top-k, gate/up, grid barrier, down) and the separate
+    # routing + GEMV kernels, both against the oracle, with the routing tables
+    # each leaves in its workspace
+    layer, x = config("sweep") if T > 1 else config("decode")
+    x = x[:T]
+    name = "sweep" if T > 1 else "decode"
     assert moe.moe_set_option(moe.MOE_OPT_DECODE_FUSED, fused) == moe.MOE_OK
     try:
-        dl = dev_layer("decode", layer)
-        y, ws = run_forward(dl, x, moe.PATH_GEMV)
+        dl = dev_layer(name, layer)
+        ws = dl.workspace(T)
+        ws.fill_(0x5A)  # no table may come from an earlier call
+        assert moe.moe_set_option(moe.MOE_OPT_FORCE_PATH, moe.PATH_GEMV) == moe.MOE_OK
+        y = bf16_to_np(dl.forward(x_to_device(x), workspace=ws))
         launches = moe.moe_last_launch_count()
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_status(ctypes.c_void_p(ws.data_ptr()), None) == moe.MOE_OK
     finally:
         moe.moe_set_option(moe.MOE_OPT_DECODE_FUSED, 1)
     ol = O.OracleLayer(layer)
-    check_output(y, O.forward(ol, x), f"decode fused={fused}")
+    check_output(y, O.forward(ol, x), f"T={T} fused={fused}")
     assert launches == (1 if fused else 4)
-    # the routing tables in the workspace agree with the oracle either way
-    v = dl.view(1, ws)
+    v = dl.view(T, ws)
     g = lambda p_, shape, dt: moe.ws_tensor(ws, p_, shape, dt).cpu().numpy()
-    _, idx, w = O.route(ol, x)
+    logits, idx, w = O.route(ol, x)
     tb = O.route_tables(idx, layer.E, v.block_m)
-    assert np.array_equal(g(v.topk_idx, (1, layer.k), torch.int32), idx)
-    assert np.abs(g(v.topk_w, (1, layer.k), torch.float32) - w).max() <= WEIGHT_ATOL
-    assert np.array_equal(g(v.perm, (layer.k,), torch.int32), tb["perm"])
+    A = T * layer.k
+    check_logits(g(v.logits, (T, layer.E), torch.float32), logits)
+    assert np.array_equal(g(v.topk_idx, (T, layer.k), torch.int32), idx)
+    assert np.abs(g(v.topk_w, (T, layer.k), torch.float32) - w).max() <= WEIGHT_ATOL
     assert np.array_equal(g(v.count, (layer.E,), torch.int32), tb["count"])
+    assert np.array_equal(g(v.off, (layer.E + 1,), torch.int32), tb["off"])
+    assert np.array_equal(g(v.perm, (A,), torch.int32), tb["perm"])
+    assert np.array_equal(g(v.inv, (A,), torch.int32), tb["inv"])
     nb = int(g(v.n_blocks, (1,), torch.int32)[0])
+    assert nb == len(tb["blocks"])
     assert np.array_equal(g(v.blocks, (v.max_blocks, 3), torch.int32)[:nb], tb["blocks"])
 
 
