@@ -45,38 +45,58 @@ namespace moe {
 namespace {
 
 constexpr int WM = 128;               // weight rows per tile (MMA M, TMEM lanes)
-constexpr int kMaxN = kWtBlockRows;   // token rows per tile (MMA N <= 192)
 constexpr int WK = 64;                // one quantisation group
 constexpr int kGroupsPerStage = 2;    // a pipeline stage spans 128 of K
 constexpr int kBStages = 3;           // token operand ring (shared memory)
-constexpr int kAStages = 2;           // dequantised weight ring (tensor memory)
 constexpr int kCStages = 8;           // packed-code ring, one group per stage
-constexpr uint32_t kBHalf = kMaxN * WK * 2;             // 24 KB: one 128-byte-swizzled K block of 64
-constexpr uint32_t kBBytes = kBHalf * kGroupsPerStage;  // 48 KB
 constexpr uint32_t kCBytes = WM * WK / 2;               // 4 KB of codes
-constexpr uint32_t kAccCols = kMaxN;                    // fp32 columns of one accumulator
 constexpr uint32_t kAGroupCols = WK / 2;                // 32 columns: one group's 64 bf16 per lane
 constexpr uint32_t kAStageCols = kAGroupCols * kGroupsPerStage;
-constexpr uint32_t kAColBase = 2 * kAccCols;  // 384: after the two accumulators
 constexpr uint32_t kTmemCols = 512;
-static_assert(kAColBase + kAStages * kAStageCols <= kTmemCols, "tensor memory budget");
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpB0 = 2, kNumBWarps = 4, kWarpDq0 = 6, kNumDqWarps = 8,
-              kWarpEpi0 = 14, kNumEpiWarps = 8;
-constexpr int kNumWarps = 22;
-constexpr int kGatherPerThread = kMaxN * 8 / (kNumBWarps * 32);  // 16-byte chunks per thread per K block
-constexpr int kNumThreads = kNumWarps * 32;
-constexpr int kXposeStride = 36;               // floats per row of an epilogue transpose buffer (conflict-free float4 reads)
-constexpr int kEpiChunks = (kMaxN + 31) / 32;  // 16-token chunks per epilogue warp and tile
+constexpr int kXposeStride = 36;  // floats per row of an epilogue transpose buffer (conflict-free float4 reads)
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpB0 = 2, kNumBWarps = 4, kWarpDq0 = 6;
 
-constexpr uint32_t kOffB = 0;
-constexpr uint32_t kOffC = kOffB + kBStages * kBBytes;
-constexpr uint32_t kOffXpose = kOffC + kCStages * kCBytes;       // down epilogue: [warp][16][36] floats
-constexpr uint32_t kOffBar = kOffXpose + kNumEpiWarps * 16 * kXposeStride * 4;
-// bfull, bempty [kBStages]; afull, aempty [kAStages]; cfull, cempty [kCStages]; accf, acce [2]; drain; never
-constexpr uint32_t kNumBars = 2 * kBStages + 2 * kAStages + 2 * kCStages + 6;
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-constexpr size_t kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+// A launch shape of the kernel: the largest token block of a tile (MMA N),
+// the dequantising warp sets (one per A stage in tensor memory: set p fills
+// the stages t = p, p + SETS, ... and owns A stage p; four warps, one per
+// TMEM lane quarter, each) and the epilogue warps (EPIW / 4 per lane quarter).
+// Tensor memory holds two accumulators of MAXN columns and SETS A stages.
+template <int MAXN, int SETS, int EPIW>
+struct WtCfg {
+  static constexpr int kMaxN = MAXN;
+  static constexpr int kAStages = SETS;
+  static constexpr int kNumDqWarps = 4 * SETS;
+  static constexpr int kNumEpiWarps = EPIW;
+  static constexpr int kWarpEpi0 = kWarpDq0 + kNumDqWarps;
+  static constexpr int kNumWarps = kWarpEpi0 + kNumEpiWarps;
+  static constexpr int kNumThreads = kNumWarps * 32;
+  static constexpr uint32_t kBHalf = kMaxN * WK * 2;             // one 128-byte-swizzled K block of 64
+  static constexpr uint32_t kBBytes = kBHalf * kGroupsPerStage;
+  static constexpr uint32_t kAccCols = kMaxN;                    // fp32 columns of one accumulator
+  static constexpr uint32_t kAColBase = 2 * kAccCols;            // after the two accumulators
+  static constexpr int kGatherPerThread = kMaxN * 8 / (kNumBWarps * 32);  // 16-byte chunks per thread per K block
+  static constexpr int kEpiHalves = kNumEpiWarps / 4;            // epilogue warps per lane quarter
+  static constexpr int kEpiStep = 16 * kEpiHalves;               // columns between a warp's 16-column chunks
+  static constexpr int kEpiChunks = (kMaxN + kEpiStep - 1) / kEpiStep;
+  static constexpr uint32_t kOffB = 0;
+  static constexpr uint32_t kOffC = kOffB + kBStages * kBBytes;
+  static constexpr uint32_t kOffXpose = kOffC + kCStages * kCBytes;  // down epilogue: [warp][16][36] floats
+  static constexpr uint32_t kOffBar = kOffXpose + kNumEpiWarps * 16 * kXposeStride * 4;
+  // bfull, bempty [kBStages]; afull, aempty [kAStages]; cfull, cempty [kCStages]; accf, acce [2]; drain; never
+  static constexpr uint32_t kNumBars = 2 * kBStages + 2 * kAStages + 2 * kCStages + 6;
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr size_t kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
+  static_assert(kAColBase + kAStages * kAStageCols <= kTmemCols, "tensor memory budget");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static_assert(kMaxN % 16 == 0 && (kMaxN * 8) % (kNumBWarps * 32) == 0, "whole gather chunks");
+  static_assert(kCStages % (2 * SETS) == 0, "every code slot is read by one set");
+  static_assert(kNumEpiWarps % 4 == 0, "epilogue warps cover the four lane quarters");
+};
+// 192-token blocks with two weight stages in flight (the default), and
+// blocks of at most 64 tokens with four: small blocks leave tensor memory
+// for more A stages, and their tiles are bound by the dequantisation chain.
+using WtLarge = WtCfg<kWtBlockRows, 2, 8>;
+using WtSmall = WtCfg<kWtSmallBlockRows, 4, 4>;
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
   asm volatile(
@@ -122,7 +142,7 @@ __device__ __forceinline__ uint32_t idesc_n(int n) {
 // overwrites D when `accumulate` is 0. Executed by the whole warp so that every
 // operand is warp-uniform; one elected lane issues.
 __device__ __forceinline__ void umma_stage(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t idesc, uint32_t accumulate,
-                                           uint32_t bar_b, uint32_t bar_a) {
+                                           uint32_t bar_b, uint32_t bar_a, uint32_t b_half) {
   asm volatile(
       "{\n"
       " .reg .pred e, p, t;\n"
@@ -148,7 +168,7 @@ __device__ __forceinline__ void umma_stage(uint32_t d, uint32_t a, uint32_t b_lo
       " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n"
       " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n"
       "}" ::"r"(d),
-      "r"(a), "r"(b_lo), "r"(kSmemDescHi), "r"(idesc), "r"(accumulate), "r"(bar_b), "r"(bar_a), "r"(kBHalf >> 4)
+      "r"(a), "r"(b_lo), "r"(kSmemDescHi), "r"(idesc), "r"(accumulate), "r"(bar_b), "r"(bar_a), "r"(b_half >> 4)
       : "memory");
 }
 
@@ -216,8 +236,14 @@ struct WtMaps {
   CUtensorMap b;         // down only: h [T*k+T, I] (SW128, box 64 x kMaxN)
 };
 
-template <bool GATEUP>
-__global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs args, const __grid_constant__ WtMaps maps) {
+template <bool GATEUP, class C>
+__global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs args, const __grid_constant__ WtMaps maps) {
+  constexpr int kMaxN = C::kMaxN, kAStages = C::kAStages, kNumDqWarps = C::kNumDqWarps;
+  constexpr int kWarpEpi0 = C::kWarpEpi0, kNumEpiWarps = C::kNumEpiWarps, kEpiChunks = C::kEpiChunks;
+  constexpr int kEpiStep = C::kEpiStep, kGatherPerThread = C::kGatherPerThread;
+  constexpr uint32_t kBHalf = C::kBHalf, kBBytes = C::kBBytes, kAccCols = C::kAccCols, kAColBase = C::kAColBase;
+  constexpr uint32_t kOffB = C::kOffB, kOffC = C::kOffC, kOffXpose = C::kOffXpose, kOffBar = C::kOffBar,
+                     kOffMisc = C::kOffMisc;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -251,12 +277,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
       mbar_init(bempty(s), 1);
     }
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(afull(s), kNumDqWarps / 2);  // the four warps (one per lane quarter) of the stage's parity
+      mbar_init(afull(s), 4);  // the four warps (one per lane quarter) of the set that owns the stage
       mbar_init(aempty(s), 1);
     }
     for (int s = 0; s < kCStages; ++s) {
       mbar_init(cfull(s), 1);
-      mbar_init(cempty(s), kNumDqWarps / 2);  // the four warps of one group parity
+      mbar_init(cempty(s), 4);  // the four warps of the set that reads the slot
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf(b), 1);
@@ -363,7 +389,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
         // before the tensor cores' (async proxy) reads
         if (GATEUP) fence_proxy_async();
         umma_stage(d, tmem + kAColBase + sa * kAStageCols, smem_desc_lo(base + kOffB + s * kBBytes), idesc,
-                   t != 0 ? 1u : 0u, bempty(s), aempty(sa));
+                   t != 0 ? 1u : 0u, bempty(s), aempty(sa), kBHalf);
       }
       if (!ok) break;
       umma_commit_warp(accf(buf));
@@ -453,7 +479,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
     // row), so each barrier wait, tensor-memory store wait and arrival is paid
     // once per stage, and consecutive stages are converted side by side.
     const int q = warp & 3;                          // TMEM lane quarter of this warp
-    const int par = (warp - kWarpDq0) >> 2;          // stage parity this warp fills
+    const int par = (warp - kWarpDq0) >> 2;          // the set: this warp fills stages par, par + kAStages, ...
     const int L = q * 32 + lane;                     // TMEM lane = weight row of the tile
     const int srow_stage = GATEUP ? ((L & 1) ? 64 + (L >> 1) : (L >> 1)) : L;  // row in the code stage
     uint32_t g0 = 0, t0 = 0;  // groups and stages of the tiles before this one
@@ -470,7 +496,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
       const size_t row = GATEUP ? size_t(ex) * a.I + j * 64 + (L >> 1) : size_t(ex) * a.D + j * WM + L;
       const uint16_t* srow = m.scales + row * (K / 64);
       const uint16_t* brow = m.biases + row * (K / 64);
-      for (int t = par; t < KT && ok; t += 2) {
+      for (int t = par; t < KT && ok; t += kAStages) {
         const uint32_t is = t0 + t;
         const int s = is % kAStages;
         const uint32_t ph = (is / kAStages) & 1u;
@@ -542,7 +568,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
     // ---------------- epilogue ----------------
     const int q = warp & 3;
     const int L = q * 32 + lane;                    // TMEM lane: weight row of the tile
-    const int half = (warp - kWarpEpi0) >> 2;       // this warp takes 16-column chunks half, half+2, ...
+    const int half = (warp - kWarpEpi0) >> 2;       // this warp takes 16-column chunks half, half + kEpiHalves, ...
     float* xb = reinterpret_cast<float*>(gbase + kOffXpose) + (warp - kWarpEpi0) * 16 * kXposeStride;
     uint32_t tc = 0;
     bool ok = true;
@@ -562,7 +588,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
         int asg[kEpiChunks];
 #pragma unroll
         for (int m = 0; m < kEpiChunks; ++m) {
-          const int nn = half * 16 + 32 * m + (lane >> 1);
+          const int nn = half * 16 + kEpiStep * m + (lane >> 1);
           asg[m] = -1;
           tok[m] = 0;
           wgt[m] = 1.f;
@@ -590,10 +616,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
       tmem_wait_ld(va);
 #pragma unroll
       for (int m = 0; m < kEpiChunks; ++m) {
-        const int n0 = half * 16 + 32 * m;
+        const int n0 = half * 16 + kEpiStep * m;
         if (n0 >= R) break;
         uint32_t(&v)[16] = (m & 1) ? vb : va;
-        if (m + 1 < kEpiChunks && n0 + 32 < R) tmem_ld16(tbase + n0 + 32, (m & 1) ? va : vb);
+        if (m + 1 < kEpiChunks && n0 + kEpiStep < R) tmem_ld16(tbase + n0 + kEpiStep, (m & 1) ? va : vb);
         if (GATEUP) {
           // lane 2i holds gate row i, lane 2i+1 up row i, for tokens n0..n0+15.
           // The pair swaps halves so that the even lane finishes the even
@@ -657,19 +683,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_wt_kernel(const WtArgs ar
   }
 }
 
-}  // namespace
-
-// Both contractions run in stages of 128 of K (D for gate/up, I for down).
-bool gemm_wt_supported(const Ctx& c) {
-  return c.I % (WK * kGroupsPerStage) == 0 && c.D % WM == 0 && tmap_encoder_available();
-}
-
-cudaError_t gemm_wt(const Ctx& c) {
+// Both GEMMs of a layer with one launch shape C.
+template <class C>
+cudaError_t gemm_wt_run(const Ctx& c) {
   const moe_weights* w = c.w;
-  if (c.BM < 1 || c.BM > kWtBlockRows) return cudaErrorInvalidValue;  // a tile takes one block of <= 192 rows
+  if (c.BM < 1 || c.BM > C::kMaxN) return cudaErrorInvalidValue;  // a tile takes one block of <= kMaxN rows
   if (!c.xperm) return cudaErrorInvalidValue;  // gate/up gathers the paired-order x the router wrote
-  if (!ensure_smem_limit(reinterpret_cast<const void*>(gemm_wt_kernel<true>), int(kSmemBytes)) ||
-      !ensure_smem_limit(reinterpret_cast<const void*>(gemm_wt_kernel<false>), int(kSmemBytes)))
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(gemm_wt_kernel<true, C>), int(C::kSmemBytes)) ||
+      !ensure_smem_limit(reinterpret_cast<const void*>(gemm_wt_kernel<false, C>), int(C::kSmemBytes)))
     return cudaErrorInvalidValue;
   const int A = c.T * c.k;
   WtArgs a{c.xperm,  w->gate, w->up,   w->s_gate, w->s_up, c.blocks, c.n_blocks, c.perm, c.topk_w,
@@ -687,7 +708,7 @@ cudaError_t gemm_wt(const Ctx& c) {
   cudaError_t err = c.yacc_zeroed ? cudaSuccess : zero_yacc(c);
   if (err != cudaSuccess) return err;
   const int grid1 = std::max(1, std::min(num_sms(), c.max_blocks * (c.I / 64)));
-  gemm_wt_kernel<true><<<grid1, kNumThreads, kSmemBytes, c.stream>>>(a, maps);
+  gemm_wt_kernel<true, C><<<grid1, C::kNumThreads, C::kSmemBytes, c.stream>>>(a, maps);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done(c, "gateup_tc");
 
@@ -696,14 +717,40 @@ cudaError_t gemm_wt(const Ctx& c) {
   std::memset(&maps, 0, sizeof(maps));
   ok = make_tmap_2d(&maps.c0, U32, 4, w->down.codes, uint64_t(c.E) * c.D, c.I / 8, 8, WM, NOSW) &&
        make_tmap_2d(&maps.cs0, U32, 4, w->s_down.codes, c.D, c.I / 8, 8, WM, NOSW) &&
-       make_tmap_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.h, uint64_t(A + c.T), c.I, WK, kMaxN,
+       make_tmap_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.h, uint64_t(A + c.T), c.I, WK, C::kMaxN,
                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   const int grid2 = std::max(1, std::min(num_sms(), c.max_blocks * (c.D / WM)));
-  gemm_wt_kernel<false><<<grid2, kNumThreads, kSmemBytes, c.stream>>>(a, maps);
+  gemm_wt_kernel<false, C><<<grid2, C::kNumThreads, C::kSmemBytes, c.stream>>>(a, maps);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done(c, "down_tc");
   return cast_y(c);
+}
+
+// Pipeline stages of 128 of K per tile of each GEMM (D for gate/up, I for
+// down) divide evenly among the warp sets, so that every A stage and every
+// code slot is always filled by the same set (one set alone when a tile has
+// a single stage): no parity wait can then run two phases ahead.
+bool stages_fit_sets(const Ctx& c, int sets) {
+  for (const int K : {c.D, c.I}) {
+    const int kt = K / (WK * kGroupsPerStage);
+    if (kt % sets != 0 && kt != 1) return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+bool gemm_wt_supported(const Ctx& c) {
+  return c.I % (WK * kGroupsPerStage) == 0 && c.D % WM == 0 && c.D % (WK * kGroupsPerStage) == 0 &&
+         stages_fit_sets(c, WtLarge::kAStages) && tmap_encoder_available();
+}
+
+bool gemm_wt_small_supported(const Ctx& c) { return gemm_wt_supported(c) && stages_fit_sets(c, WtSmall::kAStages); }
+
+cudaError_t gemm_wt(const Ctx& c) {
+  if (c.BM <= WtSmall::kMaxN && gemm_wt_small_supported(c)) return gemm_wt_run<WtSmall>(c);
+  return gemm_wt_run<WtLarge>(c);
 }
 
 }  // namespace moe

@@ -18,13 +18,14 @@ constexpr int kChunkTokens = 64;
 // Rows per block-map entry consumed by the tensor-core GEMMs.
 constexpr int kTcBlockRows = 128;  // weights dequantised into shared memory (MMA M = tokens)
 constexpr int kWtBlockRows = 192;  // weights dequantised into tensor memory (MMA N = tokens)
+constexpr int kWtSmallBlockRows = 64;  // the same with four weight stages in flight (small blocks)
 constexpr int kMinBlockM = 16;      // smallest block size MOE_OPT_BLOCK_M accepts; sizes the block map
 
 // Library options (moe_set_option). A call works on its own copy, taken
 // once when the call starts, so that another thread's moe_set_option cannot
 // change a call part-way.
 struct Options {
-  int gemv_max_rows = 8;  // the measured small-row sweep: the GEMV path is faster at every row count it takes
+  int gemv_max_rows = 4;  // the measured small-row sweep: GEMV at least as fast up to 4 rows, the GEMM from 5
   int force_path = 0;
   int kernel_timing = 0;
   int gemm_impl = 0;
@@ -104,6 +105,7 @@ cudaError_t gemm_tc(const Ctx& c);
 bool gemm_tc_supported(const Ctx& c);
 cudaError_t gemm_wt(const Ctx& c);
 bool gemm_wt_supported(const Ctx& c);
+bool gemm_wt_small_supported(const Ctx& c);
 int num_sms();
 
 // 2-D TMA tensor map over a row-major [rows, cols] array (false if the

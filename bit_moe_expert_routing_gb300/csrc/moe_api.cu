@@ -198,7 +198,11 @@ Path plan(Ctx& c) {
     p = Path::GemmTc;
   else
     p = Path::GemmSimt;
-  const int path_bm = (p == Path::GemmWt) ? kWtBlockRows : (p == Path::GemmTc) ? kTcBlockRows : kDefaultBlockM;
+  int path_bm = (p == Path::GemmWt) ? kWtBlockRows : (p == Path::GemmTc) ? kTcBlockRows : kDefaultBlockM;
+  // few rows per expert (at most 32 on average): the tensor-memory GEMM's
+  // small-block shape, whose tiles keep four weight stages in flight
+  if (p == Path::GemmWt && size_t(c.T) * c.k <= size_t(32) * c.E && gemm_wt_small_supported(c))
+    path_bm = kWtSmallBlockRows;
   c.BM = o.block_m > 0 ? std::min(o.block_m, path_bm) : path_bm;
   return p;
 }

@@ -118,10 +118,10 @@ typedef struct {
 
 /* Options (process-wide). */
 typedef enum {
-  MOE_OPT_GEMV_MAX_ROWS = 1, /* T <= this runs the decode GEMV path (default 8, its
-                                maximum: on the D=2048, E=256, k=8, I=512 layer the
-                                GEMV path measured faster than the grouped GEMM
-                                at every row count from 2 to 8) */
+  MOE_OPT_GEMV_MAX_ROWS = 1, /* T <= this runs the decode GEMV path (0..8; default 4:
+                                on the D=2048, E=256, k=8, I=512 layer the GEMV path
+                                measured at least as fast as the grouped GEMM at 2,
+                                3 and 4 rows and slower at 5 and 8) */
   MOE_OPT_FORCE_PATH = 2,    /* 0 auto by row count, 1 GEMV, 2 grouped GEMM */
   MOE_OPT_KERNEL_TIMING = 3, /* 1: record CUDA events around each kernel of
                                 the next forwards (read with moe_kernel_times) */
