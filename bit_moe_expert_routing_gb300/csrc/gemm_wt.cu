@@ -47,8 +47,6 @@ namespace {
 constexpr int WM = 128;               // weight rows per tile (MMA M, TMEM lanes)
 constexpr int WK = 64;                // one quantisation group
 constexpr int kGroupsPerStage = 2;    // a pipeline stage spans 128 of K
-constexpr int kBStages = 3;           // token operand ring (shared memory)
-constexpr int kCStages = 8;           // packed-code ring, one group per stage
 constexpr uint32_t kCBytes = WM * WK / 2;               // 4 KB of codes
 constexpr uint32_t kAGroupCols = WK / 2;                // 32 columns: one group's 64 bf16 per lane
 constexpr uint32_t kAStageCols = kAGroupCols * kGroupsPerStage;
@@ -59,11 +57,19 @@ constexpr int kWarpTma = 0, kWarpMma = 1, kWarpB0 = 2, kNumBWarps = 4, kWarpDq0 
 // A launch shape of the kernel: the largest token block of a tile (MMA N),
 // the dequantising warp sets (one per A stage in tensor memory: set p fills
 // the stages t = p, p + SETS, ... and owns A stage p; four warps, one per
-// TMEM lane quarter, each) and the epilogue warps (EPIW / 4 per lane quarter).
+// TMEM lane quarter, each), the epilogue warps (EPIW / 4 per lane quarter)
+// and the slots of the packed-code and token rings (the bytes in flight per SM).
 // Tensor memory holds two accumulators of MAXN columns and SETS A stages.
-template <int MAXN, int SETS, int EPIW>
+template <int MAXN, int SETS, int EPIW, int CSLOTS, int BSLOTS, bool SBSMEM>
 struct WtCfg {
+  // SBSMEM: the TMA warp also copies each tile's scale and bias rows into a
+  // two-slot ring in shared memory, ahead of use; otherwise the dequantising
+  // warps load each stage's pair from global memory when they need it
+  static constexpr int kSbSlots = SBSMEM ? 2 : 0;
+  static constexpr uint32_t kSbBytes = 16384;  // one tile's rows: 8 K bytes, K <= 2048
   static constexpr int kMaxN = MAXN;
+  static constexpr int kBStages = BSLOTS;  // token operand ring (shared memory)
+  static constexpr int kCStages = CSLOTS;  // packed-code ring, one quantisation group per slot
   static constexpr int kAStages = SETS;
   static constexpr int kNumDqWarps = 4 * SETS;
   static constexpr int kNumEpiWarps = EPIW;
@@ -81,9 +87,11 @@ struct WtCfg {
   static constexpr uint32_t kOffB = 0;
   static constexpr uint32_t kOffC = kOffB + kBStages * kBBytes;
   static constexpr uint32_t kOffXpose = kOffC + kCStages * kCBytes;  // down epilogue: [warp][16][36] floats
-  static constexpr uint32_t kOffBar = kOffXpose + kNumEpiWarps * 16 * kXposeStride * 4;
-  // bfull, bempty [kBStages]; afull, aempty [kAStages]; cfull, cempty [kCStages]; accf, acce [2]; drain; never
-  static constexpr uint32_t kNumBars = 2 * kBStages + 2 * kAStages + 2 * kCStages + 6;
+  static constexpr uint32_t kOffSb = kOffXpose + kNumEpiWarps * 16 * kXposeStride * 4;
+  static constexpr uint32_t kOffBar = kOffSb + kSbSlots * kSbBytes;
+  // bfull, bempty [kBStages]; afull, aempty [kAStages]; cfull, cempty [kCStages]; accf, acce [2]; drain; never;
+  // sbfull, sbempty [kSbSlots]
+  static constexpr uint32_t kNumBars = 2 * kBStages + 2 * kAStages + 2 * kCStages + 6 + 2 * kSbSlots;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr size_t kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
   static_assert(kAColBase + kAStages * kAStageCols <= kTmemCols, "tensor memory budget");
@@ -94,9 +102,12 @@ struct WtCfg {
 };
 // 192-token blocks with two weight stages in flight (the default), and
 // blocks of at most 64 tokens with four: small blocks leave tensor memory
-// for more A stages, and their tiles are bound by the dequantisation chain.
-using WtLarge = WtCfg<kWtBlockRows, 2, 8>;
-using WtSmall = WtCfg<kWtSmallBlockRows, 4, 4>;
+// for more A stages, and their tiles are bound by the chain of dependent
+// loads and dequantisation, not by the tensor pipe: their scale and bias rows
+// come ahead of use through shared memory (at a stage of a few hundred
+// cycles a global load per stage would be a DRAM round trip on the chain).
+using WtLarge = WtCfg<kWtBlockRows, 2, 8, 8, 3, false>;
+using WtSmall = WtCfg<kWtSmallBlockRows, 4, 4, 8, 3, true>;
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
   asm volatile(
@@ -230,6 +241,10 @@ struct WtArgs {
   long long epi_wait_limit;  // > 0: test hook, the epilogue first waits this long on a barrier nothing arrives on
 };
 
+struct TileEntry {
+  int g, p0, R;  // expert (E: the shared expert), first row, rows
+};
+
 struct WtMaps {
   CUtensorMap c0, c1;    // routed codes: gate, up (box 8 words x 64 rows) or down (box 8 x 128)
   CUtensorMap cs0, cs1;  // shared-expert codes
@@ -244,6 +259,9 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
   constexpr uint32_t kBHalf = C::kBHalf, kBBytes = C::kBBytes, kAccCols = C::kAccCols, kAColBase = C::kAColBase;
   constexpr uint32_t kOffB = C::kOffB, kOffC = C::kOffC, kOffXpose = C::kOffXpose, kOffBar = C::kOffBar,
                      kOffMisc = C::kOffMisc;
+  constexpr int kCStages = C::kCStages, kBStages = C::kBStages, kSbSlots = C::kSbSlots;
+  constexpr int kSbRing = kSbSlots > 0 ? kSbSlots : 1;  // divisor for ring positions (unused when kSbSlots == 0)
+  constexpr uint32_t kSbBytes = C::kSbBytes, kOffSb = C::kOffSb;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -260,6 +278,8 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
   auto acce = [&](int b) { return bar0 + 8u * (kBarAcc + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (kBarAcc + 4);
   const uint32_t never_bar = bar0 + 8u * (kBarAcc + 5);  // test hook: nothing arrives here
+  auto sbfull = [&](int s) { return bar0 + 8u * (kBarAcc + 6 + s); };
+  auto sbempty = [&](int s) { return bar0 + 8u * (kBarAcc + 6 + kSbSlots + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kOffMisc + 4);
 
@@ -290,6 +310,10 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
     }
     mbar_init(drain_bar, 1);
     mbar_init(never_bar, 1);
+    for (int s = 0; s < kSbSlots; ++s) {
+      mbar_init(sbfull(s), 1);
+      mbar_init(sbempty(s), kNumDqWarps);  // every dequantising warp, after its last stage of the tile
+    }
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -311,13 +335,23 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
   }
   const int n_tiles = nb * NT;
 
-  auto tile_info = [&](int tile, int& g, int& p0, int& R, int& j) {
-    const int b = tile / NT;
-    j = tile % NT;
-    g = a.blocks[3 * b];
-    p0 = a.blocks[3 * b + 1];
-    R = a.blocks[3 * b + 2];
-    if (g < 0 || g > a.E || R < 1 || R > kMaxN || p0 < 0 || p0 + R > A_rows + a.T) {
+  // Block-map entries are loaded one tile ahead of use: every role issues
+  // the loads of its next tile's entry when it starts a tile, so a new tile
+  // does not begin with a global-memory round trip. An entry is checked when
+  // its tile starts.
+  auto entry_load = [&](int tile) {
+    TileEntry e{0, 0, 0};
+    if (tile < n_tiles) {
+      const int b = tile / NT;
+      e.g = a.blocks[3 * b];
+      e.p0 = a.blocks[3 * b + 1];
+      e.R = a.blocks[3 * b + 2];
+    }
+    return e;
+  };
+  auto entry_ok = [&](const TileEntry& e) {
+    if (e.g < 0 || e.g > a.E || e.R < 1 || e.R > kMaxN || e.p0 < 0 || e.p0 + e.R > A_rows + a.T ||
+        (e.g < a.E && e.p0 + e.R > A_rows)) {
       report(a.hdr, MOE_ERR_DEVICE_CHECK, 21);
       return false;
     }
@@ -327,16 +361,46 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
   if (warp == kWarpTma) {
     // ---------------- TMA producer: codes (and h rows for down) ----------------
     if (lane == 0) {
-      uint32_t it = 0, c_issued = 0;
+      uint32_t it = 0, c_issued = 0, sb_issued = 0;
       bool ok = true;
+      TileEntry nx = entry_load(blockIdx.x);
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        int g, p0, R, j;
-        if (!tile_info(tile, g, p0, R, j)) {
+        const TileEntry e = nx;
+        nx = entry_load(tile + gridDim.x);
+        if (!entry_ok(e)) {
           *abort_flag = 1;
           break;
         }
+        const int g = e.g, j = tile % NT;
         const bool sh = (g == a.E);
         const int ex = sh ? 0 : g;
+        if (kSbSlots > 0) {
+          // the tile's scale and bias rows: gate/up [gate s][gate b][up s][up b]
+          // of 64 rows, down [s][b] of 128 rows, K / 64 bf16 per row
+          const int ss = sb_issued % kSbRing;
+          if (!(ok = mbar_wait(sbempty(ss), ((sb_issued / kSbRing) & 1u) ^ 1u, abort_flag, a.hdr))) break;
+          const uint32_t sdst = base + kOffSb + ss * kSbBytes;
+          const int G2 = K / 64;
+          if (GATEUP) {
+            const size_t row0 = size_t(ex) * a.I + j * 64;
+            const uint32_t nb = 64u * G2 * 2;
+            mbar_arrive_tx(sbfull(ss), 4 * nb);
+            const moe_qmatrix& mg = sh ? a.s0 : a.m0;
+            const moe_qmatrix& mu = sh ? a.s1 : a.m1;
+            bulk_g2s(sdst, mg.scales + row0 * G2, nb, sbfull(ss));
+            bulk_g2s(sdst + nb, mg.biases + row0 * G2, nb, sbfull(ss));
+            bulk_g2s(sdst + 2 * nb, mu.scales + row0 * G2, nb, sbfull(ss));
+            bulk_g2s(sdst + 3 * nb, mu.biases + row0 * G2, nb, sbfull(ss));
+          } else {
+            const size_t row0 = size_t(ex) * a.D + j * WM;
+            const uint32_t nb = uint32_t(WM) * G2 * 2;
+            mbar_arrive_tx(sbfull(ss), 2 * nb);
+            const moe_qmatrix& md = sh ? a.s0 : a.m0;
+            bulk_g2s(sdst, md.scales + row0 * G2, nb, sbfull(ss));
+            bulk_g2s(sdst + nb, md.biases + row0 * G2, nb, sbfull(ss));
+          }
+          ++sb_issued;
+        }
         for (int ks = 0; ks < KS; ++ks, ++it) {
           const int cs = it % kCStages;
           const uint32_t cph = (it / kCStages) & 1u;
@@ -359,6 +423,11 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
           const uint32_t last = c_issued - 1 - ((c_issued - 1 - s) % kCStages);
           mbar_wait(cfull(s), (last / kCStages) & 1u, abort_flag, a.hdr, kWaitLimit, true);
         }
+      for (uint32_t s = 0; s < uint32_t(kSbRing); ++s)
+        if (s < sb_issued) {
+          const uint32_t last = sb_issued - 1 - ((sb_issued - 1 - s) % kSbRing);
+          mbar_wait(sbfull(s), (last / kSbRing) & 1u, abort_flag, a.hdr, kWaitLimit, true);
+        }
     }
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer: the whole warp runs the loop, one lane issues ----------------
@@ -369,12 +438,15 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
     };
     uint32_t it = 0, tc = 0;
     bool ok = true;
+    TileEntry nx = entry_load(blockIdx.x);
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
-      int g, p0, R, j;
-      if (!tile_info(tile, g, p0, R, j)) {
+      const TileEntry e = nx;
+      nx = entry_load(tile + gridDim.x);
+      if (!entry_ok(e)) {
         *abort_flag = 1;
         break;
       }
+      const int R = e.R;
       const uint32_t idesc = idesc_n((R + 15) & ~15);
       const int buf = tc & 1;
       if (!(ok = warp_wait(acce(buf), ((tc >> 1) & 1u) ^ 1u, false))) break;
@@ -400,28 +472,48 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
     // ---------------- the token operand (B) ----------------
     const int bt = threadIdx.x - kWarpB0 * 32;  // 0..127
     if (GATEUP) {
-      // chunk m of this thread: row (bt + 128m) / 8, 16-byte chunk (bt + 128m) % 8
-      uint32_t it = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        int g, p0, R, j;
-        if (!tile_info(tile, g, p0, R, j)) {
-          *abort_flag = 1;
-          break;
+      // chunk m of this thread: row (bt + 128m) / 8, 16-byte chunk (bt + 128m) % 8.
+      // The next tile's entry and its rows' perm entries are loaded while the
+      // current tile's first stage is issued, so a new tile's gathers start
+      // without waiting for two dependent global loads. The eight lanes that
+      // share a row set split those loads (lane chunk c loads the rows of
+      // chunks c, c + 8, ...) and exchange them by shuffles.
+      constexpr int kRowRegs = (kGatherPerThread + 7) / 8;
+      const int ch = bt & 7;
+      TileEntry nx = entry_load(blockIdx.x);
+      int nx_row[kRowRegs];  // routed: the perm entry of a row; shared: its token
+      auto rows_load = [&](const TileEntry& ne) {
+#pragma unroll
+        for (int i = 0; i < kRowRegs; ++i) {
+          const int m = ch + 8 * i;
+          const int row = (bt >> 3) + 16 * m;
+          const int rr = (m < kGatherPerThread && row < ne.R) ? row : 0;
+          nx_row[i] = (ne.g == a.E) ? (ne.p0 + rr - A_rows) : a.perm[ne.p0 + rr];
         }
+      };
+      uint32_t it = 0;
+      bool ok = blockIdx.x >= n_tiles || entry_ok(nx);
+      if (ok && blockIdx.x < n_tiles) rows_load(nx);
+      if (!ok) *abort_flag = 1;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const TileEntry e = nx;  // checked before its rows were loaded
+        nx = entry_load(tile + gridDim.x);
+        const bool sh = (e.g == a.E);
+        const int R = e.R;
         const int n = (R + 15) & ~15;  // rows the MMA reads; R..n-1 repeat a valid row
-        const char* src[kGatherPerThread];
+        // byte offsets into x of this thread's chunks (x is under 4 GB)
+        uint32_t src[kGatherPerThread];
 #pragma unroll
         for (int m = 0; m < kGatherPerThread; ++m) {
-          const int lin = bt + 128 * m, row = lin >> 3, ch = lin & 7;
-          const int rr = row < R ? row : 0;
-          int t = (g == a.E) ? (p0 + rr - A_rows) : (a.perm[p0 + rr] / a.k);
+          const int v = __shfl_sync(0xffffffffu, nx_row[m >> 3], (lane & 24) | (m & 7));
+          int t = sh ? v : v / a.k;
           if (t < 0 || t >= a.T) {
             report(a.hdr, MOE_ERR_DEVICE_CHECK, 22);
             t = 0;
           }
-          src[m] = reinterpret_cast<const char*>(a.x + size_t(t) * a.D) + ch * 16;
+          src[m] = uint32_t(t) * uint32_t(a.D * 2) + uint32_t(ch * 16);
         }
+        const char* xbytes = reinterpret_cast<const char*>(a.x);
         // this thread copies chunk column bt & 7 of rows r0 + 16 m: in the
         // swizzled tile those land at sw0 + 2048 m (row & 7 is the same for all m)
         const int r0 = bt >> 3;
@@ -440,8 +532,17 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
           for (int hb = 0; hb < kGroupsPerStage; ++hb)
 #pragma unroll
             for (int m = 0; m < kGatherPerThread; ++m)
-              if (live & (1u << m)) cp_async16(dst + hb * kBHalf + 2048u * m, src[m] + koff + hb * 128, 16u);
+              if (live & (1u << m)) cp_async16(dst + hb * kBHalf + 2048u * m, xbytes + src[m] + koff + hb * 128, 16u);
           cp_async_arrive_noinc(bfull(s));
+          if (t == 0 && tile + int(gridDim.x) < n_tiles) {  // the next tile's rows
+            if (entry_ok(nx)) {
+              rows_load(nx);
+            } else {
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+          }
         }
       }
       cp_async_wait<0>();
@@ -449,12 +550,15 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
       // down: rows p0.. of h as one 2-D TMA tile per k-step
       uint32_t it = 0, issued = 0;
       bool ok = true;
+      TileEntry nx = entry_load(blockIdx.x);
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        int g, p0, R, j;
-        if (!tile_info(tile, g, p0, R, j)) {
+        const TileEntry e = nx;
+        nx = entry_load(tile + gridDim.x);
+        if (!entry_ok(e)) {
           *abort_flag = 1;
           break;
         }
+        const int p0 = e.p0;
         for (int t = 0; t < KT; ++t, ++it) {
           const int s = it % kBStages;
           const uint32_t ph = (it / kBStages) & 1u;
@@ -482,20 +586,42 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
     const int par = (warp - kWarpDq0) >> 2;          // the set: this warp fills stages par, par + kAStages, ...
     const int L = q * 32 + lane;                     // TMEM lane = weight row of the tile
     const int srow_stage = GATEUP ? ((L & 1) ? 64 + (L >> 1) : (L >> 1)) : L;  // row in the code stage
-    uint32_t g0 = 0, t0 = 0;  // groups and stages of the tiles before this one
+    uint32_t g0 = 0, t0 = 0, tcount = 0;  // groups, stages and tiles before this one
     bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, g0 += KS, t0 += KT) {
-      int g, p0, R, j;
-      if (!tile_info(tile, g, p0, R, j)) {
+    // only the expert of an entry is read here (one register held ahead);
+    // the other roles check whole entries
+    auto expert_of = [&](int tile) { return tile < n_tiles ? a.blocks[3 * (tile / NT)] : 0; };
+    int nx_g = expert_of(blockIdx.x);
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, g0 += KS, t0 += KT, ++tcount) {
+      const int g = nx_g, j = tile % NT;
+      nx_g = expert_of(tile + gridDim.x);
+      if (g < 0 || g > a.E) {
+        report(a.hdr, MOE_ERR_DEVICE_CHECK, 21);
         *abort_flag = 1;
         break;
       }
       const bool sh = (g == a.E);
       const int ex = sh ? 0 : g;
-      const moe_qmatrix& m = GATEUP ? ((L & 1) ? (sh ? a.s1 : a.m1) : (sh ? a.s0 : a.m0)) : (sh ? a.s0 : a.m0);
-      const size_t row = GATEUP ? size_t(ex) * a.I + j * 64 + (L >> 1) : size_t(ex) * a.D + j * WM + L;
-      const uint16_t* srow = m.scales + row * (K / 64);
-      const uint16_t* brow = m.biases + row * (K / 64);
+      const uint16_t* srow;
+      const uint16_t* brow;
+      const int ss = int(tcount % kSbRing);
+      if (kSbSlots > 0) {  // this row's pairs in the tile's shared-memory copy
+        if (!(ok = mbar_wait(sbfull(ss), (tcount / kSbRing) & 1u, abort_flag, a.hdr))) break;
+        const int G2 = K / 64;
+        const uint16_t* sb = reinterpret_cast<const uint16_t*>(gbase + kOffSb + ss * kSbBytes);
+        if (GATEUP) {
+          srow = sb + ((L & 1) ? 128 * G2 : 0) + (L >> 1) * G2;
+          brow = srow + 64 * G2;
+        } else {
+          srow = sb + L * G2;
+          brow = srow + WM * G2;
+        }
+      } else {
+        const moe_qmatrix& m = GATEUP ? ((L & 1) ? (sh ? a.s1 : a.m1) : (sh ? a.s0 : a.m0)) : (sh ? a.s0 : a.m0);
+        const size_t row = GATEUP ? size_t(ex) * a.I + j * 64 + (L >> 1) : size_t(ex) * a.D + j * WM + L;
+        srow = m.scales + row * (K / 64);
+        brow = m.biases + row * (K / 64);
+      }
       for (int t = par; t < KT && ok; t += kAStages) {
         const uint32_t is = t0 + t;
         const int s = is % kAStages;
@@ -563,6 +689,10 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
         __syncwarp();
         if (lane == 0) mbar_arrive(afull(s));
       }
+      if (kSbSlots > 0) {  // the tile's scale and bias rows have been read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sbempty(ss));
+      }
     }
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kNumEpiWarps) {
     // ---------------- epilogue ----------------
@@ -572,12 +702,15 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
     float* xb = reinterpret_cast<float*>(gbase + kOffXpose) + (warp - kWarpEpi0) * 16 * kXposeStride;
     uint32_t tc = 0;
     bool ok = true;
+    TileEntry nx = entry_load(blockIdx.x);
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
-      int g, p0, R, j;
-      if (!tile_info(tile, g, p0, R, j)) {
+      const TileEntry e = nx;
+      nx = entry_load(tile + gridDim.x);
+      if (!entry_ok(e)) {
         *abort_flag = 1;
         break;
       }
+      const int g = e.g, p0 = e.p0, R = e.R, j = tile % NT;
       const int buf = tc & 1;
       const bool sh = (g == a.E);
       // down: this lane's token and routing weight for each of its chunks,
@@ -742,11 +875,17 @@ bool stages_fit_sets(const Ctx& c, int sets) {
 }  // namespace
 
 bool gemm_wt_supported(const Ctx& c) {
+  // the gather addresses x with 32-bit byte offsets
   return c.I % (WK * kGroupsPerStage) == 0 && c.D % WM == 0 && c.D % (WK * kGroupsPerStage) == 0 &&
-         stages_fit_sets(c, WtLarge::kAStages) && tmap_encoder_available();
+         size_t(c.T) * c.D * 2 <= 0xFFFFFFFFu && stages_fit_sets(c, WtLarge::kAStages) && tmap_encoder_available();
 }
 
-bool gemm_wt_small_supported(const Ctx& c) { return gemm_wt_supported(c) && stages_fit_sets(c, WtSmall::kAStages); }
+bool gemm_wt_small_supported(const Ctx& c) {
+  // a tile's scale and bias rows (8 K bytes for gate/up, 4 K for down) fit a
+  // 16 KB slot, and their rows start 16-byte aligned (K % 512 == 0)
+  return gemm_wt_supported(c) && stages_fit_sets(c, WtSmall::kAStages) && c.D % 512 == 0 && c.I % 512 == 0 &&
+         8u * c.D <= WtSmall::kSbBytes && 4u * c.I <= WtSmall::kSbBytes;
+}
 
 cudaError_t gemm_wt(const Ctx& c) {
   if (c.BM <= WtSmall::kMaxN && gemm_wt_small_supported(c)) return gemm_wt_run<WtSmall>(c);

@@ -31,30 +31,38 @@ __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// One try of a phase wait. The thread may be suspended in hardware (not
+// issuing) until the phase completes or, at most, kTrySuspendNs pass, so a
+// waiting warp does not take issue slots from the warps doing work.
+constexpr uint32_t kTrySuspendNs = 20000;
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kTrySuspendNs)
       : "memory");
   return ok != 0;
 }
 
 // Bounded wait for the phase of `parity` to complete. Gives up when the CTA's
 // abort flag is set (unless draining) or after `limit` cycles (then sets the
-// flag and records MOE_ERR_DEVICE_TIMEOUT with `site` as its detail).
+// flag and records MOE_ERR_DEVICE_TIMEOUT with `site` as its detail). The flag
+// and the clock are checked every 16 tries: the loop's own instructions take
+// issue slots from the warps that do the work.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr,
                                           long long limit = kWaitLimit, bool draining = false, int site = 100) {
   if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
-  while (true) {
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try(bar, parity)) return true;
-    if (!draining && *abort_flag) return false;
-    if (clock64() - t0 > limit) {
-      *abort_flag = 1;
-      report(hdr, MOE_ERR_DEVICE_TIMEOUT, site);
-      return false;
+    if ((i & 15u) == 0) {
+      if (!draining && *abort_flag) return false;
+      if (clock64() - t0 > limit) {
+        *abort_flag = 1;
+        report(hdr, MOE_ERR_DEVICE_TIMEOUT, site);
+        return false;
+      }
     }
   }
 }
