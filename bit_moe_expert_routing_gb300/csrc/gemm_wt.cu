@@ -105,9 +105,11 @@ struct WtCfg {
 // for more A stages, and their tiles are bound by the chain of dependent
 // loads and dequantisation, not by the tensor pipe: their scale and bias rows
 // come ahead of use through shared memory (at a stage of a few hundred
-// cycles a global load per stage would be a DRAM round trip on the chain).
+// cycles a global load per stage would be a DRAM round trip on the chain),
+// and their code ring holds two stages per set, so that the next stage's
+// codes are in flight while a set converts the current one.
 using WtLarge = WtCfg<kWtBlockRows, 2, 8, 8, 3, false>;
-using WtSmall = WtCfg<kWtSmallBlockRows, 4, 4, 8, 3, true>;
+using WtSmall = WtCfg<kWtSmallBlockRows, 4, 4, 16, 3, true>;
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
   asm volatile(
@@ -150,8 +152,10 @@ __device__ __forceinline__ uint32_t idesc_n(int n) {
 // blocks of 64, the first with descriptor low half b_lo, the second kBHalf
 // bytes further)^T, then commits that arrive on `bar_b` and `bar_a` (the two
 // operand stages' release barriers) when they complete. The first MMA
-// overwrites D when `accumulate` is 0. Executed by the whole warp so that every
-// operand is warp-uniform; one elected lane issues.
+// overwrites D when `accumulate` is 0. Executed by the whole, converged warp
+// (the caller reconverges it first) so that every operand is warp-uniform and
+// elect.sync picks the same lane every time: a commit tracks only the MMAs of
+// the lane that executes it.
 __device__ __forceinline__ void umma_stage(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t idesc, uint32_t accumulate,
                                            uint32_t bar_b, uint32_t bar_a, uint32_t b_half) {
   asm volatile(
@@ -183,8 +187,9 @@ __device__ __forceinline__ void umma_stage(uint32_t d, uint32_t a, uint32_t b_lo
       : "memory");
 }
 
-// Commit by one elected lane of a converged warp: `bar` receives one arrival
-// when every MMA this thread issued before has completed.
+// Commit by one elected lane of a converged warp (the same lane that issued
+// the MMAs): `bar` receives one arrival when every MMA this thread issued
+// before has completed.
 __device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
   asm volatile(
       "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
@@ -460,12 +465,17 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
         // the gathered tokens were written by cp.async (generic proxy): order them
         // before the tensor cores' (async proxy) reads
         if (GATEUP) fence_proxy_async();
+        // the lanes left the barrier waits above at different times: reconverge
+        // so that elect.sync picks lane 0, the lane of every earlier MMA
+        __syncwarp();
         umma_stage(d, tmem + kAColBase + sa * kAStageCols, smem_desc_lo(base + kOffB + s * kBBytes), idesc,
                    t != 0 ? 1u : 0u, bempty(s), aempty(sa), kBHalf);
       }
       if (!ok) break;
+      __syncwarp();
       umma_commit_warp(accf(buf));
     }
+    __syncwarp();
     umma_commit_warp(drain_bar);  // all MMAs complete before tensor memory is released
     warp_wait(drain_bar, 0, true);
   } else if (warp >= kWarpB0 && warp < kWarpB0 + kNumBWarps) {
