@@ -793,42 +793,51 @@ def run_ablations(args) -> dict:
             "weights_as_M_tcgen05": layer_ms(name, {moe.MOE_OPT_GEMM_IMPL: moe.GEMM_TENSOR_CORE}),
             "tokens_as_M_tcgen05": layer_ms(name, {moe.MOE_OPT_GEMM_IMPL: moe.GEMM_TENSOR_CORE_SMEM}),
             "cuda_cores": layer_ms(name, {moe.MOE_OPT_GEMM_IMPL: moe.GEMM_CUDA_CORE})}
-    # 4. separate dequantisation: expanding every touched expert matrix to bf16
-    #    in HBM, the pass a separate-dequant design runs before its GEMMs (its
-    #    GEMMs then read 3.6x the weight bytes), against the fused layer
+    # 4. separate dequantisation: the unfused layer (routing; a pass that
+    #    expands every selected expert's and the shared expert's weights to
+    #    bf16 in HBM; grouped GEMMs reading those bf16 weights through TMA)
+    #    against the fused layers: the same shared-memory GEMM dequantising on
+    #    chip, and the default tensor-memory GEMM
     layer, x_np, dl, x, y = layer_of("prefill4096_zipf")
-    ws = dl.workspace(x.shape[0])
-    st = moe.moe_route(dl.w, x.data_ptr(), x.shape[0], ws.data_ptr(), ws.numel(), sp, None)
-    if st != moe.MOE_OK:
-        raise moe.MoEError(st, "moe_route")
-    v = dl.view(x.shape[0], ws)
-    count = moe.ws_tensor(ws, v.count, (layer.E,), torch.int32).cpu().numpy()
-    touched = [int(e) for e in np.nonzero(count)[0]]
-    rows_k = {"gate": (layer.I, layer.D), "up": (layer.I, layer.D), "down": (layer.D, layer.I)}
-    outbuf = torch.empty(max(r * k for r, k in rows_k.values()), dtype=torch.int16, device=device)
+    T = x.shape[0]
+    ws = dl.workspace(T)
+    nb = moe.moe_expanded_weights_bytes(dl.w)
+    wbuf = torch.empty(nb, dtype=torch.uint8, device=device)
     ms = []
+    moe.moe_kernel_times()
     for i in range(3 + steps):
         flush.zero_()
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
+        if i == 3:
+            moe.moe_set_option(moe.MOE_OPT_KERNEL_TIMING, 1)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for e in touched + [None]:
-            for mname, (rows, K) in rows_k.items():
-                qm = getattr(dl.w, ("s_" + mname) if e is None else mname)
-                r = moe.moe_debug_dequant(qm, 0 if e is None else e, rows, K, outbuf.data_ptr(), sp)
-                if r != moe.MOE_OK:
-                    raise moe.MoEError(r, "moe_debug_dequant")
+        st = moe.moe_layer_forward_expanded(dl.w, x.data_ptr(), T, y.data_ptr(), ws.data_ptr(), ws.numel(),
+                                            wbuf.data_ptr(), nb, sp)
+        if st != moe.MOE_OK:
+            raise moe.MoEError(st, "moe_layer_forward_expanded")
         b.record(stream)
         b.synchronize()
         if i >= 3:
             ms.append(a.elapsed_time(b))
-    n_exp = len(touched) + 1
+    moe.moe_set_option(moe.MOE_OPT_KERNEL_TIMING, 0)
+    kt = {nm: 1e3 * tms / steps for nm, (tms, cnt) in moe.moe_kernel_times().items()}  # us per step
+    st = moe.moe_get_device_status(ctypes.c_void_p(ws.data_ptr()), sp)
+    if st != moe.MOE_OK:
+        raise moe.MoEError(st, "device status")
+    v = dl.view(T, ws)
+    count = moe.ws_tensor(ws, v.count, (layer.E,), torch.int32).cpu().numpy()
+    n_exp = int(np.count_nonzero(count)) + 1
+    del wbuf
     written = n_exp * 3 * layer.D * layer.I * 2
     read = n_exp * expert_bytes(layer.D, layer.I)
     out["separate_dequant"] = dict(
-        workload="prefill4096_zipf", experts=n_exp, dequant_pass_ms=sorted(ms)[len(ms) // 2],
-        bf16_bytes_written=written, packed_bytes_read=read,
-        hbm_floor_ms=(written + read) / (measured_peaks()["hbm_gbs"] * 1e9) * 1e3,
-        fused_layer_ms=layer_ms("prefill4096_zipf"))
+        workload="prefill4096_zipf", experts=n_exp, unfused_layer_ms=sorted(ms)[len(ms) // 2],
+        unfused_kernel_us_per_step={k: round(v, 2) for k, v in kt.items()},
+        expansion_bf16_bytes_written=written, expansion_packed_bytes_read=read,
+        expansion_hbm_floor_ms=(written + read) / (measured_peaks()["hbm_gbs"] * 1e9) * 1e3,
+        fused_same_gemm_ms=layer_ms("prefill4096_zipf", {moe.MOE_OPT_GEMM_IMPL: moe.GEMM_TENSOR_CORE_SMEM}),
+        fused_default_ms=layer_ms("prefill4096_zipf"))
     # 5. one token: the single fused kernel vs routing + two GEMV kernels
     out["decode"] = dict(fused_ms=layer_ms("decode", {moe.MOE_OPT_DECODE_FUSED: 1}),
                          separate_ms=layer_ms("decode", {moe.MOE_OPT_DECODE_FUSED: 0}))

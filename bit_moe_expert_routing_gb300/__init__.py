@@ -76,6 +76,8 @@ SIGNATURES = {
     "moe_kernel_times": (_CI, [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float),
                                ctypes.POINTER(ctypes.c_int), _CI, ctypes.POINTER(ctypes.c_int)]),
     "moe_debug_dequant": (_CI, [ctypes.POINTER(moe_qmatrix), _CI, _CI, _CI, _VP, _VP]),
+    "moe_expanded_weights_bytes": (_SZ, [_W]),
+    "moe_layer_forward_expanded": (_CI, [_W, _VP, _CI, _VP, _VP, _SZ, _VP, _SZ, _VP]),
     "moe_last_launch_count": (_CI, []),
     "moe_status_string": (ctypes.c_char_p, [_CI]),
 }
@@ -131,6 +133,17 @@ def moe_layer_forward_static(w, x_ptr, T, y_ptr, stream) -> int:
 
 def moe_get_device_status_static(stream) -> int:
     return lib().moe_get_device_status_static(stream)
+
+
+def moe_expanded_weights_bytes(w: moe_weights) -> int:
+    return lib().moe_expanded_weights_bytes(ctypes.byref(w))
+
+
+def moe_layer_forward_expanded(w, x_ptr, T, y_ptr, ws_ptr, ws_bytes, wbuf_ptr, wbuf_bytes, stream) -> int:
+    """The unfused form: a separate pass expands the selected experts'
+    weights to bf16 in wbuf, then the GEMMs read them."""
+    return lib().moe_layer_forward_expanded(ctypes.byref(w), x_ptr, T, y_ptr, ws_ptr, ws_bytes, wbuf_ptr, wbuf_bytes,
+                                            stream)
 
 
 def moe_layer_forward_host(w, x_host_ptr, T, y_host_ptr, ws_ptr, ws_bytes, stream) -> int:

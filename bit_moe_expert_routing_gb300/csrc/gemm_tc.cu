@@ -17,6 +17,11 @@
 //            combine accumulator of token t (shared-expert rows with weight 1).
 // The K loop runs one 64-wide quantisation group per step.
 //
+// A second form of each kernel reads weights that a separate pass has already
+// expanded to bf16 in device memory (the design the fused form replaces, kept
+// for measuring what fusion saves): the TMA producer then loads the weight
+// stage itself and the dequantising warps have no work.
+//
 // Warp roles (18 warps):
 //   0      TMA producer: packed codes of the 256 weight rows (and, for down,
 //          the 128 h rows of the tile)
@@ -154,12 +159,15 @@ struct TcArgs {
 };
 
 struct TcMaps {
-  CUtensorMap c0, c1;    // routed codes (gate, up) or (down, unused)
-  CUtensorMap cs0, cs1;  // shared-expert codes
+  CUtensorMap c0, c1;    // routed codes (gate, up) or (down, unused); bf16 weights in the second form
+  CUtensorMap cs0, cs1;  // shared-expert codes; bf16 weights in the second form
   CUtensorMap a;         // down only: h rows, bf16, SW128 box 64 x 128
 };
 
-template <bool GATEUP>
+// BF16W: the weights arrive as bf16 (128-byte-swizzled TMA tiles of 64 x 128
+// rows) on afull, with the h rows for down; full then counts the token
+// gather alone (gate/up) or nothing (down).
+template <bool GATEUP, bool BF16W>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs args, const __grid_constant__ TcMaps maps) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -168,7 +176,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
   const uint32_t bar0 = base + kOffBar;
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto afull = [&](int s) { return bar0 + 8u * (2 * kStages + s); };  // down: h rows landed
+  auto afull = [&](int s) { return bar0 + 8u * (2 * kStages + s); };  // TMA loads landed (down: h rows; bf16 weights)
   auto cfull = [&](int s) { return bar0 + 8u * (3 * kStages + s); };
   auto cempty = [&](int s) { return bar0 + 8u * (3 * kStages + kCStages + s); };
   constexpr uint32_t kBarAcc = 3 * kStages + 2 * kCStages;
@@ -188,7 +196,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full(s), GATEUP ? (kNumDqWarps + kNumAWarps) : kNumDqWarps);
+      mbar_init(full(s), GATEUP ? ((BF16W ? 0 : kNumDqWarps) + kNumAWarps) : (BF16W ? 1 : kNumDqWarps));
       mbar_init(empty(s), 1);
       mbar_init(afull(s), 1);
     }
@@ -253,6 +261,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
         for (int ks = 0; ks < KS; ++ks, ++it) {
           const int s = it % kStages, cs = it % kCStages;
           const uint32_t ph = (it / kStages) & 1u, cph = (it / kCStages) & 1u;
+          if (BF16W) {
+            // the weight stage (and the h rows for down) straight from memory
+            if (!(ok = mbar_wait(empty(s), ph ^ 1u, abort_flag, a.hdr))) break;
+            mbar_arrive_tx(afull(s), kBBytes + (GATEUP ? 0u : kABytes));
+            const uint32_t bdst = base + kOffB + s * kBBytes;
+            const int row = GATEUP ? ex * a.I + j * 128 : ex * a.D + j * BN;
+            tma_load_2d(bdst, sh ? &maps.cs0 : &maps.c0, ks * BK, row, afull(s));
+            if (GATEUP)
+              tma_load_2d(bdst + kBBytes / 2, sh ? &maps.cs1 : &maps.c1, ks * BK, row, afull(s));
+            else
+              tma_load_2d(bdst + kBBytes / 2, sh ? &maps.cs0 : &maps.c0, ks * BK, row + 128, afull(s));
+            if (!GATEUP) tma_load_2d(base + kOffA + s * kABytes, &maps.a, ks * BK, p0, afull(s));
+            a_issued = it + 1;
+            continue;
+          }
           if (!(ok = mbar_wait(cempty(cs), cph ^ 1u, abort_flag, a.hdr))) break;
           const uint32_t cdst = base + kOffC + cs * kCBytes;
           mbar_arrive_tx(cfull(cs), kCBytes);
@@ -299,8 +322,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
         for (int ks = 0; ks < KS; ++ks, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          if (!(ok = mbar_wait(full(s), ph, abort_flag, a.hdr))) break;
-          if (!GATEUP && !(ok = mbar_wait(afull(s), ph, abort_flag, a.hdr))) break;
+          if ((GATEUP || !BF16W) && !(ok = mbar_wait(full(s), ph, abort_flag, a.hdr))) break;
+          if ((!GATEUP || BF16W) && !(ok = mbar_wait(afull(s), ph, abort_flag, a.hdr))) break;
           tc_fence_after();
           const uint32_t sa = base + kOffA + s * kABytes, sb = base + kOffB + s * kBBytes;
 #pragma unroll
@@ -355,7 +378,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tc_kernel(const TcArgs ar
       for (uint32_t q = it - pending; q < it; ++q)
         if (lane == 0) mbar_arrive(full(q % kStages));
     }
-  } else if (warp >= kWarpDq0 && warp < kWarpDq0 + kNumDqWarps) {
+  } else if (!BF16W && warp >= kWarpDq0 && warp < kWarpDq0 + kNumDqWarps) {
     // ---------------- dequantisation: B operand ----------------
     const int r = threadIdx.x - kWarpDq0 * 32;  // weight row 0..255 of the tile
     const bool vec_sb = (K / 64) % 8 == 0;
@@ -545,6 +568,36 @@ __global__ void debug_dequant_kernel(moe_qmatrix m, int expert, int rows, int K,
   }
 }
 
+// The separate expansion pass: the matrices of expert blockIdx.y to bf16,
+// each weight rounded once from s * q + b as the fused kernels round it. A
+// thread takes four consecutive code words (32 weights of one quantisation
+// group: K is a multiple of 64, so four-word runs never straddle a group) in
+// one 16-byte load and writes 64 bytes. count: skip experts no row selected
+// (null: all).
+__global__ void expand_weights_kernel(moe_qmatrix m, int rows, int K, const int32_t* count, uint16_t* out) {
+  const int e = blockIdx.y;
+  if (count && count[e] == 0) return;
+  const int quads = K / 32;  // four-word runs per row
+  const size_t n = size_t(rows) * quads;
+  const size_t row0 = size_t(e) * rows;
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x) {
+    const size_t row = row0 + i / quads;
+    const int qi = int(i % quads);
+    const uint4 w = *reinterpret_cast<const uint4*>(m.codes + row * (K / 8) + size_t(qi) * 4);
+    const uint16_t sc = m.scales[row * (K / 64) + qi / 2], bi = m.biases[row * (K / 64) + qi / 2];
+    const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16(sc), __ushort_as_bfloat16(sc));
+    const __nv_bfloat162 b2 = __halves2bfloat162(__ushort_as_bfloat16(bi), __ushort_as_bfloat16(bi));
+    uint32_t o[4][4];
+    dq8_bf16(w.x, s2, b2, o[0]);
+    dq8_bf16(w.y, s2, b2, o[1]);
+    dq8_bf16(w.z, s2, b2, o[2]);
+    dq8_bf16(w.w, s2, b2, o[3]);
+    uint4* dst = reinterpret_cast<uint4*>(out + row * K + size_t(qi) * 32);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dst[c] = make_uint4(o[c][0], o[c][1], o[c][2], o[c][3]);
+  }
+}
+
 }  // namespace
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -596,10 +649,49 @@ cudaError_t debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, uin
 
 bool gemm_tc_supported(const Ctx& c) { return c.I % 128 == 0 && c.D % BN == 0 && encoder() != nullptr; }
 
-cudaError_t gemm_tc(const Ctx& c) {
+ExpandedWeights expanded_weights(const moe_weights* w, void* base) {
+  ExpandedWeights x;
+  const size_t gu = size_t(w->I) * w->D;  // elements of one expert's gate (or up, or down) matrix
+  uint16_t* p = static_cast<uint16_t*>(base);
+  x.gate = p;
+  x.up = x.gate + size_t(w->E) * gu;
+  x.down = x.up + size_t(w->E) * gu;
+  x.s_gate = x.down + size_t(w->E) * gu;
+  x.s_up = x.s_gate + gu;
+  x.s_down = x.s_up + gu;
+  x.bytes = (size_t(3) * w->E + 3) * gu * 2;
+  return x;
+}
+
+cudaError_t expand_weights(const Ctx& c) {
   const moe_weights* w = c.w;
-  if (!ensure_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel<true>), int(kSmemBytes)) ||
-      !ensure_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel<false>), int(kSmemBytes)))
+  const ExpandedWeights& x = c.wexp;
+  const dim3 blk(256);
+  // about four waves of CTAs over the routed experts' matrices
+  const int per_e = std::max(1, 4 * num_sms() * 4 / std::max(1, c.E));
+  struct Job {
+    const moe_qmatrix* m;
+    int rows, K, n;
+    const int32_t* count;
+    uint16_t* out;
+  } jobs[6] = {{&w->gate, c.I, c.D, c.E, c.count, x.gate},   {&w->up, c.I, c.D, c.E, c.count, x.up},
+               {&w->down, c.D, c.I, c.E, c.count, x.down},   {&w->s_gate, c.I, c.D, 1, nullptr, x.s_gate},
+               {&w->s_up, c.I, c.D, 1, nullptr, x.s_up},     {&w->s_down, c.D, c.I, 1, nullptr, x.s_down}};
+  for (const Job& j : jobs) {
+    const dim3 grid(j.n == 1 ? 4 * num_sms() : per_e, j.n);
+    expand_weights_kernel<<<grid, blk, 0, c.stream>>>(*j.m, j.rows, j.K, j.count, j.out);
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    launch_done(c, "expand_weights");
+  }
+  return cudaSuccess;
+}
+
+template <bool BF16W>
+static cudaError_t gemm_tc_run(const Ctx& c) {
+  const moe_weights* w = c.w;
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel<true, BF16W>), int(kSmemBytes)) ||
+      !ensure_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel<false, BF16W>), int(kSmemBytes)))
     return cudaErrorInvalidValue;
   const int A = c.T * c.k;
   TcArgs a{c.x,      w->gate,   w->up,      w->s_gate, w->s_up, c.blocks, c.n_blocks, c.perm,
@@ -607,34 +699,42 @@ cudaError_t gemm_tc(const Ctx& c) {
            c.I,      c.max_blocks, (long long)c.opt.test_wait_cycles};
   TcMaps maps;
   std::memset(&maps, 0, sizeof(maps));
-  const auto U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
-  const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
-  bool ok = make_tmap_2d(&maps.c0, U32, 4, w->gate.codes, uint64_t(c.E) * c.I, c.D / 8, 8, 128, NOSW) &&
-            make_tmap_2d(&maps.c1, U32, 4, w->up.codes, uint64_t(c.E) * c.I, c.D / 8, 8, 128, NOSW) &&
-            make_tmap_2d(&maps.cs0, U32, 4, w->s_gate.codes, c.I, c.D / 8, 8, 128, NOSW) &&
-            make_tmap_2d(&maps.cs1, U32, 4, w->s_up.codes, c.I, c.D / 8, 8, 128, NOSW);
+  const auto U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32, BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE, SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  const ExpandedWeights& x = c.wexp;
+  bool ok = BF16W ? make_tmap_2d(&maps.c0, BF16, 2, x.gate, uint64_t(c.E) * c.I, c.D, BK, 128, SW) &&
+                        make_tmap_2d(&maps.c1, BF16, 2, x.up, uint64_t(c.E) * c.I, c.D, BK, 128, SW) &&
+                        make_tmap_2d(&maps.cs0, BF16, 2, x.s_gate, c.I, c.D, BK, 128, SW) &&
+                        make_tmap_2d(&maps.cs1, BF16, 2, x.s_up, c.I, c.D, BK, 128, SW)
+                  : make_tmap_2d(&maps.c0, U32, 4, w->gate.codes, uint64_t(c.E) * c.I, c.D / 8, 8, 128, NOSW) &&
+                        make_tmap_2d(&maps.c1, U32, 4, w->up.codes, uint64_t(c.E) * c.I, c.D / 8, 8, 128, NOSW) &&
+                        make_tmap_2d(&maps.cs0, U32, 4, w->s_gate.codes, c.I, c.D / 8, 8, 128, NOSW) &&
+                        make_tmap_2d(&maps.cs1, U32, 4, w->s_up.codes, c.I, c.D / 8, 8, 128, NOSW);
   if (!ok) return cudaErrorInvalidValue;
 
   cudaError_t err = c.yacc_zeroed ? cudaSuccess : zero_yacc(c);
   if (err != cudaSuccess) return err;
   const int grid1 = std::max(1, std::min(num_sms(), c.max_blocks * (c.I / 128)));
-  gemm_tc_kernel<true><<<grid1, kNumThreads, kSmemBytes, c.stream>>>(a, maps);
+  gemm_tc_kernel<true, BF16W><<<grid1, kNumThreads, kSmemBytes, c.stream>>>(a, maps);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done(c, "gateup_tc");
 
   a.m0 = w->down;
   a.s0 = w->s_down;
   std::memset(&maps, 0, sizeof(maps));
-  ok = make_tmap_2d(&maps.c0, U32, 4, w->down.codes, uint64_t(c.E) * c.D, c.I / 8, 8, BN, NOSW) &&
-       make_tmap_2d(&maps.cs0, U32, 4, w->s_down.codes, c.D, c.I / 8, 8, BN, NOSW) &&
-       make_tmap_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.h, uint64_t(A + c.T), c.I, BK, kTileRows,
-                CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = (BF16W ? make_tmap_2d(&maps.c0, BF16, 2, x.down, uint64_t(c.E) * c.D, c.I, BK, 128, SW) &&
+                    make_tmap_2d(&maps.cs0, BF16, 2, x.s_down, c.D, c.I, BK, 128, SW)
+              : make_tmap_2d(&maps.c0, U32, 4, w->down.codes, uint64_t(c.E) * c.D, c.I / 8, 8, BN, NOSW) &&
+                    make_tmap_2d(&maps.cs0, U32, 4, w->s_down.codes, c.D, c.I / 8, 8, BN, NOSW)) &&
+       make_tmap_2d(&maps.a, BF16, 2, c.h, uint64_t(A + c.T), c.I, BK, kTileRows, SW);
   if (!ok) return cudaErrorInvalidValue;
   const int grid2 = std::max(1, std::min(num_sms(), c.max_blocks * (c.D / BN)));
-  gemm_tc_kernel<false><<<grid2, kNumThreads, kSmemBytes, c.stream>>>(a, maps);
+  gemm_tc_kernel<false, BF16W><<<grid2, kNumThreads, kSmemBytes, c.stream>>>(a, maps);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   launch_done(c, "down_tc");
   return cast_y(c);
 }
+
+cudaError_t gemm_tc(const Ctx& c) { return c.wexp.gate ? gemm_tc_run<true>(c) : gemm_tc_run<false>(c); }
 
 }  // namespace moe

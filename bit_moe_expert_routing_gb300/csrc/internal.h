@@ -37,6 +37,20 @@ struct Options {
 };
 Options options_snapshot();
 
+// Every expert's weights expanded to bf16 by a separate pass before the
+// GEMMs (the unfused design, kept for comparison): [E][I][D] gate and up,
+// [E][D][I] down, then the shared expert's three matrices, in one buffer.
+struct ExpandedWeights {
+  uint16_t* gate = nullptr;  // null: the kernels dequantise on chip
+  uint16_t* up = nullptr;
+  uint16_t* down = nullptr;
+  uint16_t* s_gate = nullptr;
+  uint16_t* s_up = nullptr;
+  uint16_t* s_down = nullptr;
+  size_t bytes = 0;
+};
+ExpandedWeights expanded_weights(const moe_weights* w, void* base);
+
 // One call's resolved sizes and device pointers.
 struct Ctx {
   Options opt;      // the call's options
@@ -68,6 +82,7 @@ struct Ctx {
   uint16_t* xperm_area = nullptr;  // its place in the workspace
   cudaStream_t stream;
   bool yacc_zeroed = false;  // set when routing already cleared y_acc
+  ExpandedWeights wexp;      // set: the separate expansion pass and bf16-weight GEMMs
   // x still arriving from the host on another stream: rows before
   // x_slice_end[i] are in place once x_ready[i] has completed (the last slice
   // ends at T). The router starts on each slice as it lands; every other
@@ -103,6 +118,9 @@ cudaError_t cast_y(const Ctx& c);
 cudaError_t gemm_simt(const Ctx& c);
 cudaError_t gemm_tc(const Ctx& c);
 bool gemm_tc_supported(const Ctx& c);
+// The separate pass: the weights of every expert with rows in this pass, and
+// the shared expert's, to bf16 in c.wexp.
+cudaError_t expand_weights(const Ctx& c);
 cudaError_t gemm_wt(const Ctx& c);
 bool gemm_wt_supported(const Ctx& c);
 bool gemm_wt_small_supported(const Ctx& c);
@@ -144,8 +162,11 @@ void reset_launch_count();
 
 // The layer over T tokens as consecutive passes of at most `pass_tokens`
 // tokens, all reusing one workspace laid out for a pass (the body of the
-// workspace entry points). Counts the call's launches from zero.
+// workspace entry points). Counts the call's launches from zero. With
+// `wexp` set, every pass takes the shared-memory tensor-core GEMM path with
+// the separate expansion pass (see ExpandedWeights).
 moe_status forward_passes(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* workspace,
-                          size_t workspace_bytes, void* stream, int pass_tokens, const Options& opt);
+                          size_t workspace_bytes, void* stream, int pass_tokens, const Options& opt,
+                          const ExpandedWeights* wexp = nullptr);
 
 }  // namespace moe

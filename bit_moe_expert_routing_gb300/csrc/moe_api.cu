@@ -290,7 +290,7 @@ moe_status moe_workspace_view(const moe_weights* w, int T, void* workspace, size
 static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* workspace,
                                size_t workspace_bytes, void* stream, const Options& opt, bool first_pass,
                                int n_x_slices = 0, const int* x_slice_end = nullptr,
-                               const cudaEvent_t* x_ready = nullptr) {
+                               const cudaEvent_t* x_ready = nullptr, const ExpandedWeights* wexp = nullptr) {
   Ctx c;
   if (moe_status s = make_ctx(w, x, T, y, workspace, workspace_bytes, stream, opt, &c)) return s;
   if (T == 0) return MOE_OK;
@@ -298,7 +298,13 @@ static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, u
   c.n_x_slices = n_x_slices;
   c.x_slice_end = x_slice_end;
   c.x_ready = x_ready;
-  const Path path = plan(c);
+  Path path = plan(c);
+  if (wexp) {  // the unfused form: always the shared-memory tensor-core GEMMs
+    if (!gemm_tc_supported(c)) return MOE_ERR_ARG;
+    path = Path::GemmTc;
+    c.BM = c.opt.block_m > 0 ? std::min(c.opt.block_m, kTcBlockRows) : kTcBlockRows;
+    c.wexp = *wexp;
+  }
   if (path == Path::GemmWt) c.xperm = c.xperm_area;  // the router writes the paired-order x it gathers
   timing_begin(c);
   if (path == Path::DecodeFused || path == Path::DecodeRows) {  // routing included
@@ -318,6 +324,7 @@ static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, u
     if (*nb_host < 0 || *nb_host > c.max_blocks) return MOE_ERR_CUDA;
   }
   if (path == Path::Gemv) return cuda_status(gemv(c));
+  if (c.wexp.gate && expand_weights(c) != cudaSuccess) return MOE_ERR_CUDA;
   if (path == Path::GemmWt) return cuda_status(gemm_wt(c));
   if (path == Path::GemmTc) return cuda_status(gemm_tc(c));
   return cuda_status(gemm_simt(c));
@@ -326,14 +333,16 @@ static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, u
 }  // extern "C"
 
 moe_status moe::forward_passes(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* workspace,
-                               size_t workspace_bytes, void* stream, int step, const Options& opt) {
+                               size_t workspace_bytes, void* stream, int step, const Options& opt,
+                               const ExpandedWeights* wexp) {
   t_launches = 0;
   if (T == 0) return forward_pass(w, x, 0, y, workspace, workspace_bytes, stream, opt, true);  // checks the workspace
   if (!x || !y || !aligned16(x) || !aligned16(y) || x == y || step < 1) return MOE_ERR_ARG;
   for (int t0 = 0; t0 < T; t0 += step) {
     const int n = std::min(step, T - t0);
     const size_t at = size_t(t0) * w->D;
-    if (moe_status s = forward_pass(w, x + at, n, y + at, workspace, workspace_bytes, stream, opt, t0 == 0))
+    if (moe_status s = forward_pass(w, x + at, n, y + at, workspace, workspace_bytes, stream, opt, t0 == 0, 0,
+                                    nullptr, nullptr, wexp))
       return s;
   }
   return MOE_OK;
@@ -352,6 +361,26 @@ moe_status moe_layer_forward(const moe_weights* w, const uint16_t* x, int T, uin
   if (moe_status s = check_weights(w)) return s;
   if (T < 0 || T > kMaxT) return MOE_ERR_ARG;
   return forward_passes(w, x, T, y, workspace, workspace_bytes, stream, pass_tokens(T, opt), opt);
+}
+
+size_t moe_expanded_weights_bytes(const moe_weights* w) {
+  if (check_weights(w) != MOE_OK) return 0;
+  return expanded_weights(w, nullptr).bytes;
+}
+
+// The unfused design ("Optimizing on-device inference for Apple Silicon",
+// section "Dequantise weights during matrix multiplication", which measures
+// fusing the two): routing, a pass that expands the weights of every
+// selected expert and of the shared expert to bf16 in `wbuf`, then grouped
+// GEMMs that read those bf16 weights.
+moe_status moe_layer_forward_expanded(const moe_weights* w, const uint16_t* x, int T, uint16_t* y, void* workspace,
+                                      size_t workspace_bytes, void* wbuf, size_t wbuf_bytes, void* stream) {
+  const Options opt = options_snapshot();
+  if (moe_status s = check_weights(w)) return s;
+  if (T < 0 || T > kMaxT) return MOE_ERR_ARG;
+  const ExpandedWeights ex = expanded_weights(w, wbuf);
+  if (T > 0 && (!wbuf || (reinterpret_cast<uintptr_t>(wbuf) & 255) != 0 || wbuf_bytes < ex.bytes)) return MOE_ERR_ARG;
+  return forward_passes(w, x, T, y, workspace, workspace_bytes, stream, pass_tokens(T, opt), opt, &ex);
 }
 
 // The host entry point's copy stream and events, one set per thread and

@@ -255,6 +255,30 @@ moe_status moe_kernel_times(const char** names, float* total_ms, int* launches, 
 moe_status moe_debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, uint16_t* out,
                              void* stream);
 
+/* The unfused design, for measuring what fusing dequantisation into the
+ * GEMMs saves ("Optimizing on-device inference for Apple Silicon", section
+ * "Dequantise weights during matrix multiplication", which compares a fused
+ * kernel against a separate dequantisation pass plus GEMM). The layer as in
+ * moe_layer_forward(), computed as: routing; a pass that expands the
+ * weights of every expert that some row of the pass selected, and the
+ * shared expert's, to bf16 in `wbuf` (each weight rounded once from
+ * scale*code + bias, as the fused kernels round it); then the
+ * shared-memory tensor-core grouped GEMMs reading those bf16 weights
+ * through TMA. The output equals the fused shared-memory tensor-core path's
+ * (MOE_OPT_GEMM_IMPL = 2) bit for bit.
+ *   wbuf: device buffer of at least moe_expanded_weights_bytes(w) bytes,
+ *   256-byte aligned, owned by the caller: [E][I][D] gate, [E][I][D] up,
+ *   [E][D][I] down, then the shared expert's [I][D] gate, [I][D] up and
+ *   [D][I] down, all bf16. Only selected experts' parts are written.
+ *   workspace, x, y, stream, passes and T = 0: as for moe_layer_forward().
+ *   Errors: MOE_ERR_ARG for a missing, unaligned or short wbuf or a shape
+ *   the shared-memory GEMM does not take (I % 128 or D % 256 nonzero);
+ *   otherwise as moe_layer_forward(). */
+size_t moe_expanded_weights_bytes(const moe_weights* w);
+moe_status moe_layer_forward_expanded(const moe_weights* w, const uint16_t* x, int T, uint16_t* y,
+                                      void* workspace, size_t workspace_bytes, void* wbuf,
+                                      size_t wbuf_bytes, void* stream);
+
 /* Bytes of the library's fixed device scratch array used by
  * moe_layer_forward_static(). */
 #define MOE_STATIC_SCRATCH_BYTES (8u << 20)

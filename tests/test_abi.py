@@ -89,6 +89,24 @@ def test_static_entry_point_host_checks(lib):
     assert lib.moe_layer_forward_static(None, 0x2000, 4, 0x3000, None) == moe.MOE_ERR_ARG
 
 
+def test_expanded_entry_point_host_checks(lib):
+    # the unfused form's buffer size and its host-side argument checks
+    w = _weights(D=256, E=16, k=2, I=128)
+    nb = moe.moe_expanded_weights_bytes(w)
+    assert nb == (3 * 16 + 3) * 128 * 256 * 2  # E x (gate, up, down) + the shared expert's three, bf16
+    assert moe.moe_expanded_weights_bytes(_weights(D=100)) == 0
+    ws, wsn = 1 << 30, moe.moe_workspace_size(w, 4)
+    wb = 1 << 34
+    assert moe.moe_layer_forward_expanded(w, 0x2000, 4, 0x3000, ws, wsn, None, nb, None) == moe.MOE_ERR_ARG
+    assert moe.moe_layer_forward_expanded(w, 0x2000, 4, 0x3000, ws, wsn, wb + 16, nb, None) == moe.MOE_ERR_ARG
+    assert moe.moe_layer_forward_expanded(w, 0x2000, 4, 0x3000, ws, wsn, wb, nb - 1, None) == moe.MOE_ERR_ARG
+    assert moe.moe_layer_forward_expanded(w, 0x2000, -1, 0x3000, ws, wsn, wb, nb, None) == moe.MOE_ERR_ARG
+    assert moe.moe_layer_forward_expanded(_weights(D=100), 0x2000, 4, 0x3000, ws, wsn, wb, nb, None) == \
+        moe.MOE_ERR_SHAPE
+    # an empty call is a no-op
+    assert moe.moe_layer_forward_expanded(w, None, 0, None, ws, wsn, None, 0, None) == moe.MOE_OK
+
+
 def test_workspace_view_layout(lib):
     w = _weights(D=256, E=16, k=2, I=128)
     T = 37

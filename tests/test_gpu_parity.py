@@ -423,6 +423,51 @@ def test_layer_prefill4096_zipf_sampled_cuda_core():
     assert np.isfinite(y).all()
 
 
+@pytest.mark.parametrize("name", ["tiny", "prefill512"])
+def test_layer_expanded_weights_matches_fused(name):
+    # The unfused form (a separate pass expands the selected experts' weights
+    # to bf16, then the GEMMs read them) against the fused shared-memory
+    # GEMM: the same weights rounded the same way, so h is identical bit for
+    # bit (y differs only in the order of its fp32 atomic adds); the output
+    # matches the oracle; and a selected expert's expanded matrices equal
+    # moe_debug_dequant's.
+    layer, x = config(name)
+    dl = dev_layer(name, layer)
+    T, k, I, D, E = x.shape[0], layer.k, layer.I, layer.D, layer.E
+    y_fused, ws_f = run_forward(dl, x, moe.PATH_GEMM, moe.GEMM_TENSOR_CORE_SMEM)
+    n_fused = moe.moe_last_launch_count()
+    v = dl.view(T, ws_f)
+    h_fused = moe.ws_tensor(ws_f, v.h, (T * k + T, I), torch.int16).clone()
+    xd = x_to_device(x)
+    ws = dl.workspace(T)
+    nb = moe.moe_expanded_weights_bytes(dl.w)
+    wbuf = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(xd)
+    st = moe.moe_layer_forward_expanded(dl.w, xd.data_ptr(), T, y.data_ptr(), ws.data_ptr(), ws.numel(),
+                                        wbuf.data_ptr(), nb, None)
+    assert st == moe.MOE_OK, moe.moe_status_string(st)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ctypes.c_void_p(ws.data_ptr()), None) == moe.MOE_OK
+    assert moe.moe_last_launch_count() == n_fused + 6  # the same kernels plus six expansion launches
+    v = dl.view(T, ws)
+    h = moe.ws_tensor(ws, v.h, (T * k + T, I), torch.int16)
+    assert torch.equal(h, h_fused)
+    yn = bf16_to_np(y)
+    assert np.allclose(yn, y_fused, rtol=2 ** -7, atol=1e-6)
+    check_output(yn, O.forward(O.OracleLayer(layer), x), f"expanded weights {name}")
+    # one selected expert's matrices and the shared expert's down matrix
+    idx = moe.ws_tensor(ws, v.topk_idx, (T, k), torch.int32).cpu().numpy()
+    e = int(idx[0, 0])
+    wb = wbuf.view(torch.int16)
+    gu = I * D
+    for m, ex, off, rows, K in ((dl.w.gate, e, e * gu, I, D), (dl.w.up, e, (E + e) * gu, I, D),
+                                (dl.w.down, e, (2 * E + e) * gu, D, I), (dl.w.s_down, 0, (3 * E + 2) * gu, D, I)):
+        want = torch.empty(rows * K, dtype=torch.int16, device="cuda")
+        assert moe.moe_debug_dequant(m, ex, rows, K, want.data_ptr(), None) == moe.MOE_OK
+        torch.cuda.synchronize()
+        assert torch.equal(wb[off:off + rows * K], want)
+
+
 def test_intermediate_h_matches_oracle():
     layer, x = config("tiny")
     dl = dev_layer("tiny", layer)
