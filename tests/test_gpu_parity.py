@@ -413,6 +413,23 @@ def test_layer_prefill4096_zipf_all_tokens():
         check_output(y[t0:t0 + 256], ref[t0:t0 + 256], f"prefill4096 tokens {t0}..{t0 + 255}")
 
 
+def test_layer_prefill4096_zipf_repeated_calls():
+    # An ordering race between the MMA issuer and the epilogue corrupted about
+    # one down launch in four before it was fixed: repeated calls on the same
+    # workspace must all match the oracle.
+    layer, x = config("prefill4096_zipf")
+    dl = dev_layer("prefill4096_zipf", layer)
+    ref = _prefill4096_reference()
+    moe.moe_set_option(moe.MOE_OPT_FORCE_PATH, moe.PATH_GEMM)
+    moe.moe_set_option(moe.MOE_OPT_GEMM_IMPL, moe.GEMM_TENSOR_CORE)
+    xd = x_to_device(x)
+    ws = dl.workspace(x.shape[0])
+    for i in range(8):
+        y = bf16_to_np(dl.forward(xd, workspace=ws))
+        assert moe.moe_get_device_status(ctypes.c_void_p(ws.data_ptr()), None) == moe.MOE_OK
+        check_output(y, ref, f"prefill4096 call {i}")
+
+
 def test_layer_prefill4096_zipf_sampled_cuda_core():
     layer, x = config("prefill4096_zipf")
     y, _ = run_forward(dev_layer("prefill4096_zipf", layer), x, moe.PATH_GEMM, moe.GEMM_CUDA_CORE)
