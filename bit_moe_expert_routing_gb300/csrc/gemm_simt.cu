@@ -13,6 +13,7 @@
 // never exist expanded in global memory.
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -180,6 +181,7 @@ __global__ void zero_f32_kernel(float4* p, size_t n4) {
 }
 
 __global__ void cast_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
+  griddep_wait();  // the down projection's accumulator
   for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n4; i += size_t(gridDim.x) * blockDim.x) {
     const float4 v = src[i];
     dst[i] = make_uint2(uint32_t(f32_to_bf16(v.x)) | (uint32_t(f32_to_bf16(v.y)) << 16),
@@ -197,9 +199,8 @@ cudaError_t zero_yacc(const Ctx& c) {
 
 cudaError_t cast_y(const Ctx& c) {
   const size_t n4 = size_t(c.T) * c.D / 4;
-  cast_bf16_kernel<<<4 * 152, 256, 0, c.stream>>>(reinterpret_cast<const float4*>(c.y_acc),
-                                                  reinterpret_cast<uint2*>(c.y), n4);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(c, cast_bf16_kernel, dim3(4 * 152), dim3(256), 0,
+                               reinterpret_cast<const float4*>(c.y_acc), reinterpret_cast<uint2*>(c.y), n4);
   if (err == cudaSuccess) launch_done(c, "cast_y");
   return err;
 }

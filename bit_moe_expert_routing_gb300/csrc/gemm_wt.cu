@@ -332,6 +332,13 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched as a programmatic dependent of the previous kernel: gate/up reads
+  // the routing tables and the paired-order x, so every thread waits here for
+  // that kernel; down reads only h from its predecessor (gate/up), so only the
+  // thread that loads h waits (below), and the rest of its CTA sets up, loads
+  // and dequantises its first weight stages during gate/up's last tiles.
+  if (GATEUP) griddep_wait();
+  griddep_launch();
 
   int nb = *a.n_blocks;
   if (nb > a.max_blocks || nb < 0) {
@@ -557,7 +564,8 @@ __global__ void __launch_bounds__(C::kNumThreads, 1) gemm_wt_kernel(const WtArgs
       }
       cp_async_wait<0>();
     } else if (bt == 0) {
-      // down: rows p0.. of h as one 2-D TMA tile per k-step
+      // down: rows p0.. of h as one 2-D TMA tile per k-step, once gate/up is done
+      griddep_wait();
       uint32_t it = 0, issued = 0;
       bool ok = true;
       TileEntry nx = entry_load(blockIdx.x);
@@ -851,8 +859,9 @@ cudaError_t gemm_wt_run(const Ctx& c) {
   cudaError_t err = c.yacc_zeroed ? cudaSuccess : zero_yacc(c);
   if (err != cudaSuccess) return err;
   const int grid1 = std::max(1, std::min(num_sms(), c.max_blocks * (c.I / 64)));
-  gemm_wt_kernel<true, C><<<grid1, C::kNumThreads, C::kSmemBytes, c.stream>>>(a, maps);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if ((err = launch_pdl(c, gemm_wt_kernel<true, C>, dim3(grid1), dim3(C::kNumThreads), C::kSmemBytes, a, maps)) !=
+      cudaSuccess)
+    return err;
   launch_done(c, "gateup_tc");
 
   a.m0 = w->down;
@@ -864,8 +873,9 @@ cudaError_t gemm_wt_run(const Ctx& c) {
                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   const int grid2 = std::max(1, std::min(num_sms(), c.max_blocks * (c.D / WM)));
-  gemm_wt_kernel<false, C><<<grid2, C::kNumThreads, C::kSmemBytes, c.stream>>>(a, maps);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if ((err = launch_pdl(c, gemm_wt_kernel<false, C>, dim3(grid2), dim3(C::kNumThreads), C::kSmemBytes, a, maps)) !=
+      cudaSuccess)
+    return err;
   launch_done(c, "down_tc");
   return cast_y(c);
 }

@@ -1,6 +1,8 @@
 // Internal interface between the translation units of the MoE library.
 #pragma once
 
+#include <utility>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -25,7 +27,7 @@ constexpr int kMinBlockM = 16;      // smallest block size MOE_OPT_BLOCK_M accep
 // once when the call starts, so that another thread's moe_set_option cannot
 // change a call part-way.
 struct Options {
-  int gemv_max_rows = 4;  // the measured small-row sweep: GEMV at least as fast up to 4 rows, the GEMM from 5
+  int gemv_max_rows = 1;  // the measured small-row sweep: the grouped GEMM at least as fast from 2 rows
   int force_path = 0;
   int kernel_timing = 0;
   int gemm_impl = 0;
@@ -98,6 +100,24 @@ cudaError_t wait_x(const Ctx& c);
 // unit in which x slices are sized, so that no router launch ends in a
 // partial wave).
 int router_wave_tokens(int E);
+
+// Launches `kernel` on c.stream with programmatic stream serialisation: its
+// CTAs may start while the stream's previous kernel finishes, and wait
+// (griddep_wait in the kernel) before reading what that kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(const Ctx& c, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Bookkeeping of launches: counts this library's kernels and, when kernel
 // timing is on, records an event after each one.

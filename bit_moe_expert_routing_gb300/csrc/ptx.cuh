@@ -67,6 +67,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Programmatic dependent launch. A kernel launched with launch_pdl may start
+// while the previous kernel of its stream is finishing: griddep_wait() returns
+// once that kernel has completed and its memory writes are visible (at once
+// for a kernel launched the ordinary way); griddep_launch() lets the next
+// such kernel start. A kernel triggers only after its own wait, so a kernel
+// that starts early can rely on everything before its predecessor.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Contiguous global -> shared copy by the TMA engine; completes `bytes` of

@@ -208,6 +208,8 @@ __global__ void __launch_bounds__(kTopkThreads)
                      int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                      int32_t* __restrict__ chunk_count, int n_chunks, const uint16_t* __restrict__ x, int D,
                      uint16_t* __restrict__ xperm) {
+  griddep_wait();  // the logits
+  griddep_launch();
   if (int(blockIdx.x) >= n_chunks) {
     // CTAs past the chunks write the paired-order copy of x for the
     // tensor-memory gate/up GEMM (see permute_x_kernel), on SMs the top-k
@@ -291,6 +293,8 @@ __global__ void __launch_bounds__(1024)
                        int32_t* __restrict__ chunk, int32_t* __restrict__ count,
                        int32_t* __restrict__ off, int32_t* __restrict__ blocks,
                        int32_t* __restrict__ n_blocks, WsHeader* hdr) {
+  griddep_wait();  // the per-chunk counts
+  griddep_launch();
   __shared__ int s_warp[32];
   __shared__ int s_tot_rows, s_tot_blocks;
   const int e = threadIdx.x;
@@ -359,6 +363,8 @@ __global__ void __launch_bounds__(256)
     scatter_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
                    const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm,
                    int32_t* __restrict__ inv, WsHeader* hdr) {
+  griddep_wait();  // the chunk bases
+  griddep_launch();
   extern __shared__ int sm[];
   int* base = sm;      // [E]
   int* wh = sm + E;    // [8][E] per-warp counts of the current round
@@ -649,20 +655,20 @@ cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
     // with the paired-order copy of x to write, the SMs the chunks leave idle
     // (at least 16 CTAs) take it
     const int n_copy = c.xperm ? std::max(16, num_sms() - c.n_chunks) : 0;
-    tk<<<c.n_chunks + n_copy, kTopkThreads, c.E * sizeof(int), c.stream>>>(
-        c.logits, c.T, c.E, c.k, c.topk_idx, c.topk_w, c.chunk, c.n_chunks, c.x, c.D, c.xperm);
+    err = launch_pdl(c, tk, dim3(c.n_chunks + n_copy), dim3(kTopkThreads), c.E * sizeof(int), c.logits, c.T, c.E,
+                     c.k, c.topk_idx, c.topk_w, c.chunk, c.n_chunks, c.x, c.D, c.xperm);
   }
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (err != cudaSuccess) return err;
   launch_done(c, "topk_hist");
 
-  scan_blocks_kernel<<<1, 1024, 0, c.stream>>>(c.T, c.E, c.k, c.BM, c.n_chunks, c.max_blocks, c.chunk,
-                                               c.count, c.off, c.blocks, c.n_blocks, c.hdr);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  err = launch_pdl(c, scan_blocks_kernel, dim3(1), dim3(1024), 0, c.T, c.E, c.k, c.BM, c.n_chunks, c.max_blocks,
+                   c.chunk, c.count, c.off, c.blocks, c.n_blocks, c.hdr);
+  if (err != cudaSuccess) return err;
   launch_done(c, "scan_blocks");
 
-  scatter_kernel<<<c.n_chunks, 256, 9 * c.E * sizeof(int), c.stream>>>(c.topk_idx, c.T, c.E, c.k, c.chunk,
-                                                                       c.perm, c.inv, c.hdr);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  err = launch_pdl(c, scatter_kernel, dim3(c.n_chunks), dim3(256), 9 * c.E * sizeof(int), c.topk_idx, c.T, c.E,
+                   c.k, c.chunk, c.perm, c.inv, c.hdr);
+  if (err != cudaSuccess) return err;
   launch_done(c, "scatter");
   return cudaSuccess;
 }

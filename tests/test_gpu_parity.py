@@ -349,13 +349,16 @@ def test_layer_chunked_prefill(chunk, extra):
     dl = dev_layer("prefill512", layer)
     y_one, _ = run_forward(dl, x)
     old = moe.moe_get_option(moe.MOE_OPT_CHUNK_TOKENS)
+    old_rows = moe.moe_get_option(moe.MOE_OPT_GEMV_MAX_ROWS)
     try:
         assert moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, chunk) == moe.MOE_OK
+        assert moe.moe_set_option(moe.MOE_OPT_GEMV_MAX_ROWS, 4) == moe.MOE_OK  # the 3-token tail takes the GEMV path
         assert moe.moe_workspace_size(dl.w, T) == moe.moe_workspace_size(dl.w, chunk)
         y, _ = run_forward(dl, x)
         launches = moe.moe_last_launch_count()
     finally:
         moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, old)
+        moe.moe_set_option(moe.MOE_OPT_GEMV_MAX_ROWS, old_rows)
     assert launches > 8  # more than one pass ran
     # rows that took the same (GEMM) path in both runs agree up to summation
     # order; a GEMV tail pass rounds differently (fp32 weights) and is held to
@@ -682,8 +685,10 @@ def test_device_status_survives_later_passes():
     xd = x_to_device(x)
     ws = dl.workspace(x.shape[0])
     old = moe.moe_get_option(moe.MOE_OPT_CHUNK_TOKENS)
+    old_rows = moe.moe_get_option(moe.MOE_OPT_GEMV_MAX_ROWS)
     try:
         assert moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, 256) == moe.MOE_OK
+        assert moe.moe_set_option(moe.MOE_OPT_GEMV_MAX_ROWS, 4) == moe.MOE_OK  # the 3-token pass takes the GEMV path
         assert moe.moe_set_option(moe.MOE_OPT_FORCE_PATH, moe.PATH_AUTO) == moe.MOE_OK
         assert moe.moe_set_option(moe.MOE_OPT_TEST_WAIT_CYCLES, 20000) == moe.MOE_OK
         ws = dl.workspace(x.shape[0])
@@ -695,6 +700,7 @@ def test_device_status_survives_later_passes():
     finally:
         moe.moe_set_option(moe.MOE_OPT_TEST_WAIT_CYCLES, 0)
         moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, old)
+        moe.moe_set_option(moe.MOE_OPT_GEMV_MAX_ROWS, old_rows)
     check_output(y, O.forward(O.OracleLayer(layer), x), "after a timeout in an earlier pass")
 
 

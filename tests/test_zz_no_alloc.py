@@ -92,12 +92,15 @@ def test_static_status_keeps_an_earlier_pass_error():
     layer, x_bits = synth.make_config("prefill512", 453)
     dl = moe.DeviceLayer(layer)
     x = x_to_device(x_bits)
+    old_rows = moe.moe_get_option(moe.MOE_OPT_GEMV_MAX_ROWS)
+    assert moe.moe_set_option(moe.MOE_OPT_GEMV_MAX_ROWS, 4) == moe.MOE_OK  # the 2-token pass takes the GEMV path
     assert moe.moe_set_option(moe.MOE_OPT_TEST_WAIT_CYCLES, 20000) == moe.MOE_OK
     try:
         _static_forward(dl, x)
         st = moe.moe_get_device_status_static(None)
     finally:
         moe.moe_set_option(moe.MOE_OPT_TEST_WAIT_CYCLES, 0)
+        moe.moe_set_option(moe.MOE_OPT_GEMV_MAX_ROWS, old_rows)
     assert st == moe.MOE_ERR_DEVICE_TIMEOUT, moe.moe_status_string(st)
     assert moe.moe_get_device_status_static(None) == moe.MOE_OK  # read and cleared
     ref = bf16_to_np(dl.forward(x))
