@@ -428,6 +428,8 @@ __global__ void __launch_bounds__(kRouterSmallExperts * 32)
     router_small_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
                         const float* __restrict__ bias, int T, int D, int E, float* __restrict__ logits,
                         WsHeader* hdr, int clear_status) {
+  griddep_wait();  // launched as a programmatic dependent: everything before is done
+  griddep_launch();
   extern __shared__ __align__(128) uint8_t rsm[];
   const uint32_t bar = smem_u32(rsm);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(rsm + 8);
@@ -485,6 +487,8 @@ __global__ void __launch_bounds__(1024)
                        int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ count,
                        int32_t* __restrict__ off, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                        int32_t* __restrict__ blocks, int32_t* __restrict__ n_blocks, WsHeader* hdr) {
+  griddep_wait();  // the logits
+  griddep_launch();
   __shared__ int s_idx[kSmallRouteTokens * 32];
   __shared__ int s_cnt[1024];
   __shared__ int s_warp[32];
@@ -564,9 +568,9 @@ cudaError_t route_logits_small(const Ctx& c) {
       tt == 2 ? router_small_kernel<2> : tt == 8 ? router_small_kernel<8> : router_small_kernel<16>;
   const size_t smem = router_small_smem(tt, c.D);
   if (!ensure_smem_limit(reinterpret_cast<const void*>(rk), int(smem))) return cudaErrorInvalidValue;
-  rk<<<(c.E + kRouterSmallExperts - 1) / kRouterSmallExperts, kRouterSmallExperts * 32, smem, c.stream>>>(
-      c.x, w->router_w, w->router_bias, c.T, c.D, c.E, c.logits, c.hdr, c.first_pass ? 1 : 0);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(c, rk, dim3((c.E + kRouterSmallExperts - 1) / kRouterSmallExperts),
+                               dim3(kRouterSmallExperts * 32), smem, c.x, w->router_w, w->router_bias, c.T, c.D,
+                               c.E, c.logits, c.hdr, c.first_pass ? 1 : 0);
   if (err != cudaSuccess) return err;
   launch_done(c, "router_small");
   return cudaSuccess;
@@ -576,6 +580,8 @@ cudaError_t route_logits_small(const Ctx& c) {
 // path, whose router does not stage x: one 8-element chunk per thread.
 __global__ void __launch_bounds__(256) permute_x_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ xperm,
                                                         size_t n8) {
+  griddep_wait();  // launched as a programmatic dependent: everything before is done
+  griddep_launch();
   for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n8; i += size_t(gridDim.x) * blockDim.x) {
     const uint4 v = reinterpret_cast<const uint4*>(x)[i];
     const uint2 lo = make_uint2(v.x, v.y), hi = make_uint2(v.z, v.w);
@@ -605,9 +611,9 @@ cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
     if ((err = wait_x(c)) != cudaSuccess) return err;
     if (c.xperm) {
       const size_t n8 = size_t(c.T) * c.D / 8;
-      permute_x_kernel<<<unsigned(std::min<size_t>((n8 + 255) / 256, size_t(num_sms()))), 256, 0, c.stream>>>(
-          c.x, c.xperm, n8);
-      if ((err = cudaGetLastError()) != cudaSuccess) return err;
+      if ((err = launch_pdl(c, permute_x_kernel, dim3(unsigned(std::min<size_t>((n8 + 255) / 256, size_t(num_sms())))),
+                            dim3(256), 0, c.x, c.xperm, n8)) != cudaSuccess)
+        return err;
       launch_done(c, "permute_x");
     }
     if ((err = route_logits_small(c)) != cudaSuccess) return err;
@@ -615,10 +621,9 @@ cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
     void (*rs)(const float*, int, int, int, int, int, int32_t*, float*, int32_t*, int32_t*, int32_t*, int32_t*,
                int32_t*, int32_t*, WsHeader*) =
         mpl <= 4 ? route_small_kernel<4> : mpl <= 8 ? route_small_kernel<8> : route_small_kernel<16>;
-    rs<<<1, 1024, 0, c.stream>>>(c.logits, c.T, c.E, c.k, c.BM, c.max_blocks, c.topk_idx,
-                                                 c.topk_w, c.count, c.off, c.perm, c.inv, c.blocks, c.n_blocks,
-                                                 c.hdr);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if ((err = launch_pdl(c, rs, dim3(1), dim3(1024), 0, c.logits, c.T, c.E, c.k, c.BM, c.max_blocks, c.topk_idx,
+                          c.topk_w, c.count, c.off, c.perm, c.inv, c.blocks, c.n_blocks, c.hdr)) != cudaSuccess)
+      return err;
     launch_done(c, "route_small");
     return cudaSuccess;
   }
