@@ -164,7 +164,9 @@ bool decode_fused_supported(const Ctx& c);
 cudaError_t decode_rows(const Ctx& c);
 bool decode_rows_supported(const Ctx& c);
 // Router logits only, for up to 16 tokens.
-cudaError_t route_logits_small(const Ctx& c);
+// With xperm, it also writes the paired-order copy of x; with yacc, it clears
+// the combine accumulator [T, D].
+cudaError_t route_logits_small(const Ctx& c, uint16_t* xperm = nullptr, float* yacc = nullptr);
 
 cudaError_t debug_dequant(const moe_qmatrix* m, int expert, int rows, int K, uint16_t* out,
                           cudaStream_t s);

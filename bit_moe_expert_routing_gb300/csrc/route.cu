@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kTopkThreads)
   griddep_launch();
   if (int(blockIdx.x) >= n_chunks) {
     // CTAs past the chunks write the paired-order copy of x for the
-    // tensor-memory gate/up GEMM (see permute_x_kernel), on SMs the top-k
+    // tensor-memory gate/up GEMM (see dq8_bf16_paired), on SMs the top-k
     // leaves idle
     const size_t n8 = size_t(T) * D / 8, step = size_t(gridDim.x - n_chunks) * blockDim.x;
     for (size_t i = size_t(blockIdx.x - n_chunks) * blockDim.x + threadIdx.x; i < n8; i += step) {
@@ -427,7 +427,7 @@ template <int TT>
 __global__ void __launch_bounds__(kRouterSmallExperts * 32)
     router_small_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
                         const float* __restrict__ bias, int T, int D, int E, float* __restrict__ logits,
-                        WsHeader* hdr, int clear_status) {
+                        WsHeader* hdr, int clear_status, uint16_t* __restrict__ xperm, float4* __restrict__ yacc) {
   griddep_wait();  // launched as a programmatic dependent: everything before is done
   griddep_launch();
   extern __shared__ __align__(128) uint8_t rsm[];
@@ -449,11 +449,34 @@ __global__ void __launch_bounds__(kRouterSmallExperts * 32)
     mbar_arrive_tx(bar, uint32_t(ne) * D * 4);
     bulk_g2s(bar + 16, wr + size_t(e0) * D, uint32_t(ne) * D * 4, bar);
   }
+  // the token rows by cp.async, every copy of a thread in flight at once
+  // (rows past T, which the unrolled loop below also reads, are zeroed)
   for (int i = threadIdx.x; i < TT * (D / 8); i += blockDim.x) {
     const int t = i / (D / 8), c8 = i % (D / 8);
-    xsm4[i] = t < T ? *reinterpret_cast<const uint4*>(x + size_t(t) * D + c8 * 8) : make_uint4(0u, 0u, 0u, 0u);
+    if (t < T)
+      cp_async16_cg(smem_u32(xsm4 + i), x + size_t(t) * D + c8 * 8);
+    else
+      xsm4[i] = make_uint4(0u, 0u, 0u, 0u);
   }
+  cp_async_commit_all();
+  cp_async_wait_all();
   __syncthreads();
+  // For the tensor-memory GEMM that follows: the CTAs share out the
+  // paired-order copy of x (see dq8_bf16_paired), from the staged rows, and
+  // the clearing of the combine accumulator y_acc [T, D].
+  const size_t n8 = size_t(T) * (D / 8);
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += size_t(gridDim.x) * blockDim.x) {
+    if (xperm) {
+      const uint4 v = xsm4[i];
+      const uint2 lo = make_uint2(v.x, v.y), hi = make_uint2(v.z, v.w);
+      const uint2 pa = pair_order8_first(lo, hi), pb = pair_order8_second(lo, hi);
+      reinterpret_cast<uint4*>(xperm)[i] = make_uint4(pa.x, pa.y, pb.x, pb.y);
+    }
+    if (yacc) {  // y_acc holds 2 float4 per chunk of 8 columns
+      yacc[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      yacc[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   if (!mbar_wait(bar, 0, abort_flag, hdr, kWaitLimit, true)) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp >= ne) return;
@@ -560,34 +583,20 @@ __global__ void __launch_bounds__(1024)
 
 }  // namespace
 
-cudaError_t route_logits_small(const Ctx& c) {
+cudaError_t route_logits_small(const Ctx& c, uint16_t* xperm, float* yacc) {
   const moe_weights* w = c.w;
   if (c.T > kSmallRouteTokens || c.D > 4096) return cudaErrorInvalidValue;
   const int tt = c.T <= 2 ? 2 : c.T <= 8 ? 8 : 16;
-  void (*rk)(const uint16_t*, const float*, const float*, int, int, int, float*, WsHeader*, int) =
+  void (*rk)(const uint16_t*, const float*, const float*, int, int, int, float*, WsHeader*, int, uint16_t*, float4*) =
       tt == 2 ? router_small_kernel<2> : tt == 8 ? router_small_kernel<8> : router_small_kernel<16>;
   const size_t smem = router_small_smem(tt, c.D);
   if (!ensure_smem_limit(reinterpret_cast<const void*>(rk), int(smem))) return cudaErrorInvalidValue;
   cudaError_t err = launch_pdl(c, rk, dim3((c.E + kRouterSmallExperts - 1) / kRouterSmallExperts),
                                dim3(kRouterSmallExperts * 32), smem, c.x, w->router_w, w->router_bias, c.T, c.D,
-                               c.E, c.logits, c.hdr, c.first_pass ? 1 : 0);
+                               c.E, c.logits, c.hdr, c.first_pass ? 1 : 0, xperm, reinterpret_cast<float4*>(yacc));
   if (err != cudaSuccess) return err;
   launch_done(c, "router_small");
   return cudaSuccess;
-}
-
-// The paired-order copy of x (see dq8_bf16_paired) for the small-T routing
-// path, whose router does not stage x: one 8-element chunk per thread.
-__global__ void __launch_bounds__(256) permute_x_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ xperm,
-                                                        size_t n8) {
-  griddep_wait();  // launched as a programmatic dependent: everything before is done
-  griddep_launch();
-  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n8; i += size_t(gridDim.x) * blockDim.x) {
-    const uint4 v = reinterpret_cast<const uint4*>(x)[i];
-    const uint2 lo = make_uint2(v.x, v.y), hi = make_uint2(v.z, v.w);
-    const uint2 a = pair_order8_first(lo, hi), b = pair_order8_second(lo, hi);
-    reinterpret_cast<uint4*>(xperm)[i] = make_uint4(a.x, a.y, b.x, b.y);
-  }
 }
 
 int router_wave_tokens(int E) {
@@ -609,14 +618,10 @@ cudaError_t route(const Ctx& c, bool* yacc_zeroed) {
   // one CTA of 1024 threads does the small-T top-k: up to 16 logits per lane
   if (c.T <= kSmallRouteTokens && c.D <= 4096 && c.E <= 512) {
     if ((err = wait_x(c)) != cudaSuccess) return err;
-    if (c.xperm) {
-      const size_t n8 = size_t(c.T) * c.D / 8;
-      if ((err = launch_pdl(c, permute_x_kernel, dim3(unsigned(std::min<size_t>((n8 + 255) / 256, size_t(num_sms())))),
-                            dim3(256), 0, c.x, c.xperm, n8)) != cudaSuccess)
-        return err;
-      launch_done(c, "permute_x");
-    }
-    if ((err = route_logits_small(c)) != cudaSuccess) return err;
+    // the router also writes the paired-order x and, when the grouped GEMM
+    // follows, clears y_acc
+    if ((err = route_logits_small(c, c.xperm, yacc_zeroed ? c.y_acc : nullptr)) != cudaSuccess) return err;
+    if (yacc_zeroed) *yacc_zeroed = true;
     const int mpl = (c.E + 31) / 32;
     void (*rs)(const float*, int, int, int, int, int, int32_t*, float*, int32_t*, int32_t*, int32_t*, int32_t*,
                int32_t*, int32_t*, WsHeader*) =
