@@ -287,7 +287,7 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* s_total) {
 }
 
 // Totals, offsets, per-chunk bases and the block map. One CTA of 1024 threads;
-// thread e owns expert e (E <= 1024).
+// a group of adjacent threads owns each expert (E <= 1024).
 __global__ void __launch_bounds__(1024)
     scan_blocks_kernel(int T, int E, int k, int BM, int n_chunks, int max_blocks,
                        int32_t* __restrict__ chunk, int32_t* __restrict__ count,
@@ -295,41 +295,84 @@ __global__ void __launch_bounds__(1024)
                        int32_t* __restrict__ n_blocks, WsHeader* hdr) {
   griddep_wait();  // the per-chunk counts
   griddep_launch();
-  __shared__ int s_warp[32];
+  __shared__ int s_warp_rows[32], s_warp_blocks[32];
   __shared__ int s_tot_rows, s_tot_blocks;
-  const int e = threadIdx.x;
-  // the per-chunk counts of expert e are read kScanBatch at a time (independent
-  // loads in flight together): first for the total, then again to replace
-  // each by its base (the expert's offset plus the counts of earlier chunks)
-  constexpr int kScanBatch = 8;
-  int total = 0;
-  if (e < E) {
-    for (int c0 = 0; c0 < n_chunks; c0 += kScanBatch) {
-      int v[kScanBatch];
+  // tpe threads per expert (adjacent lanes, tpe a power of two dividing 32):
+  // thread q of expert e owns the chunks [c0, c1). Its counts are loaded in
+  // one batch and kept in registers for the second pass when they fit
+  // (kKeep), so the whole scan costs one round of dependent loads.
+  constexpr int kKeep = 32;
+  int tpe = 1;
+  while (tpe < 8 && 2 * tpe * E <= int(blockDim.x)) tpe *= 2;
+  const int e = threadIdx.x / tpe, q = threadIdx.x % tpe;
+  const bool mine = e < E;
+  const int per = (n_chunks + tpe - 1) / tpe;
+  const int c0 = min(n_chunks, q * per), c1 = min(n_chunks, c0 + per);
+  const bool keep = (c1 - c0) <= kKeep;
+  int v[kKeep];
+  int part = 0;
+  if (mine) {
+    if (keep) {
 #pragma unroll
-      for (int j = 0; j < kScanBatch; ++j) v[j] = c0 + j < n_chunks ? chunk[size_t(c0 + j) * E + e] : 0;
+      for (int j = 0; j < kKeep; ++j) v[j] = c0 + j < c1 ? chunk[size_t(c0 + j) * E + e] : 0;
 #pragma unroll
-      for (int j = 0; j < kScanBatch; ++j) total += v[j];
-    }
-  }
-  const int nb = (total + BM - 1) / BM;
-  const int ex_off = block_exclusive_scan(total, s_warp, &s_tot_rows);
-  const int ex_nb = block_exclusive_scan(nb, s_warp, &s_tot_blocks);
-  if (e < E) {
-    count[e] = total;
-    off[e] = ex_off;
-    int run = ex_off;
-    for (int c0 = 0; c0 < n_chunks; c0 += kScanBatch) {
-      int v[kScanBatch];
+      for (int j = 0; j < kKeep; ++j) part += v[j];
+    } else {
+      for (int c = c0; c < c1; c += 8) {
+        int w[8];
 #pragma unroll
-      for (int j = 0; j < kScanBatch; ++j) v[j] = c0 + j < n_chunks ? chunk[size_t(c0 + j) * E + e] : 0;
+        for (int j = 0; j < 8; ++j) w[j] = c + j < c1 ? chunk[size_t(c + j) * E + e] : 0;
 #pragma unroll
-      for (int j = 0; j < kScanBatch; ++j) {
-        if (c0 + j < n_chunks) chunk[size_t(c0 + j) * E + e] = run;
-        run += v[j];
+        for (int j = 0; j < 8; ++j) part += w[j];
       }
     }
-    for (int b = 0; b < nb; ++b) {
+  }
+  // the expert's total and this thread's offset inside it, over its group
+  int total = part, q_pre = part;
+  for (int o = 1; o < tpe; o <<= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+  for (int o = 1; o < tpe; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, q_pre, o);
+    if (q >= o) q_pre += u;
+  }
+  q_pre -= part;  // exclusive
+  const bool lead = mine && q == 0;
+  const int nb = lead ? (total + BM - 1) / BM : 0;
+  const int ex_off_l = block_exclusive_scan(lead ? total : 0, s_warp_rows, &s_tot_rows);
+  const int ex_nb_l = block_exclusive_scan(nb, s_warp_blocks, &s_tot_blocks);
+  // the group leader's scan results, to every thread of the group
+  const int src = (threadIdx.x & 31) & ~(tpe - 1);
+  const int ex_off = __shfl_sync(0xffffffffu, ex_off_l, src);
+  const int ex_nb = __shfl_sync(0xffffffffu, ex_nb_l, src);
+  const int nb_e = __shfl_sync(0xffffffffu, nb, src);
+  if (mine) {
+    if (q == 0) {
+      count[e] = total;
+      off[e] = ex_off;
+    }
+    // each chunk's count becomes its base: the expert's offset plus the
+    // counts of the expert's earlier chunks
+    int run = ex_off + q_pre;
+    if (keep) {
+#pragma unroll
+      for (int j = 0; j < kKeep; ++j)
+        if (c0 + j < c1) {
+          chunk[size_t(c0 + j) * E + e] = run;
+          run += v[j];
+        }
+    } else {
+      for (int c = c0; c < c1; c += 8) {
+        int w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = c + j < c1 ? chunk[size_t(c + j) * E + e] : 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (c + j < c1) {
+            chunk[size_t(c + j) * E + e] = run;
+            run += w[j];
+          }
+      }
+    }
+    for (int b = q; b < nb_e; b += tpe) {
       const int idx = ex_nb + b;
       if (idx < max_blocks) {
         blocks[3 * idx + 0] = e;
@@ -338,7 +381,7 @@ __global__ void __launch_bounds__(1024)
       }
     }
   }
-  if (e == 0) off[E] = s_tot_rows;
+  if (threadIdx.x == 0) off[E] = s_tot_rows;
   const int routed_blocks = s_tot_blocks;
   const int shared_blocks = (T + BM - 1) / BM;
   for (int s = threadIdx.x; s < shared_blocks; s += blockDim.x) {
