@@ -618,15 +618,15 @@ EncodeTiled encoder() {
 
 // 2-D tensor map over a row-major [rows, cols] array.
 bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t elem, const void* ptr, uint64_t rows, uint64_t cols,
-              uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+              uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw, CUtensorMapL2promotion l2) {
   EncodeTiled enc = encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * elem};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool tmap_encoder_available() { return encoder() != nullptr; }

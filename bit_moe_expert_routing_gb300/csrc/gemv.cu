@@ -284,44 +284,62 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_down_kernel(GemvArgs a) 
 }
 
 // ---------------------------------------------------------------------------
-// Fused decode for one token: router logits, top-k, gate/up + SwiGLU and
-// down + combine in one cooperative kernel.
-//   1. At once: each CTA bulk-copies its router rows (experts blockIdx.x +
-//      m * gridDim.x) and stages x.
+// Fused decode for one token: router logits, top-k, gate/up + SwiGLU and the
+// down projection in one cooperative kernel with a single grid barrier.
+//
+// A CTA owns one item: 32 consecutive intermediate rows of one expert slot
+// (slot j < k is the token's j-th expert, slot k the shared expert). It
+// computes those 32 values of h and multiplies them with the matching 32
+// columns of the expert's down matrix, which is its share of every output
+// value, and adds that share, times the routing weight, into the fp32
+// accumulator. So no CTA waits for another CTA's h.
+//   1. At entry: bulk copies of the CTA's router rows (experts blockIdx.x +
+//      m * gridDim.x). x is staged and the accumulator cleared.
 //   2. Logits of its experts in the canonical order; grid barrier.
 //   3. Every CTA takes the top-k of all logits itself (the same deterministic
-//      selection), then copies the rows of its two gate/up items (expert
-//      slot x 16 intermediate rows) and of its 16 output columns for all
-//      k+1 slots: codes by bulk copy, scales and biases by cp.async spread
-//      over the CTA; computes its h rows; grid barrier.
-//   4. Its 16 columns of y from all k+1 slots.
-// Slot j < k is the token's j-th expert, slot k the shared expert.
-constexpr int kFdRows = 16;  // intermediate rows per gate/up item
-constexpr int kFdCols = 16;  // output columns per down group
+//      selection), then starts its item's copies: gate/up codes, scales and
+//      biases by bulk copy in four sub-items of 8 rows (one mbarrier each);
+//      the down matrix's 32-code column block (16 bytes of each of its D
+//      rows) by 2-D tensor copies of 64 rows; the scale and bias words of
+//      the block's group for this thread's output columns into registers.
+//   4. Gate/up dot products as the sub-items land: warps 4s .. 4s + 3 (one
+//      per scheduler) take sub-item s, warp 4s + q its rows 2q and 2q + 1,
+//      gate and up (four dot products sharing each load of x); h =
+//      bf16(silu(g) * u); the down partials of output columns d =
+//      threadIdx.x + 512 c; red.add into the accumulator.
+//   5. The last CTA to finish (counted on the barrier's counter) converts the
+//      accumulator to bf16 y.
+// The accumulator's fp32 additions land in arrival order, as in the grouped
+// GEMM's combine: results agree up to the summation order.
+constexpr int kFdRows = 32;     // intermediate rows per item: one 32-code chunk of a down row
+constexpr int kFdSubRows = 8;   // rows per sub-item (one mbarrier)
+constexpr int kFdSubs = kFdRows / kFdSubRows;
 constexpr int kFdWarps = 16;
-
-constexpr int kFdRouterRows = 2;  // router rows (experts) per CTA
+constexpr int kFdCopies = 6;        // bulk copies per sub-item: gate codes, up codes, four scale/bias rows
+constexpr int kFdRouterRows = 2;    // router rows (experts) per CTA
+constexpr int kFdColsPerThread = 4;  // output columns per thread in the down step, 512 apart
+constexpr int kFdDownBox = 64;       // down rows per tensor copy (one lane each)
+static_assert(kFdWarps == 4 * kFdSubs && kFdSubRows == 8, "four warps per sub-item, two rows per warp");
+static_assert(kFdRows == 32, "h of an item is one warp's lanes and one 32-code chunk of a down row");
+static_assert(kFdCopies * kFdSubs <= 32, "one lane per bulk copy");
+static_assert(kFdColsPerThread * kFdWarps * 32 == 32 * kFdDownBox, "one lane per tensor copy of the down columns");
 
 struct FusedSmem {
-  size_t xs4, xsum, xraw, wr, item[2], down, dsc, dbi, hs4, hsum, red, total;
-  size_t item_codes, item_sb;  // bytes of one matrix's codes / scales of an item
-  __host__ __device__ FusedSmem(int D, int I, int k) {
-    const size_t S = size_t(k) + 1;
-    item_codes = size_t(kFdRows) * D / 2;
-    item_sb = size_t(kFdRows) * (D / 64) * 2;
-    xs4 = 64;  // bytes 0..63: four mbarriers, abort flag, grid-barrier result
+  size_t xs4, xsum, xraw, wr, item, dcodes, gu, hv, total;
+  size_t sub_codes, sub_sb, sub_bytes;  // per sub-item: one matrix's codes, one scale or bias row set, all
+  __host__ __device__ explicit FusedSmem(int D) {
+    sub_codes = size_t(kFdSubRows) * D / 2;
+    sub_sb = size_t(kFdSubRows) * (D / 64) * 2;
+    sub_bytes = 2 * sub_codes + 4 * sub_sb;
+    xs4 = 64;  // bytes 0..63: six mbarriers, abort flag, grid-barrier result, last-CTA flag
     xsum = xs4 + size_t(D) * 4;
     xraw = (xsum + size_t(D / 32) * 4 + 15) & ~size_t(15);  // the token row as bf16
     wr = (xraw + size_t(D) * 2 + 127) & ~size_t(127);       // router rows, fp32
-    item[0] = (wr + size_t(kFdRouterRows) * D * 4 + 127) & ~size_t(127);
-    item[1] = item[0] + 2 * item_codes + 4 * item_sb;
-    down = (item[1] + 2 * item_codes + 4 * item_sb + 127) & ~size_t(127);
-    dsc = down + S * kFdCols * (I / 2);
-    dbi = dsc + S * kFdCols * (I / 64) * 2;
-    hs4 = (dbi + S * kFdCols * (I / 64) * 2 + 15) & ~size_t(15);
-    hsum = hs4 + S * size_t(I) * 4;
-    red = hsum + S * size_t(I / 32) * 4;
-    total = red + size_t(kFdWarps * kFdCols > 512 ? kFdWarps * kFdCols : 512) * 4;  // also the E <= 512 logits
+    item = (wr + size_t(kFdRouterRows) * D * 4 + 127) & ~size_t(127);
+    dcodes = (item + kFdSubs * sub_bytes + 127) & ~size_t(127);  // the down column block: [D][16 bytes]
+    gu = dcodes + size_t(D) * 16;         // the item's gate and up dot products, [2][kFdRows] fp32
+    hv = gu + 2 * kFdRows * 4;        // the item's h as fp32 [kFdRows], then their sum
+    total = hv + (kFdRows + 4) * 4;
   }
 };
 
@@ -340,10 +358,11 @@ struct FusedArgs {
   int32_t* blocks;
   int32_t* n_blocks;
   uint16_t* h;  // [k+1][I]: slot-major for the one token
+  float* y_acc;
   uint16_t* y;
   WsHeader* hdr;
   int D, E, k, I;
-  int n_items, n_groups;
+  int n_items;
 };
 
 // Grid-wide barrier of a cooperative launch: every CTA arrives once on the
@@ -353,8 +372,9 @@ struct FusedArgs {
 __device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned target, volatile int* result) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(&hdr->counter, 1u);
+    // release: the CTA's writes (ordered before this thread by the CTA
+    // barrier) are visible to every CTA that sees the arrival
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&hdr->counter) : "memory");
     const long long t0 = clock64();
     int ok = 1;
     while (true) {  // relaxed polls with a short sleep, then one acquire fence
@@ -375,97 +395,97 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned target, vol
   return *result != 0;
 }
 
-__device__ __forceinline__ void cp16(void* dst_smem, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+// Tensor maps of the down codes as [rows][I/8] 32-bit words, boxes of 4
+// words x kFdDownBox rows: every expert's matrix (rows E*D) and the shared
+// expert's (rows D).
+struct DownMaps {
+  CUtensorMap routed, shared;
+};
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
 }
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+
+__device__ __forceinline__ void red_add_f32(float* dst, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(v) : "memory");
 }
 
 template <int MPL>
-__global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArgs a) {
+__global__ void __launch_bounds__(kFdWarps * 32, 1)
+    decode_fused_kernel(FusedArgs a, const __grid_constant__ DownMaps dm) {
   extern __shared__ __align__(128) uint8_t fsm[];
   __shared__ int s_exp[kMaxGemvRows * 8 + 1];
   __shared__ float s_w[kMaxGemvRows * 8 + 1];
-  const int D = a.D, I = a.I, k = a.k, E = a.E, S = k + 1, nch = D / 32, G = D / 64, Gi = I / 64;
+  const int D = a.D, I = a.I, k = a.k, E = a.E, nch = D / 32, G = D / 64, Gi = I / 64;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const FusedSmem L(D, I, k);
-  const uint32_t bar0 = smem_u32(fsm);  // mbarriers (bulk-copied codes): item 0, item 1, down, router rows
-  const uint32_t rbar = bar0 + 24u;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(fsm + 32);
-  volatile int* gb_result = reinterpret_cast<volatile int*>(fsm + 36);
-  const int RB = I / kFdRows;  // row blocks per slot
-  const bool has_down = blockIdx.x < a.n_groups;
-  const int d0 = blockIdx.x * kFdCols;
-  const uint32_t icb = uint32_t(L.item_codes), isb = uint32_t(L.item_sb);
-  const uint32_t dcb = kFdCols * (I / 2), dsb = kFdCols * Gi * 2;
+  const FusedSmem L(D);
+  const uint32_t bar0 = smem_u32(fsm);  // mbarriers: sub-items 0..3, the router rows, the down codes
+  const uint32_t rbar = bar0 + 8u * kFdSubs, dbar = rbar + 8u;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(fsm + 48);
+  volatile int* gb_result = reinterpret_cast<volatile int*>(fsm + 52);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(fsm + 56);
+  const int RB = I / kFdRows;  // items per slot
+  const bool has_item = int(blockIdx.x) < a.n_items;
+  const int slot = blockIdx.x / RB, i0 = (blockIdx.x % RB) * kFdRows;
   int n_rt = 0;  // router rows (experts) of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
   for (int m = 0; m < kFdRouterRows; ++m) n_rt += (blockIdx.x + m * int(gridDim.x) < E);
-  auto has_item = [&](int m) { return blockIdx.x + m * int(gridDim.x) < a.n_items; };
-  auto item_slot = [&](int m) { return (blockIdx.x + m * int(gridDim.x)) / RB; };
 
-  // Item m's gate/up rows and slot j's down rows of expert e. The codes, a
-  // few large contiguous blocks, go by bulk copy (one lane each); the small
-  // scale and bias rows by cp.async from every thread of the CTA.
-  auto item_codes = [&](int m, int e, int part) {  // part 0 gate, 1 up
-    const int item = blockIdx.x + m * gridDim.x, i0 = (item % RB) * kFdRows;
+  // Copy q (lane q of warp 0) of the item of expert e: sub-item q / 6, part
+  // q % 6 = gate codes, up codes, gate scales, gate biases, up scales, up
+  // biases of the sub-item's 8 rows, each a contiguous block.
+  auto item_copy = [&](int q, int e) {
+    const int sub = q / kFdCopies, part = q % kFdCopies;
     const bool sh = (e == E);
-    const moe_qmatrix mq = part == 0 ? (sh ? a.s_gate : a.gate) : (sh ? a.s_up : a.up);
-    const size_t row0 = size_t(sh ? 0 : e) * I + i0;
-    bulk_g2s(bar0 + uint32_t(m == 0 ? L.item[0] : L.item[1]) + part * icb, mq.codes + row0 * (D / 8), icb,
-             bar0 + 8u * m);
+    const moe_qmatrix& mq = part == 0 || part == 2 || part == 3 ? (sh ? a.s_gate : a.gate) : (sh ? a.s_up : a.up);
+    const size_t row0 = size_t(sh ? 0 : e) * I + i0 + sub * kFdSubRows;
+    const uint32_t dst = bar0 + uint32_t(L.item + sub * L.sub_bytes), bar = bar0 + 8u * sub;
+    if (part < 2)
+      bulk_g2s(dst + part * uint32_t(L.sub_codes), mq.codes + row0 * (D / 8), uint32_t(L.sub_codes), bar);
+    else
+      bulk_g2s(dst + uint32_t(2 * L.sub_codes + (part - 2) * L.sub_sb), ((part & 1) ? mq.biases : mq.scales) + row0 * G,
+               uint32_t(L.sub_sb), bar);
   };
-  // Item m's four small rows (gate scales, gate biases, up scales, up
-  // biases), isb bytes each, as 16-byte pieces p = 0 .. 4 * isb / 16 - 1:
-  // each thread issues the pieces p = first, first + blockDim.x, ...
-  auto item_small = [&](int m, int e, int first) {
-    const int item = blockIdx.x + m * gridDim.x, i0 = (item % RB) * kFdRows;
+  // The item's copies for expert e: warp 0 the gate/up sub-items, warp 1 the
+  // down column block (lane l: rows 64 l .. 64 l + 63); every thread loads
+  // the aligned 32-bit word holding the scale (and the bias) of the block's
+  // group for its down columns d = threadIdx.x + c * blockDim.x. Element
+  // (row, g) is number row * Gi + g of its array; the word is number (that
+  // >> 1) from the 16-byte-aligned base, so it never crosses the end of the
+  // array (D is even, so every array holds an even number of elements).
+  uint32_t dsc[kFdColsPerThread], dbi[kFdColsPerThread];
+  auto item_start = [&](int e) {
     const bool sh = (e == E);
-    const moe_qmatrix mg = sh ? a.s_gate : a.gate, mu = sh ? a.s_up : a.up;
-    const size_t row0 = size_t(sh ? 0 : e) * I + i0;
-    uint8_t* dst = fsm + (m == 0 ? L.item[0] : L.item[1]) + 2 * icb;
-    const int per = int(isb / 16);
-    for (int p = first; p < 4 * per; p += blockDim.x) {
-      const int r = p / per, o = (p % per) * 16;
-      const moe_qmatrix& mq = r < 2 ? mg : mu;
-      const uint16_t* src = ((r & 1) ? mq.biases : mq.scales) + row0 * G;
-      cp16(dst + r * isb + o, reinterpret_cast<const uint8_t*>(src) + o);
-    }
-  };
-  auto down_codes = [&](int j, int e) {
-    const bool sh = (e == E);
-    const moe_qmatrix mq = sh ? a.s_down : a.down;
-    const size_t row0 = size_t(sh ? 0 : e) * D + d0;
-    bulk_g2s(bar0 + uint32_t(L.down) + j * dcb, mq.codes + row0 * (I / 8), dcb, bar0 + 16u);
-  };
-  // The down slots' scale and bias rows, dsb bytes each, as 16-byte pieces
-  // q = 0 .. S * 2 * dsb / 16 - 1 (slot, then scales / biases), spread over
-  // all threads like the items' pieces
-  auto down_small = [&](int first) {
-    const int per = int(dsb / 16);
-    for (int q = first; q < S * 2 * per; q += blockDim.x) {
-      const int j = q / (2 * per), r = (q / per) & 1, o = (q % per) * 16;
-      const int e = s_exp[j];
-      const bool sh = (e == E);
-      const moe_qmatrix mq = sh ? a.s_down : a.down;
-      const size_t row0 = size_t(sh ? 0 : e) * D + d0;
-      const uint16_t* src = (r ? mq.biases : mq.scales) + row0 * Gi;
-      cp16(fsm + (r ? L.dbi : L.dsc) + j * dsb + o, reinterpret_cast<const uint8_t*>(src) + o);
+    if (warp == 0 && lane < kFdCopies * kFdSubs) item_copy(lane, e);
+    if (warp == 1 && lane * kFdDownBox < D)
+      tma_2d(bar0 + uint32_t(L.dcodes) + lane * kFdDownBox * 16, sh ? &dm.shared : &dm.routed, i0 / 8,
+             (sh ? 0 : e) * D + lane * kFdDownBox, dbar);
+    const moe_qmatrix& md = sh ? a.s_down : a.down;
+    const size_t r0 = size_t(sh ? 0 : e) * D;
+#pragma unroll
+    for (int c = 0; c < kFdColsPerThread; ++c) {
+      const int d = threadIdx.x + c * blockDim.x;
+      if (d < D) {
+        const size_t el = (r0 + d) * Gi + i0 / 64;
+        dsc[c] = __ldg(reinterpret_cast<const uint32_t*>(md.scales) + (el >> 1));
+        dbi[c] = __ldg(reinterpret_cast<const uint32_t*>(md.biases) + (el >> 1));
+      }
     }
   };
 
-  // --- start: barriers and byte counts; bulk copies of the router rows.
+  // --- entry: barriers and byte counts; copies that need no routing
   if (warp == 0) {
     if (lane == 0) {
       *abort_flag = 0;
-      for (int i = 0; i < 4; ++i) mbar_init(bar0 + 8u * i, 1);
+      for (int i = 0; i < kFdSubs + 2; ++i) mbar_init(bar0 + 8u * i, 1);
       mbar_init_fence();
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
-        if (has_item(m)) mbar_arrive_tx(bar0 + 8u * m, 2 * icb);
-      if (has_down) mbar_arrive_tx(bar0 + 16u, uint32_t(S) * dcb);
+      if (has_item) {
+        for (int sub = 0; sub < kFdSubs; ++sub) mbar_arrive_tx(bar0 + 8u * sub, uint32_t(L.sub_bytes));
+        mbar_arrive_tx(dbar, uint32_t(D) * 16);
+      }
       if (n_rt) mbar_arrive_tx(rbar, uint32_t(n_rt) * D * 4);
     }
     __syncwarp();
@@ -482,6 +502,9 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
     xraw4[q] = v;
     stage_bf16x8(xs4, nch, q, v);
   }
+  // the accumulator starts at zero; the grid barrier orders this before any red.add
+  for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < D / 4; q += gridDim.x * blockDim.x)
+    reinterpret_cast<float4*>(a.y_acc)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (threadIdx.x == 0) {
     s_exp[k] = E;  // slot k: the shared expert
     s_w[k] = 1.f;
@@ -503,8 +526,7 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
   if (n_rt && warp == kFdWarps - 1) mbar_wait(rbar, 0, abort_flag, a.hdr, kWaitLimit, true);  // landed before any exit
   const bool gb1 = grid_barrier(a.hdr, gridDim.x, gb_result);
 
-  // --- top-k (every CTA, the same selection), then the routed experts' copies:
-  // group 2 item 0, group 3 item 1, group 4 the down rows
+  // --- top-k (every CTA, the same selection), then the routed item's copies
   if (warp == 0) {
     int myi = 0;
     float myw = 0.f;
@@ -521,134 +543,88 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
         a.topk_w[lane] = myw;
       }
     }
-    __syncwarp();
-    // bulk copies of the codes, the shared expert's (slot k) included: they
-    // are issued only now, since copies landing during the top-k slow it down.
-    // Lanes 0..3 take the two items' gate and up, lanes 4..31 the down slots.
-    if (lane < 4) {
-      const int m = lane >> 1;
-      if (has_item(m)) item_codes(m, s_exp[item_slot(m)], lane & 1);
-    } else if (has_down) {
-      for (int j = lane - 4; j < S; j += 28) down_codes(j, s_exp[j]);
-    }
   }
   __syncthreads();
-  // groups 0, 1, 2: the scales and biases (small rows, by cp.async) of item 0,
-  // item 1 and the down slots, a few 16-byte pieces per thread (item 1's
-  // pieces start half a CTA further, so other threads take them)
-#pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    if (has_item(m)) item_small(m, s_exp[item_slot(m)], (threadIdx.x + m * (blockDim.x / 2)) % blockDim.x);
-    cp_commit();
-  }
-  if (has_down) down_small(threadIdx.x);
-  cp_commit();
+  if (has_item) item_start(s_exp[slot]);
 
-  // --- gate/up: warp w takes row w of each item
-  const bool ok = gb1;
+  // --- gate/up: warps 4s .. 4s + 3 take sub-item s; warp 4s + q its rows
+  // 2q and 2q + 1, gate and up: dot products j = 2 * row + matrix
+  float* gu = reinterpret_cast<float*>(fsm + L.gu);
+  float* hv = reinterpret_cast<float*>(fsm + L.hv);
+  bool item_ok = has_item && gb1;
+  if (has_item) {
+    const int sub = warp >> 2, r0 = 2 * (warp & 3);
+    // every copy is waited for (draining), so none is in flight at exit;
+    // warp 15 also waits for the down block
+    if (!mbar_wait(bar0 + 8u * sub, 0, abort_flag, a.hdr, kWaitLimit, true)) {
+      item_ok = false;
+    } else {
+      const uint8_t* base = fsm + L.item + sub * L.sub_bytes;
+      const uint16_t* sb = reinterpret_cast<const uint16_t*>(base + 2 * L.sub_codes);  // [4][kFdSubRows][G]
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int c = lane; c < nch; c += 32) {
+        float4 xv[8];
 #pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    if (m == 0)
-      cp_wait<2>();  // group 0: item 0's scales and biases
-    else
-      cp_wait<1>();  // group 1: item 1's
-    __syncthreads();
-    if (!has_item(m)) continue;
-    if (!mbar_wait(bar0 + 8u * m, 0, abort_flag, a.hdr, kWaitLimit, true)) continue;
-    const int item = blockIdx.x + m * gridDim.x;
-    const int slot = item / RB, i0 = (item % RB) * kFdRows;
-    const uint8_t* base = fsm + L.item[m];
-    const uint8_t* cg = base;
-    const uint8_t* cu = base + L.item_codes;
-    const uint16_t* sg = reinterpret_cast<const uint16_t*>(base + 2 * L.item_codes);
-    const uint16_t* bg = sg + kFdRows * G;
-    const uint16_t* su = bg + kFdRows * G;
-    const uint16_t* bu = su + kFdRows * G;
-    constexpr int kRowsPerWarp = kFdRows / kFdWarps;
-    float gacc[kRowsPerWarp], uacc[kRowsPerWarp];
+        for (int jq = 0; jq < 8; ++jq) xv[jq] = xs4[jq * nch + c];
+        const float sx = xsum[c];
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) gacc[i] = uacc[i] = 0.f;
-    for (int c = lane; c < nch; c += 32) {
-      float4 xv[8];
-#pragma unroll
-      for (int jq = 0; jq < 8; ++jq) xv[jq] = xs4[jq * nch + c];
-      const float sx = xsum[c];
-#pragma unroll
-      for (int i = 0; i < kRowsPerWarp; ++i) {
-        const int rr = warp + kFdWarps * i;
-        const uint4 wg = reinterpret_cast<const uint4*>(cg + size_t(rr) * D / 2)[c];
-        const uint4 wu = reinterpret_cast<const uint4*>(cu + size_t(rr) * D / 2)[c];
-        const int gi = rr * G + c / 2;
-        gacc[i] += chunk_dot_r(wg, xv, sx, sg[gi], bg[gi]);
-        uacc[i] += chunk_dot_r(wu, xv, sx, su[gi], bu[gi]);
+        for (int j = 0; j < 4; ++j) {
+          const int r = r0 + (j >> 1), mat = j & 1;
+          const uint4 w4 = reinterpret_cast<const uint4*>(base + mat * L.sub_codes + size_t(r) * (D / 2))[c];
+          const uint16_t* srow = sb + (2 * mat) * (kFdSubRows * G) + r * G;  // scales; the biases follow
+          acc[j] += chunk_dot_r(w4, xv, sx, srow[c / 2], srow[kFdSubRows * G + c / 2]);
+        }
       }
-    }
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
 #pragma unroll
       for (int off = 16; off >= 1; off >>= 1) {
-        gacc[i] += __shfl_xor_sync(0xffffffffu, gacc[i], off);
-        uacc[i] += __shfl_xor_sync(0xffffffffu, uacc[i], off);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
       }
-      if (lane == 0) a.h[size_t(slot) * I + i0 + warp + kFdWarps * i] = f32_to_bf16(silu_mul(gacc[i], uacc[i]));
+      if (lane < 4) {
+        float v = acc[0];
+#pragma unroll
+        for (int j = 1; j < 4; ++j)
+          if (lane == j) v = acc[j];
+        gu[(lane & 1) * kFdRows + sub * kFdSubRows + r0 + (lane >> 1)] = v;
+      }
+    }
+  }
+  if (has_item && warp == kFdWarps - 1 && !mbar_wait(dbar, 0, abort_flag, a.hdr, kWaitLimit, true)) item_ok = false;
+  if (!item_ok && has_item) *abort_flag = 1;
+  __syncthreads();
+  item_ok = has_item && gb1 && !*abort_flag;
+  // h of the item's 32 rows (lane i: row i0 + i), rounded to bf16, and their sum
+  if (item_ok && warp == 0) {
+    const uint16_t hb = f32_to_bf16(silu_mul(gu[lane], gu[kFdRows + lane]));
+    const float h = bf16_to_f32(hb);
+    hv[lane] = h;
+    float hs = h;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) hs += __shfl_xor_sync(0xffffffffu, hs, off);
+    if (lane == 0) hv[kFdRows] = hs;
+    a.h[size_t(slot) * I + i0 + lane] = hb;
+  }
+  __syncthreads();
+  // --- down: this thread's output columns from the item's 32 rows
+  if (item_ok) {
+    float4 hx[8];
+#pragma unroll
+    for (int jq = 0; jq < 8; ++jq) hx[jq] = reinterpret_cast<const float4*>(hv)[jq];
+    const float hs = hv[kFdRows], wj = s_w[slot];
+    const uint4* dc = reinterpret_cast<const uint4*>(fsm + L.dcodes);
+#pragma unroll
+    for (int c = 0; c < kFdColsPerThread; ++c) {
+      const int d = threadIdx.x + c * blockDim.x;
+      if (d < D) {
+        // the element's half of the loaded word (the expert's first row is
+        // even: D is even)
+        const int sh16 = 16 * ((d * Gi + i0 / 64) & 1);
+        const uint16_t sc = uint16_t(dsc[c] >> sh16), bi = uint16_t(dbi[c] >> sh16);
+        red_add_f32(a.y_acc + d, wj * chunk_dot_r(dc[d], hx, hs, sc, bi));
+      }
     }
   }
 
-  // every CTA's h rows are written: the down projection may read them
-  const bool gb2 = grid_barrier(a.hdr, 2 * gridDim.x, gb_result);
-  cp_wait<0>();  // group 2: the down scales and biases; no cp.async is left in flight
-  if (!has_down) return;
-  if (!mbar_wait(bar0 + 16u, 0, abort_flag, a.hdr, kWaitLimit, true) || !ok || !gb2) return;
-  float4* hs4 = reinterpret_cast<float4*>(fsm + L.hs4);
-  float* hsum = reinterpret_cast<float*>(fsm + L.hsum);
-  const int nchi = I / 32;
-  for (int q = threadIdx.x; q < S * (I / 8); q += blockDim.x) {
-    const int j = q / (I / 8), q8 = q % (I / 8);
-    stage_bf16x8(hs4 + size_t(j) * 8 * nchi, nchi, q8, __ldcg(reinterpret_cast<const uint4*>(a.h + size_t(j) * I) + q8));
-  }
-  __syncthreads();
-  chunk_sums(hs4, hsum, S, nchi);
-  __syncthreads();
-  const uint8_t* codes = fsm + L.down;
-  const uint16_t* sc = reinterpret_cast<const uint16_t*>(fsm + L.dsc);
-  const uint16_t* bi = reinterpret_cast<const uint16_t*>(fsm + L.dbi);
-  // unit = (item it, column quarter q): 4 dot products. Lane l of warp w
-  // takes quarter q = l / 8 and items 8w + l % 8 (+ 8 * warps per round), so
-  // the 8 lanes of one quarter read 128 contiguous bytes of one row.
-  const int q = (lane >> 3) & 3;
-  float part[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int it = 8 * warp + (lane & 7); it < S * nchi; it += 8 * kFdWarps) {
-    const int j = it / nchi, c = it % nchi;
-    float4 xv[8];
-    const float4* xr = hs4 + size_t(j) * 8 * nchi;
-#pragma unroll
-    for (int jq = 0; jq < 8; ++jq) xv[jq] = xr[jq * nchi + c];
-    const float sx = hsum[j * nchi + c], wj = s_w[j];
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      const int rowi = j * kFdCols + 4 * q + cc;
-      const uint4 w4 = reinterpret_cast<const uint4*>(codes + size_t(rowi) * (I / 2))[c];
-      const int gi = rowi * Gi + c / 2;
-      part[cc] += wj * chunk_dot_r(w4, xv, sx, sc[gi], bi[gi]);
-    }
-  }
-  float* red = reinterpret_cast<float*>(fsm + L.red);  // [kFdWarps][kFdCols]
-#pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-#pragma unroll
-    for (int off = 4; off >= 1; off >>= 1) part[cc] += __shfl_xor_sync(0xffffffffu, part[cc], off);
-  }
-  if ((lane & 7) == 0) {
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) red[warp * kFdCols + 4 * q + cc] = part[cc];
-  }
-  __syncthreads();
-  if (threadIdx.x < kFdCols) {
-    float yv = 0.f;
-#pragma unroll
-    for (int w = 0; w < kFdWarps; ++w) yv += red[w * kFdCols + threadIdx.x];
-    a.y[d0 + threadIdx.x] = f32_to_bf16(yv);
-  }
   // CTA 0: the routing tables for inspection (one token: each selected
   // expert holds one row; the permutation orders the slots by expert)
   if (blockIdx.x == 0) {
@@ -676,6 +652,28 @@ __global__ void __launch_bounds__(kFdWarps * 32, 1) decode_fused_kernel(FusedArg
       a.blocks[3 * k + 1] = k;
       a.blocks[3 * k + 2] = 1;
       *a.n_blocks = k + 1;
+    }
+  }
+
+  // --- the last CTA to arrive (2 * gridDim.x arrivals on the counter, the
+  // barrier's included) converts the accumulator. The CTA barrier orders the
+  // CTA's red.adds before thread 0's arrival, whose release makes them
+  // visible to the CTA that acquires the final count; that CTA's threads read
+  // after its own CTA barrier.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned before;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(before) : "l"(&a.hdr->counter) : "memory");
+    *last_flag = before == 2u * gridDim.x - 1u;
+  }
+  __syncthreads();
+  if (*last_flag) {
+    for (int q = threadIdx.x; q < D / 4; q += blockDim.x) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(a.y_acc) + q);
+      uint2 o;
+      o.x = uint32_t(f32_to_bf16(v.x)) | (uint32_t(f32_to_bf16(v.y)) << 16);
+      o.y = uint32_t(f32_to_bf16(v.z)) | (uint32_t(f32_to_bf16(v.w)) << 16);
+      reinterpret_cast<uint2*>(a.y)[q] = o;
     }
   }
 }
@@ -709,7 +707,7 @@ cudaError_t gemv(const Ctx& c) {
 namespace {
 
 struct FusedPlan {
-  int grid = 0, n_items = 0, n_groups = 0, mpl = 0;
+  int grid = 0, n_items = 0, mpl = 0;
   size_t smem = 0;
 };
 
@@ -718,14 +716,14 @@ struct FusedPlan {
 // all CTAs co-resident).
 FusedPlan fused_plan_uncached(const Ctx& c) {
   FusedPlan p;
-  if (c.T != 1 || c.I % kFdRows != 0 || c.D % kFdCols != 0 || c.E > 512 || c.k + 1 > kMaxGemvRows * 8 + 1)
+  if (c.T != 1 || c.I % 64 != 0 || c.D % kFdDownBox != 0 || c.D > kFdColsPerThread * kFdWarps * 32 ||
+      c.E > 512 || c.k + 1 > kMaxGemvRows * 8 + 1 || !tmap_encoder_available())
     return p;
   p.mpl = (c.E + 31) / 32 <= 8 ? 8 : 16;
-  p.smem = FusedSmem(c.D, c.I, c.k).total;
+  p.smem = FusedSmem(c.D).total;
   if (p.smem > 227 * 1024) return p;
   p.n_items = (c.k + 1) * (c.I / kFdRows);
-  p.n_groups = c.D / kFdCols;
-  const int grid = std::max(std::max(p.n_groups, (p.n_items + 1) / 2), (c.E + kFdRouterRows - 1) / kFdRouterRows);
+  const int grid = std::max(p.n_items, (c.E + kFdRouterRows - 1) / kFdRouterRows);
   int dev = 0, coop = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop ||
@@ -759,6 +757,37 @@ FusedPlan fused_plan(const Ctx& c) {
   return p;
 }
 
+// The down codes' tensor maps for this layer's weights, encoded once per
+// weight pointers and shape.
+bool down_maps(const Ctx& c, DownMaps* out) {
+  struct Entry {
+    const void* routed;
+    const void* shared;
+    int E, D, I;
+    DownMaps m;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  const moe_weights* w = c.w;
+  std::lock_guard<std::mutex> lk(mu);
+  for (const Entry& e : cache)
+    if (e.routed == w->down.codes && e.shared == w->s_down.codes && e.E == c.E && e.D == c.D && e.I == c.I) {
+      *out = e.m;
+      return true;
+    }
+  Entry e{w->down.codes, w->s_down.codes, c.E, c.D, c.I, DownMaps{}};
+  const auto U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
+  const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
+  const auto NOL2 = CU_TENSOR_MAP_L2_PROMOTION_NONE;
+  if (!make_tmap_2d(&e.m.routed, U32, 4, w->down.codes, uint64_t(c.E) * c.D, c.I / 8, 4, kFdDownBox, NOSW, NOL2) ||
+      !make_tmap_2d(&e.m.shared, U32, 4, w->s_down.codes, c.D, c.I / 8, 4, kFdDownBox, NOSW, NOL2))
+    return false;
+  if (cache.size() >= 16) cache.erase(cache.begin());
+  cache.push_back(e);
+  *out = e.m;
+  return true;
+}
+
 }  // namespace
 
 bool decode_fused_supported(const Ctx& c) { return fused_plan(c).grid > 0; }
@@ -767,17 +796,19 @@ cudaError_t decode_fused(const Ctx& c) {
   const FusedPlan p = fused_plan(c);
   if (p.grid == 0) return cudaErrorInvalidValue;
   const moe_weights* w = c.w;
-  FusedArgs a{c.x,         w->gate,        w->up,    w->down,     w->s_gate, w->s_up, w->s_down,
-              w->router_w,  w->router_bias, c.logits, c.topk_idx,  c.topk_w,  c.count, c.off,
-              c.perm,       c.inv,          c.blocks, c.n_blocks,  c.h,       c.y,     c.hdr,
-              c.D,          c.E,            c.k,      c.I,         p.n_items, p.n_groups};
+  FusedArgs a{c.x,        w->gate,        w->up,    w->down,    w->s_gate,   w->s_up, w->s_down,
+              w->router_w, w->router_bias, c.logits, c.topk_idx, c.topk_w,    c.count, c.off,
+              c.perm,      c.inv,          c.blocks, c.n_blocks, c.h,         c.y_acc, c.y,
+              c.hdr,       c.D,            c.E,      c.k,        c.I,         p.n_items};
   // the grid-barrier counter starts at zero; on the call's first pass the
   // status does too (later passes keep what earlier ones recorded)
   static_assert(offsetof(WsHeader, counter) == 8, "status, detail, counter");
   cudaError_t err = c.first_pass ? cudaMemsetAsync(c.hdr, 0, 12, c.stream)
                                  : cudaMemsetAsync(&c.hdr->counter, 0, 4, c.stream);
   if (err != cudaSuccess) return err;
-  void* args[] = {&a};
+  DownMaps dm;
+  if (!down_maps(c, &dm)) return cudaErrorInvalidValue;
+  void* args[] = {&a, &dm};
   const void* f = p.mpl == 8 ? reinterpret_cast<const void*>(decode_fused_kernel<8>)
                              : reinterpret_cast<const void*>(decode_fused_kernel<16>);
   err = cudaLaunchCooperativeKernel(f, dim3(p.grid), dim3(kFdWarps * 32), args, p.smem, c.stream);

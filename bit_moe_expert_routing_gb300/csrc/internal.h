@@ -149,7 +149,8 @@ int num_sms();
 // 2-D TMA tensor map over a row-major [rows, cols] array (false if the
 // driver's encoder is unavailable or rejects the map).
 bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t elem, const void* ptr, uint64_t rows,
-                  uint64_t cols, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
+                  uint64_t cols, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw,
+                  CUtensorMapL2promotion l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 bool tmap_encoder_available();
 
 // Decode GEMV path (a few rows).

@@ -281,9 +281,10 @@ def test_layer_decode(path):
 @pytest.mark.parametrize("fused", [0, 1], ids=["separate", "fused"])
 @pytest.mark.parametrize("T", [1, 3, 8])
 def test_layer_decode_fused_and_separate(fused, T):
-    # a few rows on the GEMV path: the one-launch cooperative kernel (router,
-    # grid barrier, top-k, gate/up, grid barrier, down) and the separate
-    # routing + GEMV kernels, both against the oracle, with the routing tables
+    # a few rows on the GEMV path: the one-launch cooperative kernels (one
+    # token: router, grid barrier, top-k, gate/up and down per 32-row item,
+    # combine; 2..8 rows: a second grid barrier before down) and the separate
+    # routing + GEMV kernels, all against the oracle, with the routing tables
     # each leaves in its workspace
     layer, x = config("sweep") if T > 1 else config("decode")
     x = x[:T]
@@ -318,6 +319,34 @@ def test_layer_decode_fused_and_separate(fused, T):
     nb = int(g(v.n_blocks, (1,), torch.int32)[0])
     assert nb == len(tb["blocks"])
     assert np.array_equal(g(v.blocks, (v.max_blocks, 3), torch.int32)[:nb], tb["blocks"])
+
+
+@pytest.mark.parametrize("name", ["decode", "tiny"])
+def test_one_token_kernel_h_and_repeated_calls(name):
+    # The one-token kernel leaves h slot-major: row j < k for the token's j-th
+    # expert, row k for the shared expert, each the oracle's SwiGLU
+    # intermediate. Its combine adds fp32 partials in arrival order, so
+    # repeated calls agree up to the summation order, and each matches the
+    # oracle.
+    layer, x = config(name)
+    x = x[:1]
+    dl = dev_layer(name, layer)
+    ol = O.OracleLayer(layer)
+    k = layer.k
+    ys = []
+    for _ in range(4):
+        y, ws = run_forward(dl, x, moe.PATH_GEMV)
+        assert moe.moe_last_launch_count() == 1
+        ys.append(y)
+    v = dl.view(1, ws)
+    h = bf16_to_np(moe.ws_tensor(ws, v.h, (k + 1, layer.I), torch.bfloat16))
+    idx = moe.ws_tensor(ws, v.topk_idx, (1, k), torch.int32).cpu().numpy()
+    ref = np.stack([O.expert_h(ol, int(idx[0, j]), x[0]) for j in range(k)] + [O.expert_h(ol, -1, x[0])])
+    check_output(h, ref, f"{name}: one-token h")
+    want = O.forward(ol, x)
+    for y in ys:
+        check_output(y, want, f"{name}: one-token y")
+        assert np.allclose(y, ys[0], rtol=2 ** -7, atol=1e-6)
 
 
 @pytest.mark.parametrize("path", PATHS, ids=[p[0] for p in PATHS])
