@@ -296,7 +296,7 @@ moe_status moe_layer_forward_expanded(const moe_weights* w, const uint16_t* x, i
  *   host, before anything is enqueued, as for moe_layer_forward().
  *   Any T: the tokens run in consecutive passes of the largest count whose
  *   workspace fits MOE_STATIC_SCRATCH_BYTES (and no larger than the chunk
- *   size; for the D=2048, E=256, k=8, I=512 layer, 451 tokens). A layer whose
+ *   size; for the D=2048, E=256, k=8, I=512 layer, 369 tokens). A layer whose
  *   single-token workspace does not fit returns MOE_ERR_WORKSPACE and
  *   enqueues nothing.
  *   The first call on each device looks up the array's device address (with

@@ -195,3 +195,14 @@ def test_product_path_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(moe, "LIB_PATH", "/nonexistent/libmoe.so")
     with pytest.raises(RuntimeError):
         moe.lib()
+
+
+def test_static_pass_size_of_the_d2048_layer(lib):
+    # The allocation-free entry point runs passes of the largest token count
+    # whose workspace fits MOE_STATIC_SCRATCH_BYTES; include/moe.h quotes that
+    # count for the D=2048, E=256, k=8, I=512 layer.
+    w = _weights(D=2048, E=256, k=8, I=512)
+    lim = 8 << 20
+    assert moe.moe_workspace_size(w, 369) <= lim < moe.moe_workspace_size(w, 370)
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    assert "I=512 layer, 369 tokens" in text

@@ -34,6 +34,21 @@ def _built():
     moe.moe_set_option(moe.MOE_OPT_GEMM_IMPL, moe.GEMM_TENSOR_CORE)
 
 
+def _static_pass_tokens(w):
+    # the largest token count whose workspace fits the static array: the
+    # size of the entry point's passes (the workspace grows with T)
+    lim = moe_static_bytes()
+    lo, hi = 0, 1 << 16  # size(lo) fits (or lo = 0), size(hi) does not
+    assert moe.moe_workspace_size(w, hi) > lim
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if moe.moe_workspace_size(w, mid) <= lim:
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
+
 def _static_forward(dl, x):
     y = torch.empty_like(x)
     st = moe.moe_layer_forward_static(dl.w, x.data_ptr(), x.shape[0], y.data_ptr(), None)
@@ -57,10 +72,12 @@ def test_static_scratch_matches_workspace_entry_point(name, T):
 
 def test_static_scratch_runs_large_token_counts_in_passes():
     # 1000 tokens of the D=2048 layer need more scratch than the array holds
-    # (one pass fits 451), so the call runs consecutive passes of the largest
-    # count that fits; the output is the regular entry point's.
+    # (one pass fits 369 tokens), so the call runs consecutive passes of the
+    # largest count that fits; the output is the regular entry point's.
     layer, x_bits = synth.make_config("prefill512", 1000)
     dl = moe.DeviceLayer(layer)
+    n = _static_pass_tokens(dl.w)
+    assert 1 < n < 500
     assert moe.moe_workspace_size(dl.w, 1000) > moe_static_bytes()
     x = x_to_device(x_bits)
     ref = bf16_to_np(dl.forward(x))
@@ -72,10 +89,10 @@ def test_static_scratch_runs_large_token_counts_in_passes():
     assert np.isfinite(y).all()
     assert moe.moe_get_device_status_static(None) == moe.MOE_OK
     # the launch count covers every pass: the same passes through the
-    # workspace entry point (chunks of 451 tokens) launch as many kernels
+    # workspace entry point (chunks of n tokens) launch as many kernels
     old = moe.moe_get_option(moe.MOE_OPT_CHUNK_TOKENS)
     try:
-        assert moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, 451) == moe.MOE_OK
+        assert moe.moe_set_option(moe.MOE_OPT_CHUNK_TOKENS, n) == moe.MOE_OK
         dl.forward(x)
         assert moe.moe_last_launch_count() == static_launches
     finally:
@@ -84,13 +101,15 @@ def test_static_scratch_runs_large_token_counts_in_passes():
 
 
 def test_static_status_keeps_an_earlier_pass_error():
-    # 453 tokens run as a 451-token grouped-GEMM pass and a 2-token GEMV
-    # pass. The test hook makes the tensor-core epilogue of the first pass
-    # give up a bounded wait (MOE_ERR_DEVICE_TIMEOUT); the second pass has no
-    # such wait, and must not wipe the first pass's error. The next call
-    # starts afresh and is correct.
-    layer, x_bits = synth.make_config("prefill512", 453)
+    # n + 2 tokens run as an n-token grouped-GEMM pass (n the largest count
+    # that fits the array) and a 2-token GEMV pass. The test hook makes the
+    # tensor-core epilogue of the first pass give up a bounded wait
+    # (MOE_ERR_DEVICE_TIMEOUT); the second pass has no such wait, and must not
+    # wipe the first pass's error. The next call starts afresh and is correct.
+    layer, _ = synth.make_config("prefill512", 1)
     dl = moe.DeviceLayer(layer)
+    n = _static_pass_tokens(dl.w)
+    _, x_bits = synth.make_config("prefill512", n + 2)
     x = x_to_device(x_bits)
     old_rows = moe.moe_get_option(moe.MOE_OPT_GEMV_MAX_ROWS)
     assert moe.moe_set_option(moe.MOE_OPT_GEMV_MAX_ROWS, 4) == moe.MOE_OK  # the 2-token pass takes the GEMV path
