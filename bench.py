@@ -629,7 +629,8 @@ def run_decode(args, moe, synth, torch, device, stream, peaks) -> dict:
     us, us_g = 1e3 * med(ms), 1e3 * med(ms_g)
     kern = {nm: dict(ms_per_launch=t / c, launches=c) for nm, (t, c) in kt.items()}
     # the one-launch kernel that ran (one token, or 2..8 rows), else the two GEMV kernels
-    names = next(((nm,) for nm in ("decode_fused", "decode_rows") if nm in kern), ("gemv_gateup", "gemv_down"))
+    names = next(((nm,) for nm in ("decode_fused", "decode_items", "decode_rows") if nm in kern),
+                 ("gemv_gateup", "gemv_down"))
     gemv_ms = sum(kern[nm]["ms_per_launch"] for nm in names if nm in kern)
     ach = work["weight_bytes"] / (gemv_ms / 1e3) / 1e9 if gemv_ms else None
     return {"us_per_token": us_g, "us_per_token_warm": 1e3 * med(ms_w), "us_per_token_stream": us,

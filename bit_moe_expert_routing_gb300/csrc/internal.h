@@ -27,7 +27,7 @@ constexpr int kMinBlockM = 16;      // smallest block size MOE_OPT_BLOCK_M accep
 // once when the call starts, so that another thread's moe_set_option cannot
 // change a call part-way.
 struct Options {
-  int gemv_max_rows = 1;  // the measured small-row sweep: the grouped GEMM at least as fast from 2 rows
+  int gemv_max_rows = 4;  // the measured small-row sweep: the item kernel faster up to 4 rows, the grouped GEMM from 5
   int force_path = 0;
   int kernel_timing = 0;
   int gemm_impl = 0;
@@ -164,6 +164,9 @@ bool decode_fused_supported(const Ctx& c);
 // the union of the rows' experts through shared-memory rings.
 cudaError_t decode_rows(const Ctx& c);
 bool decode_rows_supported(const Ctx& c);
+// 2..8 rows as items of the union's experts, one grid barrier (D <= 2048)
+cudaError_t decode_items(const Ctx& c);
+bool decode_items_supported(const Ctx& c);
 // Router logits only, for up to 16 tokens.
 // With xperm, it also writes the paired-order copy of x; with yacc, it clears
 // the combine accumulator [T, D].

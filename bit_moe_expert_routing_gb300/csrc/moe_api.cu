@@ -176,7 +176,7 @@ void fill_view(const Ctx& c, moe_route_view* v) {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-enum class Path { DecodeFused, DecodeRows, Gemv, GemmWt, GemmTc, GemmSimt };
+enum class Path { DecodeFused, DecodeItems, DecodeRows, Gemv, GemmWt, GemmTc, GemmSimt };
 
 // Chooses the expert path for this call and the block-map row count it
 // consumes: 192 tokens per block for the tensor-core GEMM with weights in
@@ -188,6 +188,8 @@ Path plan(Ctx& c) {
   Path p;
   if (path == 1 && o.decode_fused && c.T == 1 && decode_fused_supported(c))
     p = Path::DecodeFused;
+  else if (path == 1 && o.decode_fused && c.T > 1 && decode_items_supported(c))
+    p = Path::DecodeItems;
   else if (path == 1 && o.decode_fused && c.T > 1 && decode_rows_supported(c))
     p = Path::DecodeRows;
   else if (path == 1 && gemv_supported(c))
@@ -307,9 +309,11 @@ static moe_status forward_pass(const moe_weights* w, const uint16_t* x, int T, u
   }
   if (path == Path::GemmWt) c.xperm = c.xperm_area;  // the router writes the paired-order x it gathers
   timing_begin(c);
-  if (path == Path::DecodeFused || path == Path::DecodeRows) {  // routing included
+  if (path == Path::DecodeFused || path == Path::DecodeItems || path == Path::DecodeRows) {  // routing included
     if (wait_x(c) != cudaSuccess) return MOE_ERR_CUDA;
-    return cuda_status(path == Path::DecodeFused ? decode_fused(c) : decode_rows(c));
+    return cuda_status(path == Path::DecodeFused   ? decode_fused(c)
+                       : path == Path::DecodeItems ? decode_items(c)
+                                                   : decode_rows(c));
   }
   cudaError_t err = route(c, path == Path::Gemv ? nullptr : &c.yacc_zeroed);
   if (err != cudaSuccess) return MOE_ERR_CUDA;

@@ -118,11 +118,10 @@ typedef struct {
 
 /* Options (process-wide). */
 typedef enum {
-  MOE_OPT_GEMV_MAX_ROWS = 1, /* T <= this runs the decode GEMV path (0..8; default 1:
-                                on the D=2048, E=256, k=8, I=512 layer the grouped
-                                GEMM measured at least as fast as the 2..8-row GEMV
-                                kernel at 2, 3, 4, 5 and 8 rows; one row keeps the
-                                one-token kernel) */
+  MOE_OPT_GEMV_MAX_ROWS = 1, /* T <= this runs the decode GEMV path (0..8; default 4:
+                                on the D=2048, E=256, k=8, I=512 layer the one-launch
+                                item kernel measured faster than the grouped GEMM at
+                                2, 3 and 4 rows, and slower at 5 and 8) */
   MOE_OPT_FORCE_PATH = 2,    /* 0 auto by row count, 1 GEMV, 2 grouped GEMM */
   MOE_OPT_KERNEL_TIMING = 3, /* 1: record CUDA events around each kernel of
                                 the next forwards (read with moe_kernel_times) */

@@ -667,10 +667,8 @@ def test_host_buffers_entry_point_matches_device_entry_point(path):
     r = moe.moe_layer_forward_host(dl.w, xh.data_ptr(), 5, yh.data_ptr(), ws.data_ptr(), ws.numel(), None)
     assert r == moe.MOE_OK
     y_host = synth.bf16_bits_to_f32(yh.numpy().view(np.uint16)).astype(np.float64)
-    if path == moe.PATH_GEMV:  # deterministic: bitwise equal
-        assert np.array_equal(y_host, y_dev)
-    else:  # fp32 atomics in the combine: equal up to summation order
-        assert np.allclose(y_host, y_dev, rtol=2 ** -7, atol=1e-6)
+    # both paths combine with fp32 atomic adds: equal up to the summation order
+    assert np.allclose(y_host, y_dev, rtol=2 ** -7, atol=1e-6)
     check_output(y_host, O.forward(O.OracleLayer(layer), x), "host entry point")
 
 
@@ -768,12 +766,22 @@ def test_device_status_survives_later_passes():
     check_output(y, O.forward(O.OracleLayer(layer), x), "after a timeout in an earlier pass")
 
 
-def test_gemv_path_is_deterministic():
+def test_gemv_paths_repeat():
+    # The one-launch row kernel adds fp32 partials into the accumulator in
+    # arrival order: repeated calls agree up to the summation order. The
+    # separate GEMV kernels reduce in a fixed order: bit for bit.
     layer, x = config("sweep")
     dl = dev_layer("sweep", layer)
     a, _ = run_forward(dl, x[:3], moe.PATH_GEMV)
     b, _ = run_forward(dl, x[:3], moe.PATH_GEMV)
-    assert np.array_equal(a, b)
+    assert np.allclose(a, b, rtol=2 ** -7, atol=1e-6)
+    assert moe.moe_set_option(moe.MOE_OPT_DECODE_FUSED, 0) == moe.MOE_OK
+    try:
+        c, _ = run_forward(dl, x[:3], moe.PATH_GEMV)
+        d, _ = run_forward(dl, x[:3], moe.PATH_GEMV)
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_DECODE_FUSED, 1)
+    assert np.array_equal(c, d)
 
 
 def test_kernel_timing_and_launch_count():
