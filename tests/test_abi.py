@@ -206,3 +206,10 @@ def test_static_pass_size_of_the_d2048_layer(lib):
     assert moe.moe_workspace_size(w, 369) <= lim < moe.moe_workspace_size(w, 370)
     text = open(os.path.join(ROOT, "include", "moe.h")).read()
     assert "I=512 layer, 369 tokens" in text
+
+
+def test_row_switch_default_matches_the_header(lib):
+    # include/moe.h documents the measured default of MOE_OPT_GEMV_MAX_ROWS
+    assert moe.moe_get_option(moe.MOE_OPT_GEMV_MAX_ROWS) == 4
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    assert "T <= this runs the decode GEMV path (0..8; default 4" in text
