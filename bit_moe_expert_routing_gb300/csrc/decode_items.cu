@@ -20,25 +20,25 @@
 //      in the permuted order (expert-major, rows ascending), then the shared
 //      expert's pairs. CTA 0 writes the routing tables.
 //   4. Work units n = blockIdx.x, + gridDim.x, ...: a unit is an item and a
-//      group of at most two of its expert's pairs, so that an expert many rows
-//      selected is spread over several CTAs (which read its weights from L2
-//      side by side); the shared expert's units come first. Per unit: gate/up
-//      codes, scales and
-//      biases in four 8-row sub-items (bulk copies, one mbarrier each), the
-//      down column block (2-D tensor copies of 64 rows), the scale and bias
-//      words of each thread's output columns (loads into registers). Warps
-//      4s..4s+3 take sub-item s: rows 2q, 2q+1 of warp 4s+q, gate and up, for
-//      every pair of the item's expert. Once a sub-item's data has been read,
-//      the next item's gate/up copies start; once the down block has been
-//      read, the next item's down copies.
+//      group of at most two of its expert's pairs, so that an expert that many
+//      rows selected is spread over several CTAs (which read its weights from
+//      L2 side by side); the shared expert's units come first. Per unit:
+//      gate/up codes, scales and biases in four 8-row sub-items (bulk copies,
+//      one mbarrier each), the down column block (2-D tensor copies of 64
+//      rows), the scale and bias words of each thread's output columns (loads
+//      into registers). Warps 4s..4s+3 take sub-item s: rows 2q, 2q+1 of warp
+//      4s+q, gate and up, for each pair of the unit. Once every sub-item has
+//      been read, the next unit's gate/up copies start; once the down block
+//      has been read, its down copies.
 //   5. The last CTA to arrive on the counter converts the accumulator to
 //      bf16 y.
 // The accumulator's fp32 additions land in arrival order, as in the grouped
 // GEMM's combine: results agree up to the summation order.
 //
 // Every wait is bounded: an expired wait records MOE_ERR_DEVICE_TIMEOUT in the
-// workspace status word and the CTA skips its remaining items, but still
-// arrives on the counter; no copy of a later item is started after it.
+// workspace status word and the CTA skips its remaining units, but still
+// arrives on the counter; no copy of a later unit is started after it, and
+// copies already started are waited for (bounded) before the CTA exits.
 #include <algorithm>
 #include <cstddef>
 #include <mutex>
